@@ -1,0 +1,126 @@
+"""CPU oracle for the speculative-decoding verification sampler.
+
+TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only the test suite, the smoke check and
+the benchmark's CPU-baseline leg may import this package.  The oracle is plain
+C++ in double precision (``specverify_oracle.cpp``); this module compiles it
+with the host compiler and calls it through ctypes.  It shares no code with the
+CUDA library.
+
+Rule followed: "Decodificación Especulativa y EAGLE" (Phase 10 - Lesson 25),
+sections "La Regla de Exactitud" and "Caso codicioso"; the n+1 bound from
+"Accelerating Sonar through speculation", section "Decodificación especulativa".
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "specverify_oracle.cpp")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+# near-tie / condition flags (bitmask per request)
+TIE_ACCEPT = 1       # |u - p/q| < 1e-4 at an evaluated position
+TIE_CDF = 2          # the final draw's u*W lies within 1e-4*W of a bucket edge
+ILL_RESIDUAL = 4     # the final draw came from a residual holding < 1% of the mass
+RES_FALLBACK = 8     # residual mass exactly 0: the replacement was drawn from p
+BAD_INPUT = 16       # the request was rejected as invalid
+NEAR_TIE_MASK = TIE_ACCEPT | TIE_CDF | ILL_RESIDUAL | RES_FALLBACK
+
+ROW_INFO = 10        # doubles per row in row_stats()
+
+DTYPES = {"f32": 0, "bf16": 1}
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/liboracle.so`` (host compiler only)."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["g++", "-O2", "-std=c++17", "-shared", "-fPIC", "-pthread", _SRC, "-o", tmp]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            vp, i32p, f32p = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p
+            lib.oracle_verify_sample.argtypes = [vp, vp, ctypes.c_int, i32p, i32p, f32p, f32p, f32p,
+                                                 ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                 i32p, i32p, i32p, ctypes.c_int]
+            lib.oracle_verify_sample.restype = ctypes.c_int
+            lib.oracle_row_stats.argtypes = [vp, vp, ctypes.c_int, i32p, i32p, f32p, f32p, f32p,
+                                             ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, ctypes.c_int]
+            lib.oracle_row_stats.restype = ctypes.c_int
+            lib.oracle_version.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _prep(inp):
+    dt = inp["dtype"]
+    want = np.uint16 if dt == "bf16" else np.float32
+    tgt = np.ascontiguousarray(inp["target"], dtype=want)
+    drf = None if inp.get("draft") is None else np.ascontiguousarray(inp["draft"], dtype=want)
+    toks = np.ascontiguousarray(inp["draft_tokens"], dtype=np.int32)
+    dl = None if inp.get("draft_len") is None else np.ascontiguousarray(inp["draft_len"], dtype=np.int32)
+    temp = np.ascontiguousarray(inp["temperature"], dtype=np.float32)
+    uni = np.ascontiguousarray(inp["uniforms"], dtype=np.float32)
+    ur = np.ascontiguousarray(inp["uniforms_resample"], dtype=np.float32)
+    B, K, V = int(inp["B"]), int(inp["K"]), int(inp["V"])
+    assert tgt.size == B * (K + 1) * V, "target logits must be [B, K+1, V]"
+    assert drf is None or drf.size == B * K * V, "draft logits must be [B, K, V]"
+    assert toks.size == B * K and temp.size == B and uni.size == B * (K + 1) and ur.size == B
+    return tgt, drf, DTYPES[dt], toks, dl, temp, uni, ur, B, K, V
+
+
+def verify_sample(inp, nthreads: int = 1):
+    """Run the rule on host arrays.
+
+    ``inp`` holds numpy arrays ``target`` [B,K+1,V], ``draft`` [B,K,V] (bf16 as
+    raw uint16, or float32), ``draft_tokens`` [B,K], ``draft_len`` [B] (or None),
+    ``temperature`` [B], ``uniforms`` [B,K+1], ``uniforms_resample`` [B], plus
+    ``dtype`` ("f32"/"bf16") and B, K, V.  Returns (accepted_len [B],
+    out_tokens [B,K+1], flags [B]).
+    """
+    lib = _load()
+    tgt, drf, dt, toks, dl, temp, uni, ur, B, K, V = _prep(inp)
+    acc = np.empty(B, np.int32)
+    out = np.empty((B, K + 1), np.int32)
+    flags = np.empty(B, np.int32)
+    rc = lib.oracle_verify_sample(_ptr(tgt), _ptr(drf), dt, _ptr(toks), _ptr(dl), _ptr(temp),
+                                  _ptr(uni), _ptr(ur), B, K, V, _ptr(acc), _ptr(out), _ptr(flags),
+                                  int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_verify_sample rejected its arguments")
+    return acc, out, flags
+
+
+def row_stats(inp, nthreads: int = 1):
+    """Per-row quantities, float64 array [B, K+1, 10]:
+    zmax_p, S_p, log p(x_t), zmax_q, S_q, log q(x_t), W, candidate token,
+    CDF near-tie flag, accept-test near-tie flag (NaN where a row is unused)."""
+    lib = _load()
+    tgt, drf, dt, toks, dl, temp, uni, ur, B, K, V = _prep(inp)
+    info = np.empty((B, K + 1, ROW_INFO), np.float64)
+    rc = lib.oracle_row_stats(_ptr(tgt), _ptr(drf), dt, _ptr(toks), _ptr(dl), _ptr(temp),
+                              _ptr(uni), _ptr(ur), B, K, V, _ptr(info), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_row_stats rejected its arguments")
+    return info

@@ -1,0 +1,389 @@
+// Plain CPU oracle for the speculative-decoding verification sampler.
+//
+// TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only the test suite, the smoke check
+// and the benchmark's CPU-baseline leg may build, load or call this file.  It
+// shares no code, header, table or constant with the CUDA library: it is a
+// slow, double-precision restatement of the rule, written to be checked by eye
+// against the pages.
+//
+// Sources (page title, section):
+//   [SD]  "Decodificación Especulativa y EAGLE" (Phase 10 - Lesson 25),
+//         sections "El Concepto", "La Regla de Exactitud", "Caso codicioso",
+//         "Aceleración Esperada".
+//   [SON] "Accelerating Sonar through speculation", section
+//         "Decodificación especulativa" (n drafted -> at most n+1 emitted).
+//
+// Readings of points the pages leave open (the same list is kept in the
+// design notes):
+//   * u_t = uniforms[b,t] drives the accept test at position t; the bonus draw
+//     (every draft accepted) uses uniforms[b,n_b]; the replacement draw at a
+//     rejected position uses uniforms_resample[b].  One final draw per request.
+//   * The accept test is the strict "u < p(x)/q(x)", evaluated as
+//     log u + log q(x) < log p(x).  q(x)=0 with p(x)>0 accepts; p(x)=0 rejects.
+//   * T = 0 selects the greedy rule on the raw target logits; the draft logits
+//     are not read.  The same T divides both target and draft logits.
+//   * argmax ties resolve to the lowest index.
+//   * Inverse CDF: the token is the smallest i with w_i > 0 and C_i > u*W,
+//     C_i = w_0 + ... + w_i.  If rounding leaves no such i, the last i with
+//     w_i > 0 is taken.  A zero-weight token is never emitted.
+//   * If the residual mass W is exactly 0 at a rejected position (possible only
+//     through rounding), the replacement is drawn from p itself with the same
+//     uniform.
+//   * Rows after a request's draft length are never read.
+//   * out_tokens holds the j accepted drafts, then the final token, then -1.
+//
+// Everything is computed in IEEE double.  bf16 logits are widened exactly.
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <limits>
+#include <thread>
+#include <vector>
+
+namespace {
+
+constexpr int kF32 = 0;
+constexpr int kBF16 = 1;
+
+// near-tie / condition flags reported per request
+constexpr int kTieAccept = 1;     // |u - p/q| < 1e-4 at an evaluated position
+constexpr int kTieCdf = 2;        // u*W within 1e-4*W of a CDF bucket edge
+constexpr int kIllResidual = 4;   // final draw from a residual holding < 1% of the mass
+constexpr int kResFallback = 8;   // residual mass exactly 0: drawn from p instead
+constexpr int kBadInput = 16;     // request rejected as invalid
+
+constexpr double kTieBand = 1e-4;
+constexpr double kIllResidualMass = 1e-2;
+
+double widen(const void* base, int dtype, size_t idx) {
+  if (dtype == kF32) return static_cast<double>(static_cast<const float*>(base)[idx]);
+  uint32_t bits = static_cast<uint32_t>(static_cast<const uint16_t*>(base)[idx]) << 16;
+  float f;
+  std::memcpy(&f, &bits, sizeof f);
+  return static_cast<double>(f);
+}
+
+// One row of V logits, widened to double.
+void load_row(const void* base, int dtype, size_t row, int V, std::vector<double>& z) {
+  z.resize(V);
+  const size_t off = row * static_cast<size_t>(V);
+  for (int i = 0; i < V; ++i) z[i] = widen(base, dtype, off + i);
+}
+
+// Neumaier's compensated summation (Neumaier 1974), used for every long sum.
+struct CompSum {
+  double s = 0.0, c = 0.0;
+  void add(double x) {
+    double t = s + x;
+    if (std::fabs(s) >= std::fabs(x)) c += (s - t) + x; else c += (x - t) + s;
+    s = t;
+  }
+  double value() const { return s + c; }
+};
+
+// Temperature softmax of one row: p_i = exp((z_i - zmax)/T) / S,
+// S = sum_i exp((z_i - zmax)/T).  Returns false for a row with no finite
+// maximum (all -inf, +inf or NaN): the distribution is undefined there.
+bool softmax_T(const std::vector<double>& z, double T, std::vector<double>& p,
+               double& zmax, double& S) {
+  const int V = static_cast<int>(z.size());
+  zmax = -std::numeric_limits<double>::infinity();
+  for (int i = 0; i < V; ++i) if (z[i] > zmax) zmax = z[i];
+  if (!std::isfinite(zmax)) return false;
+  p.resize(V);
+  CompSum acc;
+  for (int i = 0; i < V; ++i) {
+    p[i] = std::exp((z[i] - zmax) / T);
+    acc.add(p[i]);
+  }
+  S = acc.value();
+  for (int i = 0; i < V; ++i) p[i] /= S;
+  return true;
+}
+
+// Greedy rule: index of the largest raw logit, lowest index on ties.
+int argmax_lowest(const std::vector<double>& z) {
+  int best = 0;
+  for (int i = 1; i < static_cast<int>(z.size()); ++i)
+    if (z[i] > z[best]) best = i;
+  return best;
+}
+
+// Inverse-CDF draw from non-negative weights w with total W and uniform u.
+// Sets *tie when u*W lies within kTieBand*W of either edge of the chosen
+// bucket.  Returns -1 only when every weight is zero.
+int inverse_cdf(const std::vector<double>& w, double W, double u, bool* tie) {
+  const double target = u * W;
+  CompSum cum;
+  int last_pos = -1;
+  double last_lo = 0.0, last_hi = 0.0;
+  for (int i = 0; i < static_cast<int>(w.size()); ++i) {
+    if (!(w[i] > 0.0)) continue;
+    const double lo = cum.value();
+    cum.add(w[i]);
+    const double hi = cum.value();
+    last_pos = i; last_lo = lo; last_hi = hi;
+    if (hi > target) {
+      *tie = std::fabs(target - lo) < kTieBand * W || std::fabs(target - hi) < kTieBand * W;
+      return i;
+    }
+  }
+  if (last_pos >= 0)
+    *tie = std::fabs(target - last_lo) < kTieBand * W || std::fabs(target - last_hi) < kTieBand * W;
+  return last_pos;
+}
+
+double comp_total(const std::vector<double>& w) {
+  CompSum acc;
+  for (double x : w) acc.add(x);
+  return acc.value();
+}
+
+struct Args {
+  const void* target;
+  const void* draft;
+  int dtype;
+  const int32_t* draft_tokens;
+  const int32_t* draft_len;
+  const float* temperature;
+  const float* uniforms;
+  const float* uniforms_resample;
+  int B, K, V;
+  int32_t* accepted_len;
+  int32_t* out_tokens;
+  int32_t* flags;
+  double* row_info;   // [B, K+1, kRowInfo] or null
+};
+
+constexpr int kRowInfo = 10;
+
+// Checks the per-request inputs the rule depends on; fills n on success.
+bool request_valid(const Args& a, int b, int* n_out) {
+  const int n = a.draft_len ? a.draft_len[b] : a.K;
+  if (n < 1 || n > a.K) return false;
+  const double T = a.temperature[b];
+  if (!(T >= 0.0) || !std::isfinite(T)) return false;
+  if (T > 0.0 && a.draft == nullptr) return false;
+  for (int t = 0; t < n; ++t) {
+    const int x = a.draft_tokens[static_cast<size_t>(b) * a.K + t];
+    if (x < 0 || x >= a.V) return false;
+  }
+  for (int t = 0; t <= n; ++t) {
+    const double u = a.uniforms[static_cast<size_t>(b) * (a.K + 1) + t];
+    if (!(u >= 0.0 && u < 1.0)) return false;
+  }
+  const double ur = a.uniforms_resample[b];
+  if (!(ur >= 0.0 && ur < 1.0)) return false;
+  *n_out = n;
+  return true;
+}
+
+void write_outputs(const Args& a, int b, int j, const std::vector<int>& tokens, int flags) {
+  a.accepted_len[b] = j;
+  int32_t* out = a.out_tokens + static_cast<size_t>(b) * (a.K + 1);
+  for (int t = 0; t <= a.K; ++t) out[t] = t < static_cast<int>(tokens.size()) ? tokens[t] : -1;
+  if (a.flags) a.flags[b] = flags;
+}
+
+// One request, following the rule in the order the pages give it.
+void verify_request(const Args& a, int b, std::vector<double>& zp, std::vector<double>& zq,
+                    std::vector<double>& p, std::vector<double>& q, std::vector<double>& w) {
+  int n = 0;
+  if (!request_valid(a, b, &n)) {
+    write_outputs(a, b, -1, {}, kBadInput);
+    return;
+  }
+  const double T = a.temperature[b];
+  const int32_t* x = a.draft_tokens + static_cast<size_t>(b) * a.K;
+  const float* u = a.uniforms + static_cast<size_t>(b) * (a.K + 1);
+  const size_t trow0 = static_cast<size_t>(b) * (a.K + 1);
+  const size_t drow0 = static_cast<size_t>(b) * a.K;
+  std::vector<int> tokens;
+  int flags = 0;
+
+  if (T == 0.0) {
+    // Greedy case: accept while argmax(p) equals the draft; at the first
+    // mismatch (or after the last draft) emit argmax(p) and stop.
+    for (int t = 0; t <= n; ++t) {
+      load_row(a.target, a.dtype, trow0 + t, a.V, zp);
+      const int g = argmax_lowest(zp);
+      if (t < n && g == x[t]) { tokens.push_back(x[t]); continue; }
+      tokens.push_back(g);
+      write_outputs(a, b, t, tokens, flags);
+      return;
+    }
+  }
+
+  double zmax_p, S_p, zmax_q, S_q;
+  for (int t = 0; t < n; ++t) {
+    load_row(a.target, a.dtype, trow0 + t, a.V, zp);
+    load_row(a.draft, a.dtype, drow0 + t, a.V, zq);
+    if (!softmax_T(zp, T, p, zmax_p, S_p) || !softmax_T(zq, T, q, zmax_q, S_q)) {
+      write_outputs(a, b, -1, {}, kBadInput);
+      return;
+    }
+    // log p(x_t), log q(x_t) straight from the logits: no underflow.
+    const double logp = (zp[x[t]] - zmax_p) / T - std::log(S_p);
+    const double logq = (zq[x[t]] - zmax_q) / T - std::log(S_q);
+    const double ut = u[t];
+    const double ratio = std::exp(logp - logq);
+    if (std::fabs(ut - ratio) < kTieBand) flags |= kTieAccept;
+    if (std::log(ut) + logq < logp) {          // r < p(x)/q(x): accept x_t
+      tokens.push_back(x[t]);
+      continue;
+    }
+    // Rejected: replacement ~ (p - q)+ / ||(p - q)+||_1, then stop.
+    w.resize(a.V);
+    for (int i = 0; i < a.V; ++i) w[i] = std::max(p[i] - q[i], 0.0);
+    double W = comp_total(w);
+    if (W < kIllResidualMass) flags |= kIllResidual;
+    if (!(W > 0.0)) {
+      flags |= kResFallback;
+      w = p;
+      W = comp_total(w);
+    }
+    bool tie = false;
+    const int tok = inverse_cdf(w, W, a.uniforms_resample[b], &tie);
+    if (tie) flags |= kTieCdf;
+    tokens.push_back(tok);
+    write_outputs(a, b, t, tokens, flags);
+    return;
+  }
+  // Every draft accepted: bonus token from p at position n.
+  load_row(a.target, a.dtype, trow0 + n, a.V, zp);
+  if (!softmax_T(zp, T, p, zmax_p, S_p)) {
+    write_outputs(a, b, -1, {}, kBadInput);
+    return;
+  }
+  bool tie = false;
+  const int tok = inverse_cdf(p, comp_total(p), u[n], &tie);
+  if (tie) flags |= kTieCdf;
+  tokens.push_back(tok);
+  write_outputs(a, b, n, tokens, flags);
+}
+
+// Per-row quantities for parity of probabilities: every row a request needs
+// (target rows t <= n, draft rows t < n when T > 0), not only those before
+// the first rejection.  Layout per row (double):
+//   0 zmax_p  1 S_p  2 log p(x_t)  3 zmax_q  4 S_q  5 log q(x_t)
+//   6 W (residual mass sum (p-q)+ at t < n; sum p at t = n)
+//   7 the final-draw token this row would give (residual with the resample
+//     uniform at t < n, bonus with u[n] at t = n; greedy: argmax)
+//   8 CDF near-tie flag of that draw   9 accept-test near-tie flag
+// Rows a request does not need hold NaN.
+void row_stats_request(const Args& a, int b, std::vector<double>& zp, std::vector<double>& zq,
+                       std::vector<double>& p, std::vector<double>& q, std::vector<double>& w) {
+  const double nan = std::numeric_limits<double>::quiet_NaN();
+  double* info = a.row_info + static_cast<size_t>(b) * (a.K + 1) * kRowInfo;
+  for (int i = 0; i < (a.K + 1) * kRowInfo; ++i) info[i] = nan;
+  int n = 0;
+  if (!request_valid(a, b, &n)) return;
+  const double T = a.temperature[b];
+  const int32_t* x = a.draft_tokens + static_cast<size_t>(b) * a.K;
+  const float* u = a.uniforms + static_cast<size_t>(b) * (a.K + 1);
+  const size_t trow0 = static_cast<size_t>(b) * (a.K + 1);
+  const size_t drow0 = static_cast<size_t>(b) * a.K;
+  for (int t = 0; t <= n; ++t) {
+    double* r = info + t * kRowInfo;
+    load_row(a.target, a.dtype, trow0 + t, a.V, zp);
+    if (T == 0.0) {
+      const int g = argmax_lowest(zp);
+      r[0] = zp[g];
+      r[7] = g;
+      r[8] = 0.0;
+      r[9] = 0.0;
+      continue;
+    }
+    double zmax_p, S_p, zmax_q, S_q;
+    if (!softmax_T(zp, T, p, zmax_p, S_p)) continue;
+    r[0] = zmax_p;
+    r[1] = S_p;
+    if (t == n) {
+      bool tie = false;
+      const double W = comp_total(p);
+      r[6] = W;
+      r[7] = inverse_cdf(p, W, u[n], &tie);
+      r[8] = tie ? 1.0 : 0.0;
+      continue;
+    }
+    load_row(a.draft, a.dtype, drow0 + t, a.V, zq);
+    if (!softmax_T(zq, T, q, zmax_q, S_q)) continue;
+    r[2] = (zp[x[t]] - zmax_p) / T - std::log(S_p);
+    r[3] = zmax_q;
+    r[4] = S_q;
+    r[5] = (zq[x[t]] - zmax_q) / T - std::log(S_q);
+    r[9] = std::fabs(u[t] - std::exp(r[2] - r[5])) < kTieBand ? 1.0 : 0.0;
+    w.resize(a.V);
+    for (int i = 0; i < a.V; ++i) w[i] = std::max(p[i] - q[i], 0.0);
+    double W = comp_total(w);
+    r[6] = W;
+    bool tie = false;
+    if (!(W > 0.0)) { w = p; W = comp_total(w); }
+    r[7] = inverse_cdf(w, W, a.uniforms_resample[b], &tie);
+    r[8] = tie ? 1.0 : 0.0;
+  }
+}
+
+template <class F>
+void for_requests(const Args& a, int nthreads, F body) {
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > a.B) nthreads = a.B;
+  auto work = [&](int lo, int hi) {
+    std::vector<double> zp, zq, p, q, w;
+    for (int b = lo; b < hi; ++b) body(a, b, zp, zq, p, q, w);
+  };
+  if (nthreads == 1) { work(0, a.B); return; }
+  std::vector<std::thread> pool;
+  for (int k = 0; k < nthreads; ++k) {
+    const int lo = static_cast<int>(static_cast<long long>(a.B) * k / nthreads);
+    const int hi = static_cast<int>(static_cast<long long>(a.B) * (k + 1) / nthreads);
+    pool.emplace_back(work, lo, hi);
+  }
+  for (auto& th : pool) th.join();
+}
+
+bool shape_ok(int B, int K, int V) { return B >= 1 && K >= 1 && V >= 1; }
+
+}  // namespace
+
+extern "C" {
+
+int oracle_version(void) { return 1; }
+
+// Verification sampler on host buffers.  Logits: target [B,K+1,V],
+// draft [B,K,V] (may be null when every temperature is 0), dtype 0=f32 1=bf16
+// (bf16 passed as raw uint16).  flags [B] (may be null) receives the near-tie
+// bitmask.  Returns 0 on success, 1 on a bad shape or null pointer.
+int oracle_verify_sample(const void* target_logits, const void* draft_logits, int dtype,
+                         const int32_t* draft_tokens, const int32_t* draft_len,
+                         const float* temperature, const float* uniforms,
+                         const float* uniforms_resample, int B, int K, int V,
+                         int32_t* accepted_len, int32_t* out_tokens, int32_t* flags,
+                         int nthreads) {
+  if (!shape_ok(B, K, V) || !target_logits || !draft_tokens || !temperature || !uniforms ||
+      !uniforms_resample || !accepted_len || !out_tokens || (dtype != kF32 && dtype != kBF16))
+    return 1;
+  Args a{target_logits, draft_logits, dtype, draft_tokens, draft_len, temperature, uniforms,
+         uniforms_resample, B, K, V, accepted_len, out_tokens, flags, nullptr};
+  for_requests(a, nthreads, verify_request);
+  return 0;
+}
+
+// Per-row probabilities and per-row final-draw candidates (layout above).
+int oracle_row_stats(const void* target_logits, const void* draft_logits, int dtype,
+                     const int32_t* draft_tokens, const int32_t* draft_len,
+                     const float* temperature, const float* uniforms,
+                     const float* uniforms_resample, int B, int K, int V, double* row_info,
+                     int nthreads) {
+  if (!shape_ok(B, K, V) || !target_logits || !draft_tokens || !temperature || !uniforms ||
+      !uniforms_resample || !row_info || (dtype != kF32 && dtype != kBF16))
+    return 1;
+  Args a{target_logits, draft_logits, dtype, draft_tokens, draft_len, temperature, uniforms,
+         uniforms_resample, B, K, V, nullptr, nullptr, nullptr, row_info};
+  for_requests(a, nthreads, row_stats_request);
+  return 0;
+}
+
+}  // extern "C"
