@@ -159,6 +159,16 @@ struct Args {
 
 constexpr int kRowInfo = 10;
 
+bool row_has_finite_max(const void* base, int dtype, size_t row, int V) {
+  double m = -std::numeric_limits<double>::infinity();
+  const size_t off = row * static_cast<size_t>(V);
+  for (int i = 0; i < V; ++i) {
+    const double z = widen(base, dtype, off + i);
+    if (z > m) m = z;
+  }
+  return std::isfinite(m);
+}
+
 // Checks the per-request inputs the rule depends on; fills n on success.
 bool request_valid(const Args& a, int b, int* n_out) {
   const int n = a.draft_len ? a.draft_len[b] : a.K;
@@ -176,6 +186,16 @@ bool request_valid(const Args& a, int b, int* n_out) {
   }
   const double ur = a.uniforms_resample[b];
   if (!(ur >= 0.0 && ur < 1.0)) return false;
+  // A sampled request needs a finite maximum in every row it uses (target
+  // rows t <= n, draft rows t < n), whether or not the scan reaches them.
+  if (T > 0.0) {
+    for (int t = 0; t <= n; ++t)
+      if (!row_has_finite_max(a.target, a.dtype, (static_cast<size_t>(b) * (a.K + 1) + t), a.V))
+        return false;
+    for (int t = 0; t < n; ++t)
+      if (!row_has_finite_max(a.draft, a.dtype, (static_cast<size_t>(b) * a.K + t), a.V))
+        return false;
+  }
   *n_out = n;
   return true;
 }

@@ -412,3 +412,17 @@ def test_row_stats_probabilities_normalised():
             assert abs(np.exp(info[b, t, 5]) - q[x]) <= 1e-12 * q[x] + 1e-300
             assert abs(info[b, t, 6] - np.maximum(p - q, 0).sum()) < 1e-12
         assert np.all(np.isnan(info[b, n + 1:, 0]))
+
+
+def test_sampled_request_with_unusable_row_is_flagged():
+    """A sampled request whose needed rows include one without a finite
+    maximum is invalid, even if the scan would stop before that row."""
+    inp = synth.random_case(92, B=3, K=3, V=16, temperature=1.0)
+    inp["target"][1, 3, :] = -np.inf        # the bonus row of request 1
+    inp["draft"][2, 2, :] = -np.inf         # the last draft row of request 2
+    acc, out, flags = oracle.verify_sample(inp)
+    assert list((flags & oracle.BAD_INPUT) != 0) == [False, True, True]
+    # greedy requests have an argmax on any row: no flag
+    inp["temperature"][:] = 0.0
+    acc, out, flags = oracle.verify_sample(inp)
+    assert np.all(flags == 0)
