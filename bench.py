@@ -1,0 +1,499 @@
+#!/usr/bin/env python
+"""Benchmark of the speculative-decoding verification sampler on GB300.
+
+A step is one call of the sampler over one batch (every step of the rule, one
+kernel launch).  The default workload is the Llama-3-class batch: B = 32
+requests, K = 4 drafts, V = 128256, bf16 logits, T = 0.7 (synthetic, seeded).
+
+Metric: verified rows/s, rows = B*(K+1) per step, whole job (all ranks).
+Timing: W eager warm-up steps, then exactly K steps replayed from CUDA graphs,
+bracketed by a barrier and a device synchronise, timed with CUDA events on
+the launching stream, max over ranks.  Inputs rotate over enough device copies
+to exceed 3x the L2 cache, so every step streams its logits from HBM.
+
+Also reported: the roofline of the sampler kernel (algorithmic bytes per
+launch / average launch time vs the measured HBM copy bandwidth), the same
+metric end to end through the host-buffer entry point (pinned host inputs
+copied in, results copied out, every step), SM clocks sampled during the
+timed region, and the CPU oracle timed on the host cores (rank 0, N = 1).
+
+--impl reference times the CPU oracle instead (the only reference this
+sampler has), rank 0 only, on bounded samples of the same workload.
+
+Multi-GPU: requests are independent, so each rank runs its own batch (weak
+scaling, no collective on the data path).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "verify rows/s (B×(K+1) rows of V logits) and achieved HBM GB/s vs GB300 peak"
+KERNEL_SRC = os.path.join(ROOT, "speculative_decoding_verify_sample_gb300", "csrc", "specverify.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "verify_kernel_traffic.json")
+FALLBACK_HBM_GBS = 6800.0
+
+WORKLOAD_TEXT = {
+    "llama3": "Llama-3-class verify: B=32 K=4 V=128256 bf16, draft~N(0,3^2), target=draft+N(0,1), T=0.7",
+    "greedy": "greedy verify: B=256 K=4 V=128256 bf16, T=0, target argmax = draft w.p. 0.8",
+    "dsv3_mtp": "DeepSeek-V3 MTP: B=512 K=1 V=129280 bf16, 25% T=0, else T~U(0,1.2]",
+    "ragged": "long ragged: B=128 K=8 V=128256 f32, draft_len~U{1..8}, constant overlap 0.5/0.8/0.95",
+    "tiny": "tiny: B=4 K=4 V=1024 f32, T=1",
+}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="llama3", choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--seed", type=int, default=None)
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of CUDA graphs")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.steps is None:
+        args.steps = 20000 if args.impl == "ours" else 10
+    return args
+
+
+# ---------------------------------------------------------------- helpers
+
+
+def required_bytes(inp) -> int:
+    """Logit bytes the rule must read: target rows t <= n_b of every request
+    and draft rows t < n_b of every sampled request, once each."""
+    from speculative_decoding_verify_sample_gb300 import synth
+    rows_t, rows_d = synth.rows_needed(inp)
+    elt = 2 if inp["dtype"] == "bf16" else 4
+    return (rows_t + rows_d) * inp["V"] * elt
+
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, only if it was
+    taken on the current kernel source and this workload."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    entry = rec.get(workload)
+    if not entry or entry.get("source_sha256") != kernel_source_hash():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling in the background."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.samples = []
+        self.window = None
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", gpu_id], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+        except OSError:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def wait_first(self, timeout=5.0):
+        t0 = time.time()
+        while self.proc and not self.samples and time.time() - t0 < timeout:
+            time.sleep(0.02)
+
+    def start(self):
+        self.t0 = time.time()
+
+    def stop(self):
+        self.window = (self.t0, time.time())
+        time.sleep(0.12)
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.samples or self.window is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        lo, hi = self.window
+        inside = [s for t, s in self.samples if lo - 0.05 <= t <= hi + 0.05]
+        if not inside:   # a timed region shorter than the sampling period
+            inside = [min(self.samples, key=lambda ts: abs(ts[0] - (lo + hi) / 2))[1]]
+        sm, mx, reasons = [], [], set()
+        for s in inside:
+            try:
+                sm.append(float(s[0]))
+                mx.append(float(s[1]))
+            except (ValueError, IndexError):
+                continue
+            for name, val in zip(self.REASONS, s[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(inside)}
+
+
+def gpu_id_for(torch, dev) -> str:
+    try:
+        return "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:  # noqa: BLE001
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        idx = dev.index or 0
+        return vis.split(",")[idx] if vis else str(idx)
+
+
+# ---------------------------------------------------------------- distributed
+
+
+def dist_setup(torch):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(torch, world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(torch, world, value: float, device) -> float:
+    if world == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- arms
+
+
+def device_inputs(torch, inp, dev):
+    def logits(a):
+        if a is None:
+            return None
+        if inp["dtype"] == "bf16":
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(dev)
+
+    def small(a, dt):
+        return None if a is None else torch.from_numpy(np.ascontiguousarray(a, dt)).to(dev)
+
+    return dict(target=logits(inp["target"]), draft=logits(inp.get("draft")),
+                draft_tokens=small(inp["draft_tokens"], np.int32),
+                draft_len=small(inp.get("draft_len"), np.int32),
+                temperature=small(inp["temperature"], np.float32),
+                uniforms=small(inp["uniforms"], np.float32),
+                uniforms_resample=small(inp["uniforms_resample"], np.float32))
+
+
+def host_inputs(torch, d):
+    return {k: (None if v is None else v.cpu().pin_memory()) for k, v in d.items()}
+
+
+def cpu_oracle_rate(inp, budget_s=1.5, nthreads=None, max_requests=None):
+    """The oracle as it stands on the host cores: rows/s over repeated calls
+    on a bounded sample (the first m requests of the batch)."""
+    import oracle
+    nthreads = nthreads or os.cpu_count() or 1
+    B = inp["B"]
+    m = B if max_requests is None else max(1, min(B, max_requests))
+    sub = dict(inp)
+    if m < B:
+        sub["B"] = m
+        for k in ("target", "draft", "draft_tokens", "draft_len", "temperature", "uniforms",
+                  "uniforms_resample"):
+            if sub.get(k) is not None:
+                sub[k] = np.ascontiguousarray(np.asarray(inp[k])[:m])
+    oracle.verify_sample(sub, nthreads=nthreads)          # untimed: build + page-in
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.verify_sample(sub, nthreads=nthreads)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s and reps >= 3:
+            break
+    rows = reps * m * (inp["K"] + 1)
+    return rows / el, nthreads, f"first {m} of {B} requests, {reps} repetitions, {el:.2f} s wall"
+
+
+def run_ours(args, torch, world, rank, local):
+    import speculative_decoding_verify_sample_gb300 as sv
+    from speculative_decoding_verify_sample_gb300 import synth
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    sv.build()
+    seed = (args.seed if args.seed is not None else synth.DEFAULT_SEED[args.workload]) + rank
+    inp = synth.make_inputs(args.workload, seed)
+    B, K, V = inp["B"], inp["K"], inp["V"]
+    rows_per_step = B * (K + 1)
+    req_bytes = required_bytes(inp)
+    d0 = device_inputs(torch, inp, dev)
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    n_copies = max(1, math.ceil(3 * l2 / max(req_bytes, 1)))
+    copies = [d0]
+    for _ in range(n_copies - 1):
+        copies.append({k: (v.clone() if v is not None and k in ("target", "draft") else v)
+                       for k, v in d0.items()})
+    ws = sv.Workspace(B, K, dev)
+    acc = torch.empty(B, dtype=torch.int32, device=dev)
+    out = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+
+    def step(i):
+        c = copies[i % n_copies]
+        sv.spec_verify_sample(c["target"], c["draft"], c["draft_tokens"], c["draft_len"],
+                              c["temperature"], c["uniforms"], c["uniforms_resample"],
+                              workspace=ws, accepted_len=acc, out_tokens=out)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    status = ws.read_status()
+    if status:
+        raise RuntimeError(f"device status {status:#x} after warm-up")
+
+    K_steps = args.steps
+    stream = torch.cuda.current_stream(dev)
+    graphs = []
+    if not args.no_graph:
+        cycle = n_copies * max(1, 64 // n_copies)
+        full, rem = divmod(K_steps, cycle)
+
+        def capture(nsteps):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for i in range(nsteps):
+                    step(i)
+            return g
+
+        g_cycle = capture(cycle) if full else None
+        g_rem = capture(rem) if rem else None
+        graphs = [g_cycle] * full + ([g_rem] if g_rem else [])
+        for g in graphs[:1]:
+            g.replay()      # one untimed replay of the captured graph
+        torch.cuda.synchronize(dev)
+
+    clocks = None
+    if not args.no_clocks:
+        clocks = ClockSampler(gpu_id_for(torch, dev))
+        clocks.wait_first()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    barrier(torch, world)
+    torch.cuda.synchronize(dev)
+    if clocks:
+        clocks.start()
+    ev0.record(stream)
+    if graphs:
+        for g in graphs:
+            g.replay()
+    else:
+        for i in range(K_steps):
+            step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    if clocks:
+        clocks.stop()
+    barrier(torch, world)
+    ms = ev0.elapsed_time(ev1)
+    ms = max_over_ranks(torch, world, ms, dev)
+    status = ws.read_status()
+    if status:
+        raise RuntimeError(f"device status {status:#x} after the timed region")
+
+    ms_per_step = ms / K_steps
+    value = rows_per_step * K_steps * world / (ms / 1e3)
+    achieved = req_bytes / (ms_per_step / 1e3) / 1e9
+    peak, peak_src = measured_hbm_peak()
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "rows/s", "n_gpus": world,
+        "steps": K_steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded; logits generated, no model weights)",
+        "config": {
+            "workload": WORKLOAD_TEXT[args.workload], "B": B, "K": K, "V": V,
+            "logits_dtype": inp["dtype"], "rows_per_step": rows_per_step,
+            "required_bytes_per_step": req_bytes,
+            "l2": f"rotating {n_copies} device copies of the logits "
+                  f"({n_copies * req_bytes / 1e6:.0f} MB read per cycle, L2 {l2 / 1e6:.0f} MB)",
+            "launch": "CUDA graphs of the step launches" if graphs else "eager launches",
+            "parallelism": f"{world} independent replica(s), requests sharded per rank"},
+        "roofline": {
+            "kernel": "verify_kernel", "bound": "hbm", "achieved": round(achieved, 1),
+            "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+            "traffic": recorded_traffic(args.workload),
+            "peak_source": f"{peak_src} HBM copy bandwidth",
+            "algorithmic_bytes_per_launch": req_bytes},
+        "gpu_launches": K_steps,
+    }
+    if clocks:
+        line["clocks"] = clocks.summary()
+
+    if not args.no_e2e:
+        line["e2e"] = e2e_rate(args, torch, sv, inp, d0, dev, ws, rows_per_step, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, cores, sample = cpu_oracle_rate(inp)
+        line["cpu_baseline"] = {"value": round(v, 1), "unit": "rows/s", "cores": cores,
+                                "kind": "oracle", "sample": sample}
+    return line
+
+
+def e2e_rate(args, torch, sv, inp, d0, dev, ws, rows_per_step, world):
+    """Same metric through the host-buffer entry point: every step copies
+    that step's inputs from pinned host memory and reads the results back."""
+    h = host_inputs(torch, d0)
+    B, K, V = inp["B"], inp["K"], inp["V"]
+    staging = sv.HostStaging(B, K, V, inp["dtype"], with_draft=h["draft"] is not None, device=dev)
+    acc = torch.empty(B, dtype=torch.int32).pin_memory()
+    out = torch.empty((B, K + 1), dtype=torch.int32).pin_memory()
+
+    def step():
+        sv.spec_verify_sample_host(h["target"], h["draft"], h["draft_tokens"], h["draft_len"],
+                                   h["temperature"], h["uniforms"], h["uniforms_resample"],
+                                   staging=staging, workspace=ws, accepted_len=acc,
+                                   out_tokens=out)
+
+    for _ in range(3):
+        step()
+    n = max(1, min(args.e2e_steps, args.steps))
+    barrier(torch, world)
+    t0 = time.perf_counter()
+    for _ in range(n):
+        step()
+    el = time.perf_counter() - t0
+    el = max_over_ranks(torch, world, el, dev)
+    h2d = sum(v.numel() * v.element_size() for v in h.values() if v is not None)
+    d2h = acc.numel() * 4 + out.numel() * 4
+    return {"value": round(rows_per_step * n * world / el, 1), "unit": "rows/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": n,
+            "path": "spec_verify_sample_host (pinned host buffers, synchronous per step)"}
+
+
+def run_reference(args, world, rank):
+    """The CPU oracle as it stands, timed on the host cores (rank 0 only)."""
+    from speculative_decoding_verify_sample_gb300 import synth
+    import oracle
+
+    if rank != 0:
+        return None
+    seed = args.seed if args.seed is not None else synth.DEFAULT_SEED[args.workload]
+    inp = synth.make_inputs(args.workload, seed)
+    B, K, V = inp["B"], inp["K"], inp["V"]
+    nthreads = os.cpu_count() or 1
+    oracle.build()
+    t0 = time.perf_counter()
+    oracle.verify_sample(inp, nthreads=nthreads)               # calibration, untimed
+    per_req = (time.perf_counter() - t0) / B
+    budget = 90.0
+    m = int(max(1, min(B, budget / max(per_req * (args.steps + args.warmup), 1e-9))))
+    sub = dict(inp, B=m)
+    for k in ("target", "draft", "draft_tokens", "draft_len", "temperature", "uniforms",
+              "uniforms_resample"):
+        if inp.get(k) is not None:
+            sub[k] = np.ascontiguousarray(np.asarray(inp[k])[:m])
+    for _ in range(args.warmup):
+        oracle.verify_sample(sub, nthreads=nthreads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.verify_sample(sub, nthreads=nthreads)
+    el = time.perf_counter() - t0
+    rows = m * (K + 1) * args.steps
+    value = rows / el
+    sample = f"first {m} of {B} requests per step"
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "rows/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el * 1e3 / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; logits generated, no model weights)",
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "B": B, "K": K, "V": V,
+                   "logits_dtype": inp["dtype"], "rows_per_step": m * (K + 1),
+                   "parallelism": "CPU oracle, rank 0 only"},
+        "cpu_baseline": {"value": round(value, 1), "unit": "rows/s", "cores": nthreads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 1), "unit": "rows/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        line = run_reference(args, world, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    import torch
+    world, rank, local = dist_setup(torch)
+    try:
+        line = run_ours(args, torch, world, rank, local)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

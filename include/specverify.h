@@ -1,0 +1,200 @@
+/*
+ * libspecverify: the verification sampler of speculative decoding on one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * What the library computes (page title, section):
+ *   "Decodificación Especulativa y EAGLE" (Phase 10 - Lesson 25),
+ *     section "El Concepto": the target scores K+1 positions in one pass; the
+ *     drafted tokens are accepted or rejected left to right; a rejection
+ *     draws a replacement and stops; if every draft is accepted a bonus token
+ *     is drawn from the target at position K+1.
+ *     section "La Regla de Exactitud": accept x_t iff r < p(x_t)/q(x_t) with
+ *     r ~ U(0,1); otherwise draw from (p - q)+ / ||(p - q)+||_1 and stop.
+ *     section "Caso codicioso": at temperature 0 accept iff argmax(p) = x_t,
+ *     otherwise emit argmax(p) and stop.
+ *   "Accelerating Sonar through speculation", section "Decodificación
+ *     especulativa": n drafted tokens yield at most n+1 emitted tokens; the
+ *     sampler's accepted lengths are what the scheduler reads back.
+ *
+ * Notation: request b in [0,B); n_b = draft_len[b] in [1,K]; T_b =
+ * temperature[b]; p_{b,t} = softmax(target_logits[b,t,:] / T_b) for t <= n_b;
+ * q_{b,t} = softmax(draft_logits[b,t,:] / T_b) for t < n_b.
+ *
+ * Readings fixed by this interface where the pages are silent:
+ *   - uniforms[b,t] (t < n_b) drives the accept test at position t;
+ *     uniforms[b,n_b] drives the bonus draw; uniforms_resample[b] drives the
+ *     replacement draw at a rejected position.  One final draw per request.
+ *   - The accept test is strict (u < p/q).  q(x) = 0 with p(x) > 0 accepts;
+ *     p(x) = 0 rejects.
+ *   - T_b = 0 selects the greedy rule on the raw target logits; the draft
+ *     logits of that request are never read.  The same T_b divides target
+ *     and draft logits.
+ *   - argmax ties resolve to the lowest index.
+ *   - Inverse CDF: the token is the smallest i with w_i > 0 and
+ *     w_0 + ... + w_i > u * sum(w).  If rounding leaves none, the last i with
+ *     w_i > 0.  A zero-weight token is never emitted.  A residual of exactly
+ *     zero mass (possible only through rounding) falls back to drawing from p
+ *     with the same uniform.
+ *   - Rows t > n_b of the target and t >= n_b of the draft are never read.
+ *   - out_tokens[b,:] = x_0 .. x_{j-1}, final token, then -1; accepted_len[b]
+ *     = j in [0, n_b].
+ *
+ * Conventions for every call:
+ *   - Ownership: every buffer is allocated and owned by the caller.  The
+ *     library allocates nothing and keeps no state between calls besides
+ *     what the caller's workspace holds.
+ *   - Asynchrony: device calls only enqueue work on `stream` and never
+ *     synchronise (except specv_read_device_status and
+ *     spec_verify_sample_host, which say so).
+ *   - Errors: problems visible on the host (null pointers, bad sizes,
+ *     misalignment, a workspace that is too small) return a status before
+ *     anything is enqueued.  Problems in the data (a draft length outside
+ *     1..K, a token outside [0,V), a negative or non-finite temperature, a
+ *     uniform outside [0,1), a sampled row without a finite maximum) are
+ *     detected on the device: the request's accepted_len becomes -1, its
+ *     out_tokens become -1, and a bit is set in the workspace's status word
+ *     (specv_read_device_status).  Nothing traps.
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* specv_stream_t;
+
+typedef enum specv_status {
+  SPECV_OK = 0,
+  SPECV_ERR_INVALID_ARG = 1,  /* null pointer, size out of range, misalignment */
+  SPECV_ERR_UNSUPPORTED = 2,  /* shape beyond the documented limits           */
+  SPECV_ERR_WORKSPACE = 3,    /* workspace or staging buffer too small         */
+  SPECV_ERR_CUDA = 4,         /* a CUDA call failed                            */
+  SPECV_ERR_BAD_INPUT = 5     /* the device flagged bad data (status word)     */
+} specv_status;
+
+typedef enum specv_dtype {
+  SPECV_F32 = 0,   /* IEEE float32 logits                          */
+  SPECV_BF16 = 1   /* bfloat16 logits (raw 16-bit storage)          */
+} specv_dtype;
+
+/* Bits of the device status word. */
+#define SPECV_DEV_BAD_DRAFT_LEN   0x01  /* draft_len[b] outside 1..K               */
+#define SPECV_DEV_BAD_TOKEN       0x02  /* draft_tokens[b,t] outside [0,V), t<n_b  */
+#define SPECV_DEV_BAD_TEMPERATURE 0x04  /* negative, NaN or infinite temperature   */
+#define SPECV_DEV_BAD_UNIFORM     0x08  /* a uniform the request uses not in [0,1) */
+#define SPECV_DEV_BAD_ROW         0x10  /* a row the request needs has no finite max */
+#define SPECV_DEV_NO_DRAFT        0x20  /* T_b > 0 but draft_logits is NULL        */
+#define SPECV_DEV_TIMEOUT         0x40  /* a bounded wait on a copy gave up        */
+
+/* Limits. */
+#define SPECV_MAX_DRAFT 16      /* K <= 16                               */
+#define SPECV_MAX_BATCH 65535   /* B <= 65535                            */
+
+/* Library version (major*10000 + minor*100 + patch). */
+int specv_version(void);
+
+/* Largest vocabulary supported for a dtype (on-chip capacity of one
+ * thread-block cluster): 786432 for bf16, 393216 for f32. */
+int specv_max_vocab(specv_dtype dtype);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* specv_status_string(specv_status status);
+
+/* Bytes of device workspace one call over B requests of up to K drafts
+ * needs: a status word, one arrival counter per request and one 8-byte
+ * record per (request, position).  Returns 0 for B or K out of range. */
+size_t specv_workspace_bytes(int B, int K);
+
+/* Zero a workspace on `stream` (cudaMemsetAsync).  Must run once before the
+ * first call that uses the workspace; every successful call leaves the
+ * counters at zero again.  workspace must be 16-byte aligned. */
+specv_status specv_workspace_init(void* workspace, size_t workspace_bytes, specv_stream_t stream);
+
+/*
+ * The verification sampler.  All pointers are device pointers.
+ *   target_logits     [B, K+1, V] of `dtype`, row-major, contiguous; the
+ *                     base must be aligned to the element size (16-byte
+ *                     alignment of every row enables bulk copies).
+ *   draft_logits      [B, K, V] of `dtype`; may be NULL when every T_b is 0
+ *                     (a request with T_b > 0 then fails with NO_DRAFT).
+ *   draft_tokens      [B, K] int32, entries t < n_b in [0, V).
+ *   draft_len         [B] int32 in 1..K, or NULL for "all K".
+ *   temperature       [B] float32, >= 0 and finite; 0 selects greedy.
+ *   uniforms          [B, K+1] float32 in [0,1).
+ *   uniforms_resample [B] float32 in [0,1).
+ *   accepted_len      [B] int32 output: j in [0, n_b], or -1 for bad data.
+ *   out_tokens        [B, K+1] int32 output: accepted drafts, the final
+ *                     token, then -1.
+ *   workspace         specv_workspace_bytes(B, K) bytes, 16-byte aligned,
+ *                     zeroed once with specv_workspace_init.  Calls that may
+ *                     run concurrently need separate workspaces.
+ * Enqueues one kernel on `stream`; no host synchronisation.
+ */
+specv_status spec_verify_sample(const void* target_logits, const void* draft_logits,
+                                specv_dtype dtype, const int32_t* draft_tokens,
+                                const int32_t* draft_len, const float* temperature,
+                                const float* uniforms, const float* uniforms_resample,
+                                int B, int K, int V, int32_t* accepted_len,
+                                int32_t* out_tokens, void* workspace, size_t workspace_bytes,
+                                specv_stream_t stream);
+
+/*
+ * Same as spec_verify_sample, and also writes per-row statistics for parity
+ * checks: row_stats [B, K+1, 8] float32 (device), for every row the request
+ * needs:
+ *   0 max_i z^p_i (raw logit)    1 S_p = sum_i exp((z^p_i - max)/T)
+ *   2 ln p(x_t)                  3 max_i z^q_i       4 S_q
+ *   5 ln q(x_t)                  6 final-draw mass (below)
+ *   7 the row's final-draw token (residual with uniforms_resample[b] at
+ *     t < n_b, bonus with uniforms[b,n_b] at t = n_b; greedy: argmax)
+ * Slot 6 is the normalised mass of the row's final-draw weights:
+ * sum_i (p_i - q_i)+ at t < n_b, sum_i p_i at t = n_b.  Unused slots and
+ * rows are left untouched.  Costs an extra on-chip pass per row.
+ */
+specv_status spec_verify_sample_debug(const void* target_logits, const void* draft_logits,
+                                      specv_dtype dtype, const int32_t* draft_tokens,
+                                      const int32_t* draft_len, const float* temperature,
+                                      const float* uniforms, const float* uniforms_resample,
+                                      int B, int K, int V, int32_t* accepted_len,
+                                      int32_t* out_tokens, void* workspace,
+                                      size_t workspace_bytes, float* row_stats,
+                                      specv_stream_t stream);
+
+/* Copy the workspace's device status word to *status (host), then clear it.
+ * Synchronises `stream`.  Returns SPECV_ERR_BAD_INPUT when the word was
+ * non-zero, SPECV_OK when it was zero. */
+specv_status specv_read_device_status(void* workspace, size_t workspace_bytes, int32_t* status,
+                                      specv_stream_t stream);
+
+/* Bytes of device staging spec_verify_sample_host needs (inputs and
+ * outputs, each padded to 256 bytes).  with_draft = 0 when draft logits are
+ * not passed. */
+size_t specv_host_staging_bytes(int B, int K, int V, specv_dtype dtype, int with_draft);
+
+/*
+ * The sampler on HOST buffers: copies each input host->device with one
+ * cudaMemcpyAsync into `staging` (device, specv_host_staging_bytes bytes,
+ * 256-byte aligned), runs spec_verify_sample, copies accepted_len and
+ * out_tokens back, and synchronises `stream` before returning.  Host buffers
+ * should be page-locked for asynchronous copies.  Same shapes and readings
+ * as spec_verify_sample; draft_len and draft_logits may be NULL as there.
+ */
+specv_status spec_verify_sample_host(const void* target_logits, const void* draft_logits,
+                                     specv_dtype dtype, const int32_t* draft_tokens,
+                                     const int32_t* draft_len, const float* temperature,
+                                     const float* uniforms, const float* uniforms_resample,
+                                     int B, int K, int V, int32_t* accepted_len,
+                                     int32_t* out_tokens, void* staging, size_t staging_bytes,
+                                     void* workspace, size_t workspace_bytes,
+                                     specv_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECVERIFY_H */

@@ -1,0 +1,212 @@
+"""GB300-native speculative-decoding verification sampler.
+
+The sampler ("Decodificación Especulativa y EAGLE", Phase 10 - Lesson 25,
+sections "La Regla de Exactitud" and "Caso codicioso") runs as hand-written
+CUDA for sm_103a behind the C ABI in include/specverify.h.  This module is the
+thin Python binding: it checks shapes and dtypes of torch tensors, passes
+their device pointers and the current CUDA stream to the library, and turns
+status codes into exceptions.  Nothing here computes any step of the rule.
+"""
+
+from __future__ import annotations
+
+from ._native import (DEV_BAD_DRAFT_LEN, DEV_BAD_ROW, DEV_BAD_TEMPERATURE, DEV_BAD_TOKEN,
+                      DEV_BAD_UNIFORM, DEV_NO_DRAFT, DEV_TIMEOUT, SPECV_BF16, SPECV_F32,
+                      SpecVerifyError, check, lib)
+from .build import build
+
+__all__ = [
+    "build", "lib", "Workspace", "HostStaging", "spec_verify_sample", "spec_verify_sample_debug",
+    "spec_verify_sample_host", "workspace_bytes", "max_vocab", "SpecVerifyError",
+    "DEV_BAD_DRAFT_LEN", "DEV_BAD_TOKEN", "DEV_BAD_TEMPERATURE", "DEV_BAD_UNIFORM",
+    "DEV_BAD_ROW", "DEV_NO_DRAFT", "DEV_TIMEOUT",
+]
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_ptr(stream, device):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dtype_code(t):
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return SPECV_BF16
+    if t.dtype == torch.float32:
+        return SPECV_F32
+    raise TypeError(f"logits must be bfloat16 or float32, got {t.dtype}")
+
+
+def workspace_bytes(B: int, K: int) -> int:
+    return int(lib().specv_workspace_bytes(B, K))
+
+
+def max_vocab(dtype) -> int:
+    torch = _torch()
+    code = SPECV_BF16 if dtype in (torch.bfloat16, "bf16") else SPECV_F32
+    return int(lib().specv_max_vocab(code))
+
+
+class Workspace:
+    """Device workspace for calls over up to B requests of up to K drafts,
+    zeroed once on creation (the library keeps it zeroed between calls)."""
+
+    def __init__(self, B: int, K: int, device=None, stream=None):
+        torch = _torch()
+        n = workspace_bytes(B, K)
+        if n == 0:
+            raise ValueError(f"unsupported workspace shape B={B} K={K}")
+        self.B, self.K, self.nbytes = B, K, n
+        self.tensor = torch.empty(n, dtype=torch.uint8, device=device)
+        check("specv_workspace_init",
+              lib().specv_workspace_init(self.tensor.data_ptr(), n,
+                                         _stream_ptr(stream, self.tensor.device)))
+
+    def read_status(self, stream=None) -> int:
+        """Device status word (bits DEV_*); synchronises the stream and clears it."""
+        out = __import__("ctypes").c_int32(0)
+        lib().specv_read_device_status(self.tensor.data_ptr(), self.nbytes,
+                                       __import__("ctypes").byref(out),
+                                       _stream_ptr(stream, self.tensor.device))
+        return int(out.value)
+
+
+def _check_inputs(target, draft, draft_tokens, draft_len, temperature, uniforms, uniforms_resample):
+    torch = _torch()
+    if target.dim() != 3:
+        raise ValueError("target_logits must be [B, K+1, V]")
+    B, K1, V = target.shape
+    K = K1 - 1
+    if K < 1:
+        raise ValueError("target_logits needs K+1 >= 2 positions")
+    dev = target.device
+    if dev.type != "cuda":
+        raise ValueError("spec_verify_sample takes CUDA tensors (use spec_verify_sample_host)")
+
+    def need(name, t, shape, dtype):
+        if t is None:
+            return
+        if tuple(t.shape) != tuple(shape):
+            raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+        if t.dtype != dtype:
+            raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+        if t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, target_logits on {dev}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+
+    need("target_logits", target, (B, K + 1, V), target.dtype)
+    _dtype_code(target)
+    need("draft_logits", draft, (B, K, V), target.dtype)
+    need("draft_tokens", draft_tokens, (B, K), torch.int32)
+    need("draft_len", draft_len, (B,), torch.int32)
+    need("temperature", temperature, (B,), torch.float32)
+    need("uniforms", uniforms, (B, K + 1), torch.float32)
+    need("uniforms_resample", uniforms_resample, (B,), torch.float32)
+    return B, K, V
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _run(fn_name, target, draft, draft_tokens, draft_len, temperature, uniforms, uniforms_resample,
+         workspace, accepted_len, out_tokens, stream, row_stats):
+    torch = _torch()
+    B, K, V = _check_inputs(target, draft, draft_tokens, draft_len, temperature, uniforms,
+                            uniforms_resample)
+    dev = target.device
+    if accepted_len is None:
+        accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = Workspace(B, K, dev, stream)
+    args = [_ptr(target), _ptr(draft), _dtype_code(target), _ptr(draft_tokens), _ptr(draft_len),
+            _ptr(temperature), _ptr(uniforms), _ptr(uniforms_resample), B, K, V,
+            _ptr(accepted_len), _ptr(out_tokens), workspace.tensor.data_ptr(), workspace.nbytes]
+    if row_stats is not None:
+        args.append(_ptr(row_stats))
+    args.append(_stream_ptr(stream, dev))
+    check(fn_name, getattr(lib(), fn_name)(*args))
+    return accepted_len, out_tokens
+
+
+def spec_verify_sample(target_logits, draft_logits, draft_tokens, draft_len, temperature, uniforms,
+                       uniforms_resample, *, workspace=None, accepted_len=None, out_tokens=None,
+                       stream=None):
+    """Verify drafted tokens on the GPU.  Tensors on one CUDA device:
+    target_logits [B,K+1,V] bf16/f32, draft_logits [B,K,V] same dtype (or None
+    when every temperature is 0), draft_tokens [B,K] int32, draft_len [B]
+    int32 (or None = all K), temperature [B] f32 (0 = greedy), uniforms
+    [B,K+1] f32, uniforms_resample [B] f32.  Returns (accepted_len [B],
+    out_tokens [B,K+1]) int32; asynchronous on the current stream."""
+    return _run("spec_verify_sample", target_logits, draft_logits, draft_tokens, draft_len,
+                temperature, uniforms, uniforms_resample, workspace, accepted_len, out_tokens,
+                stream, None)
+
+
+def spec_verify_sample_debug(target_logits, draft_logits, draft_tokens, draft_len, temperature,
+                             uniforms, uniforms_resample, *, workspace=None, accepted_len=None,
+                             out_tokens=None, row_stats=None, stream=None):
+    """As spec_verify_sample, plus per-row statistics [B, K+1, 8] float32
+    (max_p, S_p, ln p(x), max_q, S_q, ln q(x), final-draw mass, candidate);
+    rows the request does not need are left as NaN."""
+    torch = _torch()
+    B, K1, _ = target_logits.shape
+    if row_stats is None:
+        row_stats = torch.full((B, K1, 8), float("nan"), dtype=torch.float32,
+                               device=target_logits.device)
+    acc, out = _run("spec_verify_sample_debug", target_logits, draft_logits, draft_tokens,
+                    draft_len, temperature, uniforms, uniforms_resample, workspace, accepted_len,
+                    out_tokens, stream, row_stats)
+    return acc, out, row_stats
+
+
+class HostStaging:
+    """Device staging buffer for spec_verify_sample_host."""
+
+    def __init__(self, B: int, K: int, V: int, dtype, with_draft: bool = True, device=None):
+        torch = _torch()
+        code = SPECV_BF16 if dtype in (torch.bfloat16, "bf16") else SPECV_F32
+        n = int(lib().specv_host_staging_bytes(B, K, V, code, int(with_draft)))
+        if n == 0:
+            raise ValueError("unsupported staging shape")
+        self.nbytes = n
+        self.tensor = torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def spec_verify_sample_host(target_logits, draft_logits, draft_tokens, draft_len, temperature,
+                            uniforms, uniforms_resample, *, staging, workspace, accepted_len=None,
+                            out_tokens=None, stream=None):
+    """The sampler on host (CPU, ideally pinned) tensors: the library copies
+    inputs to the device, runs, copies the outputs back and synchronises."""
+    torch = _torch()
+    if target_logits.device.type != "cpu":
+        raise ValueError("spec_verify_sample_host takes host tensors")
+    B, K1, V = target_logits.shape
+    K = K1 - 1
+    for name, t in (("target_logits", target_logits), ("draft_logits", draft_logits),
+                    ("draft_tokens", draft_tokens), ("draft_len", draft_len),
+                    ("temperature", temperature), ("uniforms", uniforms),
+                    ("uniforms_resample", uniforms_resample)):
+        if t is not None and (t.device.type != "cpu" or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous host tensor")
+    if accepted_len is None:
+        accepted_len = torch.empty(B, dtype=torch.int32).pin_memory()
+    if out_tokens is None:
+        out_tokens = torch.empty((B, K + 1), dtype=torch.int32).pin_memory()
+    dev = staging.tensor.device
+    check("spec_verify_sample_host", lib().spec_verify_sample_host(
+        _ptr(target_logits), _ptr(draft_logits), _dtype_code(target_logits), _ptr(draft_tokens),
+        _ptr(draft_len), _ptr(temperature), _ptr(uniforms), _ptr(uniforms_resample), B, K, V,
+        _ptr(accepted_len), _ptr(out_tokens), staging.tensor.data_ptr(), staging.nbytes,
+        workspace.tensor.data_ptr(), workspace.nbytes, _stream_ptr(stream, dev)))
+    return accepted_len, out_tokens

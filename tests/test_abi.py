@@ -1,0 +1,93 @@
+"""The C ABI without a GPU: the library builds, loads, exports every function
+include/specverify.h declares, and rejects bad host-side arguments before
+touching the device."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import speculative_decoding_verify_sample_gb300 as sv
+from speculative_decoding_verify_sample_gb300 import _native
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "specverify.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    sv.build()
+    return sv.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(spec\w+)\s*\(", text)))
+
+
+def test_header_declares_expected_entry_points():
+    names = declared_functions()
+    for must in ("spec_verify_sample", "spec_verify_sample_debug", "spec_verify_sample_host",
+                 "specv_workspace_bytes", "specv_workspace_init", "specv_read_device_status"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+        assert name in _native.SIGNATURES, f"binding lacks {name}"
+
+
+def test_limits_and_sizes(L):
+    assert L.specv_max_vocab(0) >= 262144
+    assert L.specv_max_vocab(1) >= 262144
+    assert L.specv_max_vocab(7) == 0
+    assert L.specv_workspace_bytes(0, 4) == 0
+    assert L.specv_workspace_bytes(4, 17) == 0
+    assert L.specv_workspace_bytes(32, 4) >= 16 + 32 * 4 + 32 * 5 * 8
+    assert L.specv_host_staging_bytes(2, 2, 100, 1, 1) >= 2 * 3 * 100 * 2 + 2 * 2 * 100 * 2
+    assert L.specv_status_string(0) == b"ok"
+
+
+FAKE = 0x10000  # a 64 KB-aligned non-null address: host checks never dereference it
+
+
+def _call(L, **over):
+    a = dict(target=FAKE, draft=FAKE, dtype=1, tokens=FAKE, dlen=FAKE, temp=FAKE, uni=FAKE,
+             ures=FAKE, B=4, K=4, V=1024, acc=FAKE, out=FAKE, ws=FAKE, wsb=1 << 20)
+    a.update(over)
+    return L.spec_verify_sample(a["target"], a["draft"], a["dtype"], a["tokens"], a["dlen"],
+                                a["temp"], a["uni"], a["ures"], a["B"], a["K"], a["V"], a["acc"],
+                                a["out"], a["ws"], a["wsb"], None)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(target=None), 1), (dict(tokens=None), 1), (dict(acc=None), 1), (dict(ws=None), 1),
+    (dict(dtype=3), 1), (dict(B=0), 1), (dict(K=0), 1), (dict(V=0), 1),
+    (dict(K=17), 2), (dict(B=70000), 2), (dict(V=786433), 2), (dict(dtype=0, V=393217), 2),
+    (dict(wsb=8), 3), (dict(target=FAKE + 1), 1), (dict(ws=FAKE + 8), 1), (dict(uni=FAKE + 2), 1),
+])
+def test_host_side_argument_errors(L, over, status):
+    assert _call(L, **over) == status
+
+
+def test_debug_entry_requires_row_stats(L):
+    rc = L.spec_verify_sample_debug(FAKE, FAKE, 1, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 4, 1024, FAKE,
+                                    FAKE, FAKE, 1 << 20, None, None)
+    assert rc == 1
+
+
+def test_host_entry_rejects_small_staging(L):
+    rc = L.spec_verify_sample_host(FAKE, FAKE, 1, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 4, 1024, FAKE,
+                                   FAKE, FAKE, 64, FAKE, 1 << 20, None)
+    assert rc == 3
+
+
+def test_binding_refuses_cpu_tensors():
+    torch = pytest.importorskip("torch")
+    t = torch.zeros(2, 3, 8)
+    with pytest.raises(ValueError):
+        sv.spec_verify_sample(t, None, torch.zeros(2, 2, dtype=torch.int32), None,
+                              torch.zeros(2), torch.zeros(2, 3), torch.zeros(2))
