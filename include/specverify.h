@@ -193,6 +193,41 @@ specv_status spec_verify_sample_host(const void* target_logits, const void* draf
                                      void* workspace, size_t workspace_bytes,
                                      specv_stream_t stream);
 
+/*
+ * The sampler without any allocation, for callers that cannot allocate
+ * device memory where they run it: plugin interfaces that hand the plugin
+ * only the tensors it declared, serving loops that forbid cudaMalloc after
+ * start-up (it can synchronise the device and fragment a fixed budget), and
+ * hosts whose device memory is owned by another allocator.  The pages have
+ * no counterpart; this is a packaging variant of spec_verify_sample.
+ *
+ * Same inputs, outputs, readings and errors as spec_verify_sample, with no
+ * workspace argument: the scratch (status word, arrival counters, per-unit
+ * records) lives in a module-scope device array of the library, sized for
+ * SPECV_NOALLOC_MAX_BATCH requests and SPECV_NOALLOC_MAX_UNITS =
+ * B*(K+1) units (about 144 KB); every GPU that loads the library holds it
+ * until the process exits.  Larger shapes return SPECV_ERR_UNSUPPORTED.
+ *   - It calls no cudaMalloc, cudaFree or allocating library routine.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - Each call zeroes the part of the array it uses (cudaMemsetAsync on
+ *     `stream`), then launches the kernel.  All calls on a device share the
+ *     one array: calls that may overlap on the GPU (different streams, or
+ *     concurrent host threads) race and must be serialised by the caller.
+ *   - The device status word is not exposed: bad data shows as
+ *     accepted_len[b] = -1 and out_tokens[b,:] = -1.
+ */
+#define SPECV_NOALLOC_MAX_BATCH 4096
+#define SPECV_NOALLOC_MAX_UNITS 16384
+
+specv_status spec_verify_sample_noalloc(const void* target_logits, const void* draft_logits,
+                                        specv_dtype dtype, const int32_t* draft_tokens,
+                                        const int32_t* draft_len, const float* temperature,
+                                        const float* uniforms, const float* uniforms_resample,
+                                        int B, int K, int V, int32_t* accepted_len,
+                                        int32_t* out_tokens, specv_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

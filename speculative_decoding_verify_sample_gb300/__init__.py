@@ -17,7 +17,7 @@ from .build import build
 
 __all__ = [
     "build", "lib", "Workspace", "HostStaging", "spec_verify_sample", "spec_verify_sample_debug",
-    "spec_verify_sample_host", "workspace_bytes", "max_vocab", "SpecVerifyError",
+    "spec_verify_sample_host", "spec_verify_sample_noalloc", "workspace_bytes", "max_vocab", "SpecVerifyError",
     "DEV_BAD_DRAFT_LEN", "DEV_BAD_TOKEN", "DEV_BAD_TEMPERATURE", "DEV_BAD_UNIFORM",
     "DEV_BAD_ROW", "DEV_NO_DRAFT", "DEV_TIMEOUT",
 ]
@@ -209,4 +209,31 @@ def spec_verify_sample_host(target_logits, draft_logits, draft_tokens, draft_len
         _ptr(draft_len), _ptr(temperature), _ptr(uniforms), _ptr(uniforms_resample), B, K, V,
         _ptr(accepted_len), _ptr(out_tokens), staging.tensor.data_ptr(), staging.nbytes,
         workspace.tensor.data_ptr(), workspace.nbytes, _stream_ptr(stream, dev)))
+    return accepted_len, out_tokens
+
+
+def spec_verify_sample_noalloc(target_logits, draft_logits, draft_tokens, draft_len, temperature,
+                               uniforms, uniforms_resample, *, accepted_len, out_tokens,
+                               stream=None):
+    """The sampler for callers that cannot allocate device memory at the call
+    site (plugin hooks handed only their declared tensors, serving loops that
+    forbid cudaMalloc after start-up, hosts whose memory another allocator
+    owns).  The caller passes preallocated outputs; the scratch is the
+    library's own fixed device array (at most 4096 requests and 16384
+    request-positions), shared by every call on the device, so calls that
+    may overlap on the GPU must be serialised.  Make the first call on a
+    device before any stream capture: it looks up the array's address."""
+    B, K, V = _check_inputs(target_logits, draft_logits, draft_tokens, draft_len, temperature,
+                            uniforms, uniforms_resample)
+    torch = _torch()
+    dev = target_logits.device
+    for name, t, shape in (("accepted_len", accepted_len, (B,)),
+                           ("out_tokens", out_tokens, (B, K + 1))):
+        if (t is None or tuple(t.shape) != shape or t.dtype != torch.int32 or t.device != dev
+                or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a preallocated int32 tensor {shape} on {dev}")
+    check("spec_verify_sample_noalloc", lib().spec_verify_sample_noalloc(
+        _ptr(target_logits), _ptr(draft_logits), _dtype_code(target_logits), _ptr(draft_tokens),
+        _ptr(draft_len), _ptr(temperature), _ptr(uniforms), _ptr(uniforms_resample), B, K, V,
+        _ptr(accepted_len), _ptr(out_tokens), _stream_ptr(stream, dev)))
     return accepted_len, out_tokens

@@ -43,7 +43,12 @@ SIGNATURES = {
     "specv_host_staging_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "spec_verify_sample_host": (_i, [_vp, _vp, _i, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _vp, _vp,
                                      _vp, _sz, _vp, _sz, _vp]),
+    "spec_verify_sample_noalloc": (_i, [_vp, _vp, _i, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _vp, _vp,
+                                        _vp]),
 }
+
+NOALLOC_MAX_BATCH = 4096
+NOALLOC_MAX_UNITS = 16384
 
 _lock = threading.Lock()
 _lib = None

@@ -853,6 +853,41 @@ specv_status launch(const void* target, const void* draft, specv_dtype dtype,
 
 size_t pad256(size_t x) { return (x + 255) / 256 * 256; }
 
+// ---------------------------------------------------------------- no-allocation scratch
+//
+// Scratch for spec_verify_sample_noalloc: the same layout as a caller's
+// workspace (status word, per-request counters, per-unit records), sized for
+// SPECV_NOALLOC_MAX_BATCH requests and SPECV_NOALLOC_MAX_UNITS units.  It is
+// a module-scope device array, so every GPU that loads this library holds it
+// until the process exits, and every call on a device shares it.
+constexpr size_t kNoAllocScratchBytes =
+    (16 + 4 * static_cast<size_t>(SPECV_NOALLOC_MAX_BATCH) + 8 * static_cast<size_t>(SPECV_NOALLOC_MAX_UNITS) +
+     255) / 256 * 256;
+
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch on the current device.  In host code
+// the symbol's name is only a host-side handle, so the address is looked up
+// once per device with cudaGetSymbolAddress (with that device current) and
+// cached.
+cudaError_t noalloc_scratch(void** out) {
+  static std::mutex mu;
+  static void* addr[64] = {nullptr};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return cudaSuccess;
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------- C ABI
@@ -997,6 +1032,27 @@ specv_status spec_verify_sample_host(const void* target_logits, const void* draf
                       cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return SPECV_ERR_CUDA;
   return cudaStreamSynchronize(s) == cudaSuccess ? SPECV_OK : SPECV_ERR_CUDA;
+}
+
+specv_status spec_verify_sample_noalloc(const void* target_logits, const void* draft_logits,
+                                        specv_dtype dtype, const int32_t* draft_tokens,
+                                        const int32_t* draft_len, const float* temperature,
+                                        const float* uniforms, const float* uniforms_resample,
+                                        int B, int K, int V, int32_t* accepted_len,
+                                        int32_t* out_tokens, specv_stream_t stream) {
+  if (B < 1 || K < 1 || K > SPECV_MAX_DRAFT) return SPECV_ERR_INVALID_ARG;
+  if (B > SPECV_NOALLOC_MAX_BATCH ||
+      static_cast<long long>(B) * (K + 1) > SPECV_NOALLOC_MAX_UNITS)
+    return SPECV_ERR_UNSUPPORTED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  void* scratch = nullptr;
+  if (noalloc_scratch(&scratch) != cudaSuccess) return SPECV_ERR_CUDA;
+  const size_t bytes = specv_workspace_bytes(B, K);
+  // The array keeps the previous call's contents: zero the status word and
+  // the arrival counters this call relies on.
+  if (cudaMemsetAsync(scratch, 0, bytes, s) != cudaSuccess) return SPECV_ERR_CUDA;
+  return launch(target_logits, draft_logits, dtype, draft_tokens, draft_len, temperature, uniforms,
+                uniforms_resample, B, K, V, accepted_len, out_tokens, scratch, bytes, nullptr, s);
 }
 
 }  // extern "C"
