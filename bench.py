@@ -376,6 +376,7 @@ def run_ours(args, torch, world, rank, local):
             "l2": f"rotating {n_copies} device copies of the logits "
                   f"({n_copies * req_bytes / 1e6:.0f} MB read per cycle, L2 {l2 / 1e6:.0f} MB)",
             "launch": "CUDA graphs of the step launches" if graphs else "eager launches",
+            "kernel_plan": sv.launch_plan(B, K, V, inp["dtype"], inp.get("draft") is not None),
             "parallelism": f"{world} independent replica(s), requests sharded per rank"},
         "roofline": {
             "kernel": "verify_kernel", "bound": "hbm", "achieved": round(achieved, 1),

@@ -193,6 +193,14 @@ specv_status spec_verify_sample_host(const void* target_logits, const void* draf
                                      void* workspace, size_t workspace_bytes,
                                      specv_stream_t stream);
 
+/* The launch shape the library picks for these sizes (diagnostics): out[0]
+ * CTAs per thread-block cluster, out[1] vocabulary elements per CTA slice,
+ * out[2] shared-memory stages per CTA, out[3] clusters launched, out[4]
+ * dynamic shared memory per CTA (bytes), out[5] threads per CTA.  Queries
+ * the current device's occupancy; launches nothing. */
+specv_status specv_launch_plan(int B, int K, int V, specv_dtype dtype, int with_draft,
+                               int32_t* out);
+
 /*
  * The sampler without any allocation, for callers that cannot allocate
  * device memory where they run it: plugin interfaces that hand the plugin

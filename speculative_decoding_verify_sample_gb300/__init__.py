@@ -17,7 +17,7 @@ from .build import build
 
 __all__ = [
     "build", "lib", "Workspace", "HostStaging", "spec_verify_sample", "spec_verify_sample_debug",
-    "spec_verify_sample_host", "spec_verify_sample_noalloc", "workspace_bytes", "max_vocab", "SpecVerifyError",
+    "spec_verify_sample_host", "spec_verify_sample_noalloc", "launch_plan", "workspace_bytes", "max_vocab", "SpecVerifyError",
     "DEV_BAD_DRAFT_LEN", "DEV_BAD_TOKEN", "DEV_BAD_TEMPERATURE", "DEV_BAD_UNIFORM",
     "DEV_BAD_ROW", "DEV_NO_DRAFT", "DEV_TIMEOUT",
 ]
@@ -46,6 +46,17 @@ def _dtype_code(t):
 
 def workspace_bytes(B: int, K: int) -> int:
     return int(lib().specv_workspace_bytes(B, K))
+
+
+def launch_plan(B: int, K: int, V: int, dtype, with_draft: bool = True) -> dict:
+    """The launch shape the library picks for these sizes (needs a GPU)."""
+    import ctypes
+    torch = _torch()
+    code = SPECV_BF16 if dtype in (torch.bfloat16, "bf16") else SPECV_F32
+    out = (ctypes.c_int32 * 6)()
+    check("specv_launch_plan", lib().specv_launch_plan(B, K, V, code, int(with_draft), out))
+    return dict(cluster=out[0], slice=out[1], stages=out[2], clusters=out[3], smem=out[4],
+                threads=out[5])
 
 
 def max_vocab(dtype) -> int:

@@ -43,6 +43,7 @@ SIGNATURES = {
     "specv_host_staging_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "spec_verify_sample_host": (_i, [_vp, _vp, _i, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _vp, _vp,
                                      _vp, _sz, _vp, _sz, _vp]),
+    "specv_launch_plan": (_i, [_i, _i, _i, _i, _i, _vp]),
     "spec_verify_sample_noalloc": (_i, [_vp, _vp, _i, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _vp, _vp,
                                         _vp]),
 }
