@@ -294,7 +294,7 @@ def run_ours(args, torch, world, rank, local):
     for _ in range(n_copies - 1):
         copies.append({k: (v.clone() if v is not None and k in ("target", "draft") else v)
                        for k, v in d0.items()})
-    ws = sv.Workspace(B, K, dev)
+    ws = sv.Workspace(B, K, V, inp["dtype"], dev)
     acc = torch.empty(B, dtype=torch.int32, device=dev)
     out = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
 

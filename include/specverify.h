@@ -98,21 +98,24 @@ typedef enum specv_dtype {
 /* Library version (major*10000 + minor*100 + patch). */
 int specv_version(void);
 
-/* Largest vocabulary supported for a dtype (on-chip capacity of one
- * thread-block cluster): 786432 for bf16, 393216 for f32. */
+/* Largest vocabulary supported for a dtype (128 chunks of 16 KB per row):
+ * 1048576 for bf16, 524288 for f32. */
 int specv_max_vocab(specv_dtype dtype);
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* specv_status_string(specv_status status);
 
-/* Bytes of device workspace one call over B requests of up to K drafts
- * needs: a status word, one arrival counter per request and one 8-byte
- * record per (request, position).  Returns 0 for B or K out of range. */
-size_t specv_workspace_bytes(int B, int K);
+/* Bytes of device workspace one call over B requests of up to K drafts of
+ * a V-entry vocabulary needs: a header (status word, tile tickets, draw
+ * queue counters, a call counter), 64 bytes of state per request, one
+ * partial per (row, 16 KB chunk), the final-draw partial sums and the draw
+ * queue.  Returns 0 for sizes out of range. */
+size_t specv_workspace_bytes(int B, int K, int V, specv_dtype dtype);
 
 /* Zero a workspace on `stream` (cudaMemsetAsync).  Must run once before the
- * first call that uses the workspace; every successful call leaves the
- * counters at zero again.  workspace must be 16-byte aligned. */
+ * first call that uses the workspace; every call that completes leaves it
+ * ready for the next (counters back at zero).  workspace must be 256-byte
+ * aligned.  After a CUDA error inside a call, zero it again. */
 specv_status specv_workspace_init(void* workspace, size_t workspace_bytes, specv_stream_t stream);
 
 /*
@@ -130,7 +133,7 @@ specv_status specv_workspace_init(void* workspace, size_t workspace_bytes, specv
  *   accepted_len      [B] int32 output: j in [0, n_b], or -1 for bad data.
  *   out_tokens        [B, K+1] int32 output: accepted drafts, the final
  *                     token, then -1.
- *   workspace         specv_workspace_bytes(B, K) bytes, 16-byte aligned,
+ *   workspace         specv_workspace_bytes(B, K, V, dtype) bytes, 256-byte aligned,
  *                     zeroed once with specv_workspace_init.  Calls that may
  *                     run concurrently need separate workspaces.
  * Enqueues one kernel on `stream`; no host synchronisation.
@@ -145,16 +148,17 @@ specv_status spec_verify_sample(const void* target_logits, const void* draft_log
 
 /*
  * Same as spec_verify_sample, and also writes per-row statistics for parity
- * checks: row_stats [B, K+1, 8] float32 (device), for every row the request
- * needs:
+ * checks: row_stats [B, K+1, 8] float32 (device), for the rows the request
+ * needs (slots 6 and 7 only for the row of the final draw, t = accepted_len):
  *   0 max_i z^p_i (raw logit)    1 S_p = sum_i exp((z^p_i - max)/T)
  *   2 ln p(x_t)                  3 max_i z^q_i       4 S_q
  *   5 ln q(x_t)                  6 final-draw mass (below)
  *   7 the row's final-draw token (residual with uniforms_resample[b] at
  *     t < n_b, bonus with uniforms[b,n_b] at t = n_b; greedy: argmax)
- * Slot 6 is the normalised mass of the row's final-draw weights:
- * sum_i (p_i - q_i)+ at t < n_b, sum_i p_i at t = n_b.  Unused slots and
- * rows are left untouched.  Costs an extra on-chip pass per row.
+ * Slot 6 is the normalised mass of the final draw's weights: sum_i (p_i - q_i)+
+ * at a rejected position, sum_i p_i at the bonus position.  At T = 0 slot 0
+ * is the row maximum and slot 7 the argmax for every row t <= n_b.  Unused
+ * slots and rows are left untouched.
  */
 specv_status spec_verify_sample_debug(const void* target_logits, const void* draft_logits,
                                       specv_dtype dtype, const int32_t* draft_tokens,
@@ -194,8 +198,8 @@ specv_status spec_verify_sample_host(const void* target_logits, const void* draf
                                      specv_stream_t stream);
 
 /* The launch shape the library picks for these sizes (diagnostics): out[0]
- * CTAs per thread-block cluster, out[1] vocabulary elements per CTA slice,
- * out[2] shared-memory stages per CTA, out[3] clusters launched, out[4]
+ * CTAs launched (persistent), out[1] vocabulary elements per chunk (tile),
+ * out[2] shared-memory stages per CTA, out[3] chunks per row, out[4]
  * dynamic shared memory per CTA (bytes), out[5] threads per CTA.  Queries
  * the current device's occupancy; launches nothing. */
 specv_status specv_launch_plan(int B, int K, int V, specv_dtype dtype, int with_draft,
@@ -210,11 +214,11 @@ specv_status specv_launch_plan(int B, int K, int V, specv_dtype dtype, int with_
  * no counterpart; this is a packaging variant of spec_verify_sample.
  *
  * Same inputs, outputs, readings and errors as spec_verify_sample, with no
- * workspace argument: the scratch (status word, arrival counters, per-unit
- * records) lives in a module-scope device array of the library, sized for
- * SPECV_NOALLOC_MAX_BATCH requests and SPECV_NOALLOC_MAX_UNITS =
- * B*(K+1) units (about 144 KB); every GPU that loads the library holds it
- * until the process exits.  Larger shapes return SPECV_ERR_UNSUPPORTED.
+ * workspace argument: the scratch (the workspace of spec_verify_sample)
+ * lives in a module-scope device array of the library of
+ * SPECV_NOALLOC_SCRATCH_BYTES (4 MiB); every GPU that loads the library
+ * holds it until the process exits.  Shapes whose workspace
+ * (specv_workspace_bytes) exceeds it return SPECV_ERR_UNSUPPORTED.
  *   - It calls no cudaMalloc, cudaFree or allocating library routine.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current) and caches it; make
@@ -226,8 +230,7 @@ specv_status specv_launch_plan(int B, int K, int V, specv_dtype dtype, int with_
  *   - The device status word is not exposed: bad data shows as
  *     accepted_len[b] = -1 and out_tokens[b,:] = -1.
  */
-#define SPECV_NOALLOC_MAX_BATCH 4096
-#define SPECV_NOALLOC_MAX_UNITS 16384
+#define SPECV_NOALLOC_SCRATCH_BYTES (4u << 20)
 
 specv_status spec_verify_sample_noalloc(const void* target_logits, const void* draft_logits,
                                         specv_dtype dtype, const int32_t* draft_tokens,

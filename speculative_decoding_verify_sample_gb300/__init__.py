@@ -44,8 +44,13 @@ def _dtype_code(t):
     raise TypeError(f"logits must be bfloat16 or float32, got {t.dtype}")
 
 
-def workspace_bytes(B: int, K: int) -> int:
-    return int(lib().specv_workspace_bytes(B, K))
+def _code(dtype):
+    torch = _torch()
+    return SPECV_BF16 if dtype in (torch.bfloat16, "bf16", SPECV_BF16) else SPECV_F32
+
+
+def workspace_bytes(B: int, K: int, V: int, dtype) -> int:
+    return int(lib().specv_workspace_bytes(B, K, V, _code(dtype)))
 
 
 def launch_plan(B: int, K: int, V: int, dtype, with_draft: bool = True) -> dict:
@@ -55,7 +60,7 @@ def launch_plan(B: int, K: int, V: int, dtype, with_draft: bool = True) -> dict:
     code = SPECV_BF16 if dtype in (torch.bfloat16, "bf16") else SPECV_F32
     out = (ctypes.c_int32 * 6)()
     check("specv_launch_plan", lib().specv_launch_plan(B, K, V, code, int(with_draft), out))
-    return dict(cluster=out[0], slice=out[1], stages=out[2], clusters=out[3], smem=out[4],
+    return dict(ctas=out[0], chunk=out[1], stages=out[2], chunks_per_row=out[3], smem=out[4],
                 threads=out[5])
 
 
@@ -66,15 +71,16 @@ def max_vocab(dtype) -> int:
 
 
 class Workspace:
-    """Device workspace for calls over up to B requests of up to K drafts,
-    zeroed once on creation (the library keeps it zeroed between calls)."""
+    """Device workspace for calls over B requests of up to K drafts of a
+    V-entry vocabulary, zeroed once on creation (every call leaves it ready
+    for the next)."""
 
-    def __init__(self, B: int, K: int, device=None, stream=None):
+    def __init__(self, B: int, K: int, V: int, dtype, device=None, stream=None):
         torch = _torch()
-        n = workspace_bytes(B, K)
+        n = workspace_bytes(B, K, V, dtype)
         if n == 0:
-            raise ValueError(f"unsupported workspace shape B={B} K={K}")
-        self.B, self.K, self.nbytes = B, K, n
+            raise ValueError(f"unsupported workspace shape B={B} K={K} V={V}")
+        self.B, self.K, self.V, self.nbytes = B, K, V, n
         self.tensor = torch.empty(n, dtype=torch.uint8, device=device)
         check("specv_workspace_init",
               lib().specv_workspace_init(self.tensor.data_ptr(), n,
@@ -139,7 +145,7 @@ def _run(fn_name, target, draft, draft_tokens, draft_len, temperature, uniforms,
     if out_tokens is None:
         out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
     if workspace is None:
-        workspace = Workspace(B, K, dev, stream)
+        workspace = Workspace(B, K, V, target.dtype, dev, stream)
     args = [_ptr(target), _ptr(draft), _dtype_code(target), _ptr(draft_tokens), _ptr(draft_len),
             _ptr(temperature), _ptr(uniforms), _ptr(uniforms_resample), B, K, V,
             _ptr(accepted_len), _ptr(out_tokens), workspace.tensor.data_ptr(), workspace.nbytes]
@@ -168,8 +174,8 @@ def spec_verify_sample_debug(target_logits, draft_logits, draft_tokens, draft_le
                              uniforms, uniforms_resample, *, workspace=None, accepted_len=None,
                              out_tokens=None, row_stats=None, stream=None):
     """As spec_verify_sample, plus per-row statistics [B, K+1, 8] float32
-    (max_p, S_p, ln p(x), max_q, S_q, ln q(x), final-draw mass, candidate);
-    rows the request does not need are left as NaN."""
+    (max_p, S_p, ln p(x), max_q, S_q, ln q(x), final-draw mass, drawn token;
+    the last two at the final row only); unused slots are left as NaN."""
     torch = _torch()
     B, K1, _ = target_logits.shape
     if row_stats is None:
@@ -230,9 +236,9 @@ def spec_verify_sample_noalloc(target_logits, draft_logits, draft_tokens, draft_
     site (plugin hooks handed only their declared tensors, serving loops that
     forbid cudaMalloc after start-up, hosts whose memory another allocator
     owns).  The caller passes preallocated outputs; the scratch is the
-    library's own fixed device array (at most 4096 requests and 16384
-    request-positions), shared by every call on the device, so calls that
-    may overlap on the GPU must be serialised.  Make the first call on a
+    library's own fixed 4 MiB device array (shapes whose workspace exceeds
+    it are rejected), shared by every call on the device, so calls that may
+    overlap on the GPU must be serialised.  Make the first call on a
     device before any stream capture: it looks up the array's address."""
     B, K, V = _check_inputs(target_logits, draft_logits, draft_tokens, draft_len, temperature,
                             uniforms, uniforms_resample)

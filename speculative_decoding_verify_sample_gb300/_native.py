@@ -35,7 +35,7 @@ SIGNATURES = {
     "specv_version": (_i, []),
     "specv_max_vocab": (_i, [_i]),
     "specv_status_string": (ctypes.c_char_p, [_i]),
-    "specv_workspace_bytes": (_sz, [_i, _i]),
+    "specv_workspace_bytes": (_sz, [_i, _i, _i, _i]),
     "specv_workspace_init": (_i, [_vp, _sz, _vp]),
     "spec_verify_sample": (_i, _VERIFY_ARGS + [_vp]),
     "spec_verify_sample_debug": (_i, _VERIFY_ARGS + [_vp, _vp]),
@@ -48,8 +48,7 @@ SIGNATURES = {
                                         _vp]),
 }
 
-NOALLOC_MAX_BATCH = 4096
-NOALLOC_MAX_UNITS = 16384
+NOALLOC_SCRATCH_BYTES = 4 << 20
 
 _lock = threading.Lock()
 _lib = None

@@ -44,9 +44,14 @@ def test_limits_and_sizes(L):
     assert L.specv_max_vocab(0) >= 262144
     assert L.specv_max_vocab(1) >= 262144
     assert L.specv_max_vocab(7) == 0
-    assert L.specv_workspace_bytes(0, 4) == 0
-    assert L.specv_workspace_bytes(4, 17) == 0
-    assert L.specv_workspace_bytes(32, 4) >= 16 + 32 * 4 + 32 * 5 * 8
+    assert L.specv_workspace_bytes(0, 4, 1000, 1) == 0
+    assert L.specv_workspace_bytes(4, 17, 1000, 1) == 0
+    assert L.specv_workspace_bytes(4, 4, 0, 1) == 0
+    assert L.specv_workspace_bytes(4, 4, 1000, 5) == 0
+    assert L.specv_workspace_bytes(4, 4, L.specv_max_vocab(1) + 1, 1) == 0
+    # at least one 8-byte partial per (request, row, 16 KB chunk)
+    assert L.specv_workspace_bytes(32, 4, 128256, 1) >= 32 * 9 * 16 * 8
+    assert L.specv_workspace_bytes(32, 4, 128256, 0) > L.specv_workspace_bytes(32, 4, 128256, 1)
     assert L.specv_host_staging_bytes(2, 2, 100, 1, 1) >= 2 * 3 * 100 * 2 + 2 * 2 * 100 * 2
     assert L.specv_status_string(0) == b"ok"
 
@@ -66,8 +71,8 @@ def _call(L, **over):
 @pytest.mark.parametrize("over,status", [
     (dict(target=None), 1), (dict(tokens=None), 1), (dict(acc=None), 1), (dict(ws=None), 1),
     (dict(dtype=3), 1), (dict(B=0), 1), (dict(K=0), 1), (dict(V=0), 1),
-    (dict(K=17), 2), (dict(B=70000), 2), (dict(V=786433), 2), (dict(dtype=0, V=393217), 2),
-    (dict(wsb=8), 3), (dict(target=FAKE + 1), 1), (dict(ws=FAKE + 8), 1), (dict(uni=FAKE + 2), 1),
+    (dict(K=17), 2), (dict(B=70000), 2), (dict(V=1048577), 2), (dict(dtype=0, V=524289), 2),
+    (dict(wsb=8), 3), (dict(target=FAKE + 1), 1), (dict(ws=FAKE + 128), 1), (dict(uni=FAKE + 2), 1),
 ])
 def test_host_side_argument_errors(L, over, status):
     assert _call(L, **over) == status

@@ -34,7 +34,7 @@ def _full_check(inp, debug=True, nthreads=8):
         acc_d, out_d, rs = run_gpu(inp, debug=True)
         assert np.array_equal(acc_d, acc_g) and np.array_equal(out_d, out_g)
         info = oracle.row_stats(inp, nthreads=nthreads)
-        assert_row_stats_match(inp, rs, info)
+        assert_row_stats_match(inp, rs, info, acc_d)
     return ties
 
 
@@ -59,8 +59,8 @@ RANDOM_CASES = [
     (6, 4, 1, 1, "f32", 1.0, None, 0.0),             # one-token vocabulary
     (7, 4, 2, 2, "bf16", 0.7, None, 0.5),
     (8, 10, 4, 50257, "bf16", 0.9, "random", 0.2),   # GPT-2 vocabulary
-    (9, 4, 4, 300000, "bf16", 1.0, None, 0.25),      # 16-CTA clusters, large slices
-    (10, 3, 2, 200001, "f32", 0.6, "random", 0.0),   # unaligned f32, 16-CTA clusters
+    (9, 4, 4, 300000, "bf16", 1.0, None, 0.25),      # 37 chunks per row
+    (10, 3, 2, 200001, "f32", 0.6, "random", 0.0),   # unaligned f32, 49 chunks per row
     (11, 7, 5, 8, "f32", 0.3, "random", 0.3),
     (12, 2, 3, 129280, "bf16", 0.05, None, 0.0),     # small temperature
 ]
@@ -114,7 +114,7 @@ def test_all_greedy_without_draft_logits():
 
 def test_workspace_reused_across_calls():
     import speculative_decoding_verify_sample_gb300 as sv
-    ws = sv.Workspace(16, 4, "cuda")
+    ws = sv.Workspace(16, 4, 2048, "bf16", "cuda")
     a = synth.random_case(23, 16, 4, 2048, "bf16", temperature=0.9, draft_len="random",
                           greedy_frac=0.3)
     b = synth.random_case(24, 16, 4, 2048, "bf16", temperature=1.1)
@@ -134,7 +134,7 @@ def test_device_flags_bad_data():
     inp["temperature"][4] = -0.5
     inp["uniforms"][5, 2] = 1.0
     inp["target"][6, 1, :] = -np.inf         # sampled row without a finite maximum
-    ws = sv.Workspace(8, 3, "cuda")
+    ws = sv.Workspace(8, 3, 1000, "f32", "cuda")
     acc, out = run_gpu(inp, workspace=ws)
     assert list(acc[[1, 2, 3, 4, 5, 6]]) == [-1] * 6
     assert np.all(out[[1, 2, 3, 4, 5, 6]] == -1)
@@ -152,7 +152,7 @@ def test_sampled_request_without_draft_logits_is_flagged():
     import speculative_decoding_verify_sample_gb300 as sv
     inp = synth.random_case(26, 4, 2, 512, "f32", temperature=np.array([0, 1, 0, 0], np.float32))
     inp["draft"] = None
-    ws = sv.Workspace(4, 2, "cuda")
+    ws = sv.Workspace(4, 2, 512, "f32", "cuda")
     acc, out = run_gpu(inp, workspace=ws)
     assert acc[1] == -1
     assert ws.read_status() & sv.DEV_NO_DRAFT
@@ -165,7 +165,7 @@ def test_host_entry_point_matches_device():
     acc_d, out_d = run_gpu(inp)
     h = {k: v.cpu().pin_memory() if v is not None else None for k, v in to_device(inp, "cpu").items()}
     staging = sv.HostStaging(12, 4, 9000, "bf16", with_draft=True, device="cuda")
-    ws = sv.Workspace(12, 4, "cuda")
+    ws = sv.Workspace(12, 4, 9000, "bf16", "cuda")
     acc_h, out_h = sv.spec_verify_sample_host(h["target"], h["draft"], h["draft_tokens"],
                                               h["draft_len"], h["temperature"], h["uniforms"],
                                               h["uniforms_resample"], staging=staging, workspace=ws)
@@ -183,7 +183,7 @@ def test_llama3_full():
     rows = np.arange(0, inp["B"], 4)
     sub, *_ = oracle_subset(inp, rows)
     info = oracle.row_stats(sub, nthreads=16)
-    assert_row_stats_match(inp, rs, info, rows=rows)
+    assert_row_stats_match(inp, rs, info, acc_g, rows=rows)
 
 
 def test_greedy_full_bit_exact_against_planted_argmax():

@@ -35,7 +35,7 @@ def test_noalloc_matches_workspace_entry_twice(seed, B, K, V, dtype):
     inp = synth.random_case(seed, B, K, V, dtype, temperature=0.9, draft_len="random",
                             greedy_frac=0.3)
     args = _device_args(inp)
-    ws = sv.Workspace(B, K, "cuda")
+    ws = sv.Workspace(B, K, V, dtype, "cuda")
     acc_ref, out_ref = sv.spec_verify_sample(*args, workspace=ws)
     torch.cuda.synchronize()
     acc_ref, out_ref = acc_ref.cpu().numpy(), out_ref.cpu().numpy()
@@ -55,8 +55,9 @@ def test_noalloc_rejects_shapes_beyond_its_array():
         pytest.skip("no CUDA device")
     import speculative_decoding_verify_sample_gb300 as sv
     sv.build()
-    B, K, V = sv._native.NOALLOC_MAX_BATCH + 1, 1, 64
-    inp = synth.random_case(9, B, K, V, "f32", temperature=1.0)
+    B, K, V = 2048, 4, 50000
+    assert sv.workspace_bytes(B, K, V, "bf16") > sv._native.NOALLOC_SCRATCH_BYTES
+    inp = synth.random_case(9, B, K, V, "bf16", temperature=1.0)
     args = _device_args(inp)
     acc = torch.empty(B, dtype=torch.int32, device="cuda")
     out = torch.empty((B, K + 1), dtype=torch.int32, device="cuda")
