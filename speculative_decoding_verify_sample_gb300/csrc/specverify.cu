@@ -8,28 +8,31 @@
 // draft is accepted draw a bonus token from p at the next position; at
 // temperature 0 compare argmax(p) with the draft instead.
 //
-// Work is split into tiles of one 16 KB chunk of one row.  Groups of four
-// consecutive chunks of a row are dealt round-robin, in request-major order,
-// to a grid of persistent CTAs.  Each CTA has three roles:
-//   * a producer warp streams each of its tiles' chunk(s) into a ring of
-//     shared-memory stages with TMA bulk copies (full / empty mbarriers);
-//   * eight consumer warps reduce a stats tile to a partial - the chunk's
-//     maximum and sum of exp((z - max)/T), or its argmax at T = 0, plus the
-//     drafted token's logit if the chunk holds it - or, for a draw tile, to
-//     per-warp prefix sums of the final-draw weights;
-//   * a control warp counts finished tiles per request (acq_rel atomics).
-//     The CTA that finishes a request's last stats tile combines the
-//     request's partials, runs the left-to-right accept test and publishes
-//     the decision; for a sampled request the final row (a rejected
-//     position's residual (p - q)+, or the bonus position's p) is then read
-//     again as draw tiles, each chunk group owned by a fixed CTA that polls
-//     for the decision.  The CTA that finishes the last draw tile locates the
-//     drawn token from the per-warp sums, re-reading one 32-vector segment,
-//     and writes the outputs.
-// No CTA waits for another: every wait is on this CTA's own mbarriers and is
-// bounded in time, with a status bit on timeout.  Each needed logit is read
-// from HBM once; the final row of a sampled request is read a second time,
-// normally from L2, because tickets run request by request.
+// Design.  Every warp of the grid is an independent agent.  The logits a
+// call needs are cut into items of one 8 KB chunk of one row ("stats"
+// items), numbered request by request, and agent a takes items a, a + G,
+// a + 2G, ... (G agents).  An agent streams its items through a private ring
+// of three shared-memory slots with TMA bulk copies, each slot completing on
+// its own mbarrier, and reduces each chunk alone to a partial: the chunk's
+// maximum and sum of exp((z - max)/T), or at T = 0 its maximum and the
+// lowest index holding it.  It then counts the item on the request's
+// counter in global memory.  The agent whose count completes a request
+// combines the request's partials, runs the left-to-right accept test and
+// either answers the request (greedy, or bad data) or publishes the final
+// row for the draw.  The final row (the residual (p - q)+ at a rejected
+// position, p at the bonus position) is read again as "draw" items of 4 KB
+// of target and draft each; draw item d of the request-major draw space
+// belongs to agent d mod G, which polls the request's state between its
+// stats items.  A draw item stores per-sweep sums of the final-draw weights;
+// the agent whose count completes the draw locates the token from them,
+// re-reading one 512-byte segment, and writes the outputs.
+//
+// No agent waits on another while it still has stats items: a wait for a
+// decision happens only once its own ring is empty and its counts are
+// flushed, so every wait ends.  Every wait is also bounded in time and sets
+// a status bit when it gives up.  Each needed logit is read from HBM once;
+// the final row of a sampled request is read a second time, normally from
+// L2, because items run request by request.
 
 #include <cuda/atomic>
 #include <cuda_runtime.h>
@@ -45,103 +48,118 @@
 
 namespace {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kProducerWarp = kConsumerWarps;
-constexpr int kControlWarp = kConsumerWarps + 1;
-constexpr int kThreads = kConsumers + 64;
-constexpr int kChunkBytes = 16384;                        // one tile of one row
-constexpr int kVecs = kChunkBytes / 16 + 1;               // 16-byte vectors incl. phase
-constexpr int kSweeps = (kVecs + kConsumers - 1) / kConsumers;
-constexpr int kParts = kSweeps * kConsumerWarps;          // per chunk, per weight mode
-constexpr int kSlotBytes = kChunkBytes + 128;
-constexpr int kStageBytes = 2 * kSlotBytes;               // target chunk + draft chunk
-constexpr int kMaxStages = 6;
-constexpr int kMailbox = 32;
-constexpr int kGroup = 4;                                 // chunks per dealt group
-constexpr int kCtlBuf = 2048;                             // control-warp staging (floats)
-constexpr int kRunMax = 8;                                // event groups per control pass
-constexpr int kMaxChunks = 128;                           // per row
-constexpr long long kWaitLimitCycles = 4000000000ll;      // ~2 s at 2 GHz
+constexpr int kAgents = 8;                              // agent warps per CTA
+constexpr int kThreads = (kAgents + 1) * 32;            // + the control warp
+constexpr int kSlots = 2;                               // ring slots per agent
+constexpr int kChunkBytes = 12288;                      // stats item: one chunk of one row
+constexpr int kDrawBytes = 4096;                        // draw item: this much of the target row
+constexpr int kDrawSweeps = kDrawBytes / 512;           // 32 lanes x 16 bytes per sweep
+constexpr int kDraftOff = kDrawBytes;                   // draft part of a draw slot
+constexpr int kSlotBytes = kChunkBytes + 32;            // >= kDraftOff + kDrawBytes + 16
+constexpr int kMassMax = 520;                           // chunks per row, either size
+constexpr int kRingBytes = kAgents * kSlots * kSlotBytes;
+constexpr int kCtlRecords = 2080;                       // control-warp staging (8-byte records)
+constexpr int kPend = 16;                               // decided requests awaiting their draw
+constexpr int kMaxRowBytes = 1 << 21;                   // 2 MB per row of logits
+constexpr long long kWaitLimitCycles = 4000000000ll;    // ~2 s at 2 GHz
 constexpr uint32_t kSuspendHintNs = 20000;
+
+static_assert(kSlotBytes >= kDraftOff + kDrawBytes + 16, "draw slot too small");
+static_assert(kSlotBytes % 16 == 0, "slots must keep 16-byte alignment");
+static_assert(kDrawSweeps == 8, "a draw chunk has eight sweeps");
+static_assert(kCtlRecords >= 513, "the draw records of a 2 MB row fit the staging buffer");
+static_assert(kCtlRecords * 8 >= kChunkBytes + 16 && kCtlRecords * 8 >= kDraftOff + kDrawBytes + 16,
+              "a chunk of logits fits the control warp's buffer");
+static_assert(kMassMax >= (kMaxRowBytes + 15) / kDrawBytes + 1, "chunk masses of a 2 MB row fit");
 
 // workspace header words, one 128-byte line each
 constexpr int kHStatus = 0, kHExit = 32, kHEpoch = 64;
 constexpr int kHeaderBytes = 512;
 
-// per-request decision state: (call tag << 2) | value
-constexpr int kStateDraws = 1, kStateNone = 2;
+// per-request decision state: (call tag << 32) | payload, payload =
+// kind | residual << 2 | final row << 3
+constexpr uint32_t kStateDraws = 1, kStateNone = 2;
 
-// tile kinds and control events
-constexpr int kTileSentinel = 0, kTileStats = 1, kTileDraw = 2;
-constexpr int kEvSentinel = 0, kEvStats = 1, kEvDraw = 2;
+// A record is one 8-byte word written at once; bit 31 of its high half is
+// set in every written record, so a zero record is "not written yet".
+constexpr uint32_t kReady = 0x80000000u;
+
+constexpr int kItemStats = 1, kItemDraw = 2;
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-// Per-request state in the workspace (64 bytes).
-struct Req {
-  int stats_done;   // stats tiles finished
-  int draw_done;    // draw tiles finished
-  int j;            // accepted drafts
-  int t_f;          // row of the final draw
-  int residual;     // final draw from (p - q)+ (else from p)
-  int state;        // decision, tagged with the call (kStateDraws / kStateNone)
-  int pad1, pad2;
-  float u;          // uniform of the final draw
-  float Mp, Mq;     // row maxima (raw logits)
-  float sT;         // log2(e) / T
-  float ratio;      // S_p / S_q
-  float Sp, Sq;
-  float pad3;
+// Per-request record in the workspace (64 bytes).
+struct __align__(16) Req {
+  unsigned long long state;   // decision, tagged with the call
+  int pad0[6];
+  float4 prm;                 // final row: Mp, Mq, log2(e)/T, S_p/S_q
+  float pad1[4];
 };
+static_assert(sizeof(Req) == 64, "Req is one 64-byte record");
 
 struct Params {
-  const void* target;
-  const void* draft;
+  const unsigned char* target;
+  const unsigned char* draft;
   const int32_t* draft_tokens;
   const int32_t* draft_len;
   const float* temperature;
   const float* uniforms;
   const float* uniforms_resample;
   int B, K, V;
-  int R;            // rows per request in the ticket space: K+1 target, K draft
-  int NC;           // chunks per row
-  int NG;           // chunk groups per row
-  int CE;           // elements per chunk
-  int stages;
+  int R;            // record rows per request: K+1 target, then K draft
+  int NC;           // stats chunks per row
+  int NCd;          // draw chunks per row
+  float inv_NC;     // 1 / NC
+  // 16-byte-aligned address ranges the bulk copies may read
+  uintptr_t t_lo, t_hi, d_lo, d_hi;
   int32_t* accepted_len;
   int32_t* out_tokens;
   int32_t* header;
   Req* req;         // [B]
-  float2* part;     // [B][R][NC] stats partials
-  float* zx;        // [B][R] logit of the drafted token in each row
-  float* dpart;     // [B][NC][2][kParts] draw partial sums (mode 0: final weights, 1: p)
+  uint2* part;      // [B][R][NC] stats records: (max, sum | ready) or (max, index | ready)
+  uint2* dpart;     // [B][NCd] draw records: (p mass, final-draw mass | ready)
+  uint2* zx;        // [B][R] records of the drafted token's logit in rows t < n: (z, ready)
   float* row_stats; // [B][K+1][8] or null
 };
 
-// One tile as the producer hands it to the consumers (64 bytes).
-struct __align__(16) Tile {
-  int kind, b, r, c;
-  int x, greedy, t, residual;
-  float sT, Mp, Mq, ratio;
-  int pad[4];
+// One item as its agent staged it (48 bytes).
+struct __align__(16) Item {
+  int kind;     // kItemStats / kItemDraw
+  int b;
+  int row;      // stats: t (target) or K+1+t (draft); draw: final row t
+  int c;        // chunk
+  int mode;     // stats: greedy; draw: residual
+  float sT;     // stats: log2(e)/T
+  int xrow;     // stats: t if the row's drafted token x_t is needed, else -1
+  int peek_b;   // request whose state `peek` samples (-1: none)
+  // copied in with the slot (cp.async on the slot's barrier):
+  unsigned long long peek;   // state of request peek_b when the item was staged
+  unsigned long long peek_pad;
+  int x;                     // x_t (when xrow >= 0)
+  int pad[3];
+  float4 prm;   // draw: the decision's Mp, Mq, log2(e)/T, S_p/S_q
 };
 
-struct Ctl {
-  uint64_t full[kMaxStages];
-  uint64_t empty[kMaxStages];
-  uint64_t mb_full[kMailbox];
-  uint64_t mb_empty[kMailbox];
-  Tile tile[kMaxStages];
-  int2 mb[kMailbox];
-  float4 wpart[kMaxStages][kConsumerWarps];   // per-warp partials of a stats tile
-  int done_cnt[kMaxStages];                     // consumer warps finished with a stage
-  int mb_head;                                  // next mailbox slot to fill
-  alignas(16) float cbuf[kCtlBuf];   // control warp: staged partials (read as float2)
-  float ctot[kMaxChunks];       // control warp: chunk totals
-  int run_kind[kRunMax], run_b[kRunMax], run_cnt[kRunMax];
-  uint32_t tag;     // this call's tag for request states
+struct AgentSmem {
+  uint64_t full[kSlots];
+  Item item[kSlots];
+};
+
+// A decided request whose final draw is pending (the control warp's).
+struct __align__(16) Pend {
+  int b, j, t_f, residual;
+  float u, Sp, pad0, pad1;
+  float4 prm;
+};
+
+struct Smem {
+  AgentSmem ag[kAgents];
+  alignas(128) uint2 cbuf[kCtlRecords];   // control warp: staged records, or a chunk of logits
+  uint64_t cbar;                          // control warp: its chunk copies
+  float cmass[kMassMax];     // control warp: chunk masses of a final draw
+  Pend pend[kPend];
+  uint32_t tag;
 };
 
 // ---------------------------------------------------------------- elements
@@ -161,7 +179,6 @@ template <> struct Elt<SPECV_F32> {
                  fmaxf(__uint_as_float(raw.z), __uint_as_float(raw.w)));
   }
   __device__ static float load(const unsigned char* p) { return *reinterpret_cast<const float*>(p); }
-  // running elementwise max of vectors, and its final value
   struct MaxAcc {
     float a = -INFINITY, b = -INFINITY;
     __device__ void add(uint4 raw) {
@@ -208,9 +225,7 @@ template <> struct Elt<SPECV_BF16> {
       asm("max.bf16x2 %0, %0, %1;" : "+r"(w[2]) : "r"(raw.z));
       asm("max.bf16x2 %0, %0, %1;" : "+r"(w[3]) : "r"(raw.w));
     }
-    __device__ float value() const {
-      return vec_max(make_uint4(w[0], w[1], w[2], w[3]));
-    }
+    __device__ float value() const { return vec_max(make_uint4(w[0], w[1], w[2], w[3])); }
   };
   __device__ static float ldg(const unsigned char* p) {
     return __uint_as_float(static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short*>(p)))
@@ -236,10 +251,6 @@ __device__ __forceinline__ void mbar_init_fence() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
                "r"(bytes)
@@ -260,54 +271,46 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
-// Non-blocking test of phase `parity` (acquire on success).
-__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-
-// Waits for phase `parity` of the barrier; gives up after kWaitLimitCycles.
-// Called by one thread of a group: the others wait on a hardware barrier,
-// so polling never takes issue slots from the warps doing the work; the
-// poller sleeps between polls.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
+// Whole warp: waits for phase `parity` of the barrier; gives up after
+// kWaitLimitCycles.  Every lane polls, so every lane acquires the phase.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
+  bool ok = mbar_try_wait(bar, parity);
+  if (__all_sync(0xffffffffu, ok)) return true;
   const long long t0 = clock64();
-  uint32_t ns = 32;
   for (;;) {
-    __nanosleep(ns);
-    if (mbar_try_wait(bar, parity)) return true;
-    if (ns < 256) ns <<= 1;
-    if (clock64() - t0 > kWaitLimitCycles) return false;
+    ok = ok || mbar_try_wait(bar, parity);
+    if (__all_sync(0xffffffffu, ok)) return true;
+    if (__any_sync(0xffffffffu, clock64() - t0 > kWaitLimitCycles)) return false;
   }
 }
 
-// Whole warp: lane 0 waits, the other lanes take the phase afterwards.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int lane) {
-  int ok = 0;
-  if (lane == 0) ok = mbar_wait(bar, parity);
-  ok = __shfl_sync(0xffffffffu, ok, 0);
-  if (ok) mbar_test(bar, parity);
-  return ok != 0;
+// Orders this thread's earlier shared-memory accesses (generic proxy) before
+// later bulk copies into the same bytes (async proxy).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // Non-tensor TMA bulk copy global -> this CTA's shared memory.  Both
 // addresses 16-byte aligned, size a multiple of 16.
-__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes,
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, uintptr_t src, uint32_t bytes,
                                               uint64_t* bar) {
-  const unsigned long long gsrc = static_cast<unsigned long long>(__cvta_generic_to_global(src));
+  const unsigned long long gsrc =
+      static_cast<unsigned long long>(__cvta_generic_to_global(reinterpret_cast<const void*>(src)));
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
           "r"(smem_addr(dst)),
       "l"(gsrc), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(__cvta_generic_to_global(p)));
+}
+
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
 }
 
 // 2^x on the MUFU unit (PTX ex2.approx.ftz.f32); -inf -> +0.
@@ -318,28 +321,14 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 // exp((z - m)/T) as 2^((z - m) * log2(e)/T), the argument formed from the
-// exact difference to the reference m.
+// difference to the reference m.
 __device__ __forceinline__ float scaled_exp(float z, float m, float sT) {
   return ex2(__fmul_rn(__fsub_rn(z, m), sT));
 }
 
 __device__ __forceinline__ float temp_scale(float T) { return __fdiv_rn(kLog2e, T); }
 
-using AtomicInt = cuda::atomic_ref<int, cuda::thread_scope_device>;
-
 // ---------------------------------------------------------------- reductions
-
-// Online (max, sum of exp) pairs: the sum is relative to the max.
-__device__ __forceinline__ void pair_combine(float& m, float& s, float om, float os, float sT) {
-  const float M = fmaxf(m, om);
-  if (M == -INFINITY) {
-    m = M;
-    s = 0.0f;
-    return;
-  }
-  s = __fadd_rn(__fmul_rn(s, scaled_exp(m, M, sT)), __fmul_rn(os, scaled_exp(om, M, sT)));
-  m = M;
-}
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -359,31 +348,6 @@ __device__ __forceinline__ int warp_min_int(int v) {
   return v;
 }
 
-// Warp-wide (max, sum of exp) from per-lane pairs relative to each lane's
-// max: the max first, then every lane rescales its sum once, then a sum.
-__device__ __forceinline__ void warp_max_sum(float& m, float& s, float sT) {
-  const float M = warp_max(m);
-  const float sc = (m > -INFINITY) ? __fmul_rn(s, scaled_exp(m, M, sT)) : 0.0f;
-  s = warp_sum(sc);
-  m = M;
-}
-
-__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
-  return v > bv || (v == bv && i < bi);
-}
-
-__device__ __forceinline__ void warp_argmax(float& v, int& i) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
-    const int oi = __shfl_xor_sync(0xffffffffu, i, o);
-    if (better(ov, oi, v, i)) {
-      v = ov;
-      i = oi;
-    }
-  }
-}
-
 __device__ __forceinline__ float warp_incl_scan(float v, int lane) {
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -393,84 +357,170 @@ __device__ __forceinline__ float warp_incl_scan(float v, int lane) {
   return v;
 }
 
-// ---------------------------------------------------------------- chunks
+__device__ __forceinline__ int warp_incl_scan_int(int v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += y;
+  }
+  return v;
+}
 
-// Where chunk c of a row sits: elements [e0, e0 + cnt) of the row.  Shared
-// memory keeps the row's global 16-byte phase h, so element i of the chunk
-// is at byte h + i * elt and vector j covers bytes [16 j, 16 j + 16).
-struct Geo {
-  int e0, cnt, h, nvec;
+// ---------------------------------------------------------------- geometry
+
+// A chunk of a row as it sits in a slot.  Slot byte 0 is global address g0;
+// the row's element e is at slot byte off0 + e * elt; elements [e_lo, e_hi)
+// belong to the chunk.  For the target row of any item g0 is the 16-byte
+// boundary at or below the row's start plus c * CB, so the slot's 16-byte
+// vectors are the row's aligned vectors.
+struct Chunk {
+  uintptr_t g0;
+  int off0;
+  int e_lo, e_hi;
 };
 
 template <int DT>
-__device__ __forceinline__ const unsigned char* row_ptr(const void* base, size_t row, int V) {
-  return static_cast<const unsigned char*>(base) + row * static_cast<size_t>(V) * Elt<DT>::kBytes;
+__device__ __forceinline__ uintptr_t row_addr(const unsigned char* base, size_t row, int V) {
+  return reinterpret_cast<uintptr_t>(base) + row * static_cast<size_t>(V) * Elt<DT>::kBytes;
 }
 
 template <int DT>
-__device__ __forceinline__ Geo chunk_geo(const Params& P, const unsigned char* row, int c) {
-  using E = Elt<DT>;
-  Geo g;
-  g.e0 = c * P.CE;
-  g.cnt = min(P.CE, P.V - g.e0);
-  g.h = static_cast<int>((reinterpret_cast<uintptr_t>(row) + static_cast<size_t>(g.e0) * E::kBytes) & 15);
-  g.nvec = (g.h + g.cnt * E::kBytes + 15) / 16;
-  return g;
+__device__ __forceinline__ Chunk chunk_of(uintptr_t row, int V, int c, int CB) {
+  constexpr int eb = Elt<DT>::kBytes;
+  const uintptr_t a0 = row & ~static_cast<uintptr_t>(15);
+  const int h = static_cast<int>(row - a0);   // a multiple of the element size
+  Chunk k;
+  k.g0 = a0 + static_cast<size_t>(c) * CB;
+  k.off0 = h - c * CB;
+  k.e_lo = max(0, (c * CB - h) / eb);
+  k.e_hi = min(V, ((c + 1) * CB - h) / eb);
+  return k;
 }
 
+// The draft elements [e_lo, e_hi) of a draw chunk, placed from the 16-byte
+// boundary at or below the first of them.
 template <int DT>
-__device__ __forceinline__ int vec_base(const Geo& g, int j) {
-  return (16 * j - g.h) / Elt<DT>::kBytes;
+__device__ __forceinline__ Chunk draft_part(uintptr_t row, const Chunk& tgt) {
+  constexpr int eb = Elt<DT>::kBytes;
+  Chunk k;
+  const uintptr_t first = row + static_cast<size_t>(max(tgt.e_lo, 0)) * eb;
+  k.g0 = first & ~static_cast<uintptr_t>(15);
+  k.off0 = static_cast<int>(static_cast<intptr_t>(row) - static_cast<intptr_t>(k.g0));
+  k.e_lo = tgt.e_lo;
+  k.e_hi = tgt.e_hi;
+  return k;
 }
 
+// The bytes of a chunk a bulk copy moves: the 16-byte-aligned cover of its
+// elements, inside the tensor's aligned range [lo, hi).  Returns the byte
+// count (0: nothing) and the global start.
 template <int DT>
-__device__ __forceinline__ bool vec_full(const Geo& g, int j) {
-  const int i0 = vec_base<DT>(g, j);
-  return i0 >= 0 && i0 + Elt<DT>::kPerVec <= g.cnt;
+__device__ __forceinline__ uint32_t bulk_span(const Chunk& k, uintptr_t lo, uintptr_t hi,
+                                              uintptr_t* start) {
+  constexpr int eb = Elt<DT>::kBytes;
+  if (k.e_hi <= k.e_lo) return 0;
+  const uintptr_t first = k.g0 + static_cast<intptr_t>(k.off0) + static_cast<intptr_t>(k.e_lo) * eb;
+  const uintptr_t end = k.g0 + static_cast<intptr_t>(k.off0) + static_cast<intptr_t>(k.e_hi) * eb;
+  const uintptr_t a = first & ~static_cast<uintptr_t>(15);
+  const uintptr_t z = (end + 15) & ~static_cast<uintptr_t>(15);
+  const uintptr_t s = a > lo ? a : lo;
+  const uintptr_t e = z < hi ? z : hi;
+  if (e <= s) return 0;
+  *start = s;
+  return static_cast<uint32_t>(e - s);
 }
 
-// Values of vector j of a chunk held in shared memory; lanes outside the
-// chunk read as -inf.
+// Whole warp: elements of the chunk that lie outside the tensor's aligned
+// range (at most 15 bytes at either end of a tensor) are loaded by lanes.
 template <int DT>
-__device__ __forceinline__ void smem_vec(const unsigned char* buf, const Geo& g, int j, float* v) {
-  using E = Elt<DT>;
-  E::unpack(reinterpret_cast<const uint4*>(buf)[j], v);
-  if (!vec_full<DT>(g, j)) {
-    const int i0 = vec_base<DT>(g, j);
-#pragma unroll
-    for (int q = 0; q < E::kPerVec; ++q)
-      if (i0 + q < 0 || i0 + q >= g.cnt) v[q] = -INFINITY;
+__device__ __forceinline__ void fix_edges(const Chunk& k, uintptr_t lo, uintptr_t hi,
+                                          unsigned char* slot, int lane) {
+  constexpr int eb = Elt<DT>::kBytes;
+  if (k.e_hi <= k.e_lo) return;
+  const uintptr_t g_first = k.g0 + static_cast<intptr_t>(k.off0) + static_cast<intptr_t>(k.e_lo) * eb;
+  const uintptr_t g_end = k.g0 + static_cast<intptr_t>(k.off0) + static_cast<intptr_t>(k.e_hi) * eb;
+  const uintptr_t h1 = g_end < lo ? g_end : lo;                 // head [g_first, h1)
+  uintptr_t t0 = g_first > hi ? g_first : hi;                   // tail [t0, g_end)
+  if (t0 < h1) t0 = h1;
+  const int nh = h1 > g_first ? static_cast<int>((h1 - g_first) / eb) : 0;
+  const int nt = g_end > t0 ? static_cast<int>((g_end - t0) / eb) : 0;
+  if (nh == 0 && nt == 0) return;
+  if (lane < nh) {
+    const uintptr_t g = g_first + static_cast<uintptr_t>(lane) * eb;
+    Elt<DT>::copy1(slot + (g - k.g0), reinterpret_cast<const unsigned char*>(g));
+  } else if (lane >= 16 && lane - 16 < nt) {
+    const uintptr_t g = t0 + static_cast<uintptr_t>(lane - 16) * eb;
+    Elt<DT>::copy1(slot + (g - k.g0), reinterpret_cast<const unsigned char*>(g));
   }
+  __syncwarp();
 }
 
-// Final-draw weights of one vector: mode 0 = the residual (p - q)+ (or p at
-// the bonus position), mode 1 = p; both scaled by S_p.
+// Vectors of a target chunk: fully valid vectors [vf0, vf1), and up to two
+// partly valid edge vectors va (first) and vb (last) (-1: none).
+struct Vecs {
+  int e_base;      // element of vector 0, part 0 (may be negative)
+  int vf0, vf1;
+  int va, vb;
+};
+
 template <int DT>
-__device__ __forceinline__ void vec_weights(const float* vp, const float* vq, bool residual,
-                                            float Mp, float Mq, float sT, float ratio, float* w0,
-                                            float* w1) {
-  constexpr int CH = Elt<DT>::kPerVec;
-#pragma unroll
-  for (int q = 0; q < CH; ++q) {
-    const float ep = scaled_exp(vp[q], Mp, sT);
-    w1[q] = ep;
-    w0[q] = residual ? fmaxf(__fmaf_rn(-ratio, scaled_exp(vq[q], Mq, sT), ep), 0.0f) : ep;
+__device__ __forceinline__ Vecs vecs_of(const Chunk& k) {
+  constexpr int CH = Elt<DT>::kPerVec, eb = Elt<DT>::kBytes;
+  Vecs v;
+  v.e_base = -k.off0 / eb;
+  v.va = v.vb = -1;
+  if (k.e_hi <= k.e_lo) {
+    v.vf0 = v.vf1 = 0;
+    return v;
   }
+  const int lo = k.e_lo - v.e_base, hi = k.e_hi - v.e_base;   // element offsets in the slot
+  v.vf0 = (lo + CH - 1) / CH;
+  v.vf1 = hi / CH;
+  if (lo % CH) v.va = lo / CH;
+  if (hi % CH) v.vb = hi / CH;
+  if (v.vf1 < v.vf0) {   // the whole chunk inside one vector
+    v.vf1 = v.vf0;
+    v.va = lo / CH;
+    v.vb = -1;
+  } else if (v.va >= 0 && v.va == v.vb) {
+    v.vb = -1;
+  }
+  return v;
+}
+
+// Values of vector j with elements outside [e_lo, e_hi) set to -inf.
+template <int DT>
+__device__ __forceinline__ void masked_vec(const unsigned char* slot, const Vecs& vs,
+                                           const Chunk& k, int j, float* v) {
+  using E = Elt<DT>;
+  E::unpack(reinterpret_cast<const uint4*>(slot)[j], v);
+  const int e0 = vs.e_base + j * E::kPerVec;
+#pragma unroll
+  for (int q = 0; q < E::kPerVec; ++q)
+    if (e0 + q < k.e_lo || e0 + q >= k.e_hi) v[q] = -INFINITY;
 }
 
 // ---------------------------------------------------------------- requests
 
-__device__ int request_len(const Params& P, int b) {
-  return P.draft_len ? __ldg(P.draft_len + b) : P.K;
+__device__ __forceinline__ int request_bad(const Params& P, int n, float T) {
+  if (n < 1 || n > P.K) return SPECV_DEV_BAD_DRAFT_LEN;
+  if (!(T >= 0.0f) || isinf(T)) return SPECV_DEV_BAD_TEMPERATURE;
+  if (T > 0.0f && P.draft == nullptr) return SPECV_DEV_NO_DRAFT;
+  return 0;
 }
 
-// Stats tiles a valid request needs: target rows t <= n, draft rows t < n
-// when sampled, every chunk.
-__device__ __forceinline__ int request_tiles(const Params& P, int n, float T) {
+// Stats items of a request: target rows t <= n, draft rows t < n when
+// sampled, every chunk; none if its length or temperature is unusable.
+__device__ __forceinline__ int request_items(const Params& P, int n, float T) {
+  if (request_bad(P, n, T)) return 0;
   return ((n + 1) + (T > 0.0f ? n : 0)) * P.NC;
 }
 
-// Writes a finished request's outputs and returns its counters to zero.
+__device__ __forceinline__ int request_len(const Params& P, int b) {
+  return P.draft_len ? __ldg(P.draft_len + b) : P.K;
+}
+
+// Whole warp: writes a request's outputs.
 __device__ void finish_request(const Params& P, int b, int j, int tok, int lane) {
   const int K = P.K;
   int32_t* out = P.out_tokens + static_cast<size_t>(b) * (K + 1);
@@ -481,18 +531,14 @@ __device__ void finish_request(const Params& P, int b, int j, int tok, int lane)
     else if (s == j) v = tok;
     out[s] = v;
   }
-  if (lane == 0) {
-    P.accepted_len[b] = j;
-    P.req[b].stats_done = 0;
-    P.req[b].draw_done = 0;
-  }
+  if (lane == 0) P.accepted_len[b] = j;
   __syncwarp();
 }
 
-// Publishes request b's decision for the producers that own its draw tiles.
-__device__ __forceinline__ void set_state(const Params& P, int b, uint32_t tag, int v) {
-  AtomicInt(P.req[b].state).store(static_cast<int>((tag << 2) | static_cast<uint32_t>(v)),
-                                  cuda::memory_order_release);
+// Publishes request b's decision for the agents that own its draw items.
+__device__ __forceinline__ void set_state(const Params& P, int b, uint32_t tag, uint32_t payload) {
+  cuda::atomic_ref<unsigned long long, cuda::thread_scope_device>(P.req[b].state)
+      .store((static_cast<unsigned long long>(tag) << 32) | payload, cuda::memory_order_release);
 }
 
 __device__ void finish_bad(const Params& P, int b, int bits, int lane, uint32_t tag) {
@@ -503,855 +549,1032 @@ __device__ void finish_bad(const Params& P, int b, int bits, int lane, uint32_t 
   finish_request(P, b, -1, -1, lane);
 }
 
-// ---------------------------------------------------------------- producer
+// ---------------------------------------------------------------- chunk reductions
 
-// Copies one chunk into shared memory: the 16-byte-aligned interior by one
-// bulk copy (issued later by lane 0), the unaligned head and tail by the
-// lanes.  Returns the bulk byte count.
+// Whole warp: argmax of a stats chunk, lowest index on ties.  Each lane
+// keeps its maximum and the first of its vectors holding it (its vectors
+// taken in increasing order); the warp's first vector holding the maximum
+// is then searched once.
 template <int DT>
-__device__ uint32_t stage_chunk(const Params& P, const unsigned char* row, int c,
-                                unsigned char* dst, int lane, const unsigned char** bulk_src,
-                                unsigned char** bulk_dst) {
-  using E = Elt<DT>;
-  const Geo g = chunk_geo<DT>(P, row, c);
-  const unsigned char* gsrc = row + static_cast<size_t>(g.e0) * E::kBytes;
-  const uintptr_t s0 = reinterpret_cast<uintptr_t>(gsrc);
-  const uintptr_t s1 = s0 + static_cast<uintptr_t>(g.cnt) * E::kBytes;
-  const uintptr_t a = (s0 + 15) & ~static_cast<uintptr_t>(15);
-  const uintptr_t z = s1 & ~static_cast<uintptr_t>(15);
-  uint32_t bulk = 0;
-  uintptr_t head_end = s1, tail_begin = s1;
-  if (a < z) {
-    bulk = static_cast<uint32_t>(z - a);
-    *bulk_src = reinterpret_cast<const unsigned char*>(a);
-    *bulk_dst = dst + g.h + (a - s0);
-    head_end = a;
-    tail_begin = z;
-  }
-  const int nhead = static_cast<int>((head_end - s0) / E::kBytes);
-  const int ntail = static_cast<int>((s1 - tail_begin) / E::kBytes);
-  for (int i = lane; i < nhead + ntail; i += 32) {
-    const uintptr_t off = i < nhead ? static_cast<uintptr_t>(i) * E::kBytes
-                                    : (tail_begin - s0) + static_cast<uintptr_t>(i - nhead) * E::kBytes;
-    E::copy1(dst + g.h + off, gsrc + off);
-  }
-  return bulk;
-}
-
-// Stages one tile into the ring (waits, bounded, for a free stage).
-template <int DT>
-__device__ bool issue_tile(const Params& P, Ctl& S, unsigned char* dyn, int lane, int& k,
-                           const Tile& tl) {
-  const int K = P.K;
-  const int s = k % P.stages;
-  const uint32_t ph = static_cast<uint32_t>(k / P.stages) & 1u;
-  if (!warp_wait(&S.empty[s], ph ^ 1u, lane)) return false;
-  unsigned char* slot0 = dyn + static_cast<size_t>(s) * kStageBytes;
-  const unsigned char *src0 = nullptr, *src1 = nullptr;
-  unsigned char *dst0 = nullptr, *dst1 = nullptr;
-  uint32_t b0 = 0, b1 = 0;
-  if (tl.kind == kTileStats) {
-    const bool is_draft = tl.r > K;
-    const size_t row = is_draft ? static_cast<size_t>(tl.b) * K + tl.t
-                                : static_cast<size_t>(tl.b) * (K + 1) + tl.t;
-    const unsigned char* rp = row_ptr<DT>(is_draft ? P.draft : P.target, row, P.V);
-    b0 = stage_chunk<DT>(P, rp, tl.c, slot0, lane, &src0, &dst0);
-  } else {
-    const unsigned char* rp = row_ptr<DT>(P.target, static_cast<size_t>(tl.b) * (K + 1) + tl.t, P.V);
-    b0 = stage_chunk<DT>(P, rp, tl.c, slot0, lane, &src0, &dst0);
-    if (tl.residual) {
-      const unsigned char* rq = row_ptr<DT>(P.draft, static_cast<size_t>(tl.b) * K + tl.t, P.V);
-      b1 = stage_chunk<DT>(P, rq, tl.c, slot0 + kSlotBytes, lane, &src1, &dst1);
-    }
-  }
-  if (lane == 0) S.tile[s] = tl;
-  __syncwarp();
-  if (lane == 0) {
-    mbar_arrive_expect_tx(&S.full[s], b0 + b1);
-    if (b0) bulk_copy_g2s(dst0, src0, b0, &S.full[s]);
-    if (b1) bulk_copy_g2s(dst1, src1, b1, &S.full[s]);
-  }
-  ++k;
-  return true;
-}
-
-// Issues the draw tiles this CTA owns.  Draw group D = b * NG + d (chunks
-// [4d, 4d + 4) of request b's final row) belongs to CTA D mod grid, so this
-// CTA walks D = blockIdx.x + i * grid in request order, from the cursor i,
-// issuing the group of every request whose decision is published.  Without
-// `blocking` it returns at the first undecided request (a relaxed peek, so
-// the producer does not stall); with `blocking` it waits (bounded) for each.
-template <int DT>
-__device__ bool serve_draws(const Params& P, Ctl& S, unsigned char* dyn, int lane, int& k,
-                            long long& di, bool blocking) {
-  const int NC = P.NC, NG = P.NG;
-  const uint32_t tag = S.tag;
-  const long long total = static_cast<long long>(P.B) * NG;
-  for (;;) {
-    const long long D = blockIdx.x + di * static_cast<long long>(gridDim.x);
-    if (D >= total) return true;
-    const int b = static_cast<int>(D / NG);
-    const int dg = static_cast<int>(D - static_cast<long long>(b) * NG);
-    int st = 0;
-    if (lane == 0) {
-      const int peek = AtomicInt(P.req[b].state).load(cuda::memory_order_relaxed);
-      if ((static_cast<uint32_t>(peek) >> 2) == tag) st = peek & 3;
-      if (st == 0 && blocking) {
-        const long long t0 = clock64();
-        for (;;) {
-          __nanosleep(200);
-          const int v = AtomicInt(P.req[b].state).load(cuda::memory_order_relaxed);
-          if ((static_cast<uint32_t>(v) >> 2) == tag) {
-            st = v & 3;
-            break;
-          }
-          if (clock64() - t0 > kWaitLimitCycles) {
-            st = -1;
-            break;
-          }
-        }
-      }
-      if (st > 0) AtomicInt(P.req[b].state).load(cuda::memory_order_acquire);   // order the reads below
-    }
-    st = __shfl_sync(0xffffffffu, st, 0);
-    __syncwarp();
-    if (st < 0) return false;
-    if (st == 0) return true;   // not decided yet: look again later
-    if (st == kStateDraws) {
-      const Req* q = P.req + b;
-      Tile tl;
-      tl.kind = kTileDraw;
-      tl.b = b;
-      tl.r = 0;
-      tl.t = __ldcg(&q->t_f);
-      tl.residual = __ldcg(&q->residual);
-      tl.sT = __ldcg(&q->sT);
-      tl.Mp = __ldcg(&q->Mp);
-      tl.Mq = __ldcg(&q->Mq);
-      tl.ratio = __ldcg(&q->ratio);
-      tl.x = -1;
-      tl.greedy = 0;
-      for (int c = dg * kGroup; c < min(NC, dg * kGroup + kGroup); ++c) {
-        tl.c = c;
-        if (!issue_tile<DT>(P, S, dyn, lane, k, tl)) return false;
-      }
-    }
-    ++di;
-  }
-}
-
-// The producer warp: this CTA's stats groups (groups g, g + grid, ... of the
-// request-major group space), its draw tiles as their requests are decided,
-// then a sentinel.  Requests whose length or temperature is unusable are
-// answered by the owner of their first group.
-template <int DT>
-__device__ void producer(const Params& P, Ctl& S, unsigned char* dyn, int lane) {
-  const int K = P.K, NC = P.NC, R = P.R, NG = P.NG;
-  const long long total = static_cast<long long>(P.B) * R * NG;
-  int k = 0;         // stage uses
-  long long di = 0;  // draw cursor
-  bool ok = true;
-  int mb = -1, mn = 0, mbad = 0;
-  float mT = 0.0f;
-  for (long long gi = blockIdx.x; gi < total && ok; gi += gridDim.x) {
-    const int cg = static_cast<int>(gi % NG);
-    const long long br = gi / NG;
-    const int r = static_cast<int>(br % R);
-    const int b = static_cast<int>(br / R);
-    if (b != mb) {
-      mb = b;
-      mn = request_len(P, b);
-      mT = __ldg(P.temperature + b);
-      mbad = 0;
-      if (mn < 1 || mn > K) mbad = SPECV_DEV_BAD_DRAFT_LEN;
-      else if (!(mT >= 0.0f) || isinf(mT)) mbad = SPECV_DEV_BAD_TEMPERATURE;
-      else if (mT > 0.0f && P.draft == nullptr) mbad = SPECV_DEV_NO_DRAFT;
-    }
-    if (mbad) {
-      if (r == 0 && cg == 0) finish_bad(P, b, mbad, lane, S.tag);
-      continue;
-    }
-    const bool sampled = mT > 0.0f;
-    const bool valid = r <= K ? r <= mn : (sampled && r - (K + 1) < mn);
-    if (!valid) continue;   // rows after the draft are never read
-    Tile tl;
-    tl.kind = kTileStats;
-    tl.b = b;
-    tl.r = r;
-    tl.t = r <= K ? r : r - (K + 1);
-    tl.greedy = !sampled;
-    tl.x = tl.t < mn ? __ldg(P.draft_tokens + static_cast<size_t>(b) * K + tl.t) : -1;
-    tl.sT = sampled ? temp_scale(mT) : 0.0f;
-    tl.residual = 0;
-    tl.Mp = tl.Mq = tl.ratio = 0.0f;
-    for (int c = cg * kGroup; c < min(NC, cg * kGroup + kGroup) && ok; ++c) {
-      tl.c = c;
-      ok = issue_tile<DT>(P, S, dyn, lane, k, tl);
-    }
-    if (ok) ok = serve_draws<DT>(P, S, dyn, lane, k, di, false);
-  }
-  if (ok) ok = serve_draws<DT>(P, S, dyn, lane, k, di, true);
-  if (!ok && lane == 0) atomicOr(P.header + kHStatus, SPECV_DEV_TIMEOUT);
-  // sentinel: the consumers stop at it
-  const int s = k % P.stages;
-  const uint32_t ph = static_cast<uint32_t>(k / P.stages) & 1u;
-  const bool free_slot = warp_wait(&S.empty[s], ph ^ 1u, lane);
-  if (lane == 0) {
-    if (!free_slot) atomicOr(P.header + kHStatus, SPECV_DEV_TIMEOUT);
-    S.tile[s].kind = kTileSentinel;
-    mbar_arrive(&S.full[s]);
-  }
-}
-
-// ---------------------------------------------------------------- consumers
-
-// Each consumer warp runs on its own: it waits for a stage itself, and no
-// block-wide barrier is taken per tile.
-
-// Lane 0 of the posting warp: hands an event to the control warp.  Several
-// warps may post; each reserves a mailbox slot with a block-scope atomic.
-__device__ __forceinline__ void post_event(Ctl& S, const Params& P, int kind, int b) {
-  const int e = atomicAdd_block(&S.mb_head, 1);
-  const int slot = e % kMailbox;
-  const uint32_t ph = static_cast<uint32_t>(e / kMailbox) & 1u;
-  if (!mbar_wait(&S.mb_empty[slot], ph ^ 1u)) atomicOr(P.header + kHStatus, SPECV_DEV_TIMEOUT);
-  S.mb[slot] = make_int2(kind, b);
-  mbar_arrive(&S.mb_full[slot]);
-}
-
-// Lane 0: counts this warp's finish of the tile in stage s; true for the
-// last of the consumer warps (the one that combines and posts).
-__device__ __forceinline__ bool last_warp(Ctl& S, int s) {
-  __threadfence_block();
-  const bool last = atomicAdd_block(&S.done_cnt[s], 1) == kConsumerWarps - 1;
-  if (last) {
-    S.done_cnt[s] = 0;
-    __threadfence_block();
-  }
-  return last;
-}
-
-template <int DT>
-__device__ void consumer(const Params& P, Ctl& S, unsigned char* dyn, int tid) {
+__device__ __forceinline__ float2 chunk_argmax(const unsigned char* slot, const Chunk& k, int lane) {
   using E = Elt<DT>;
   constexpr int CH = E::kPerVec;
-  const int lane = tid & 31;
-  const int warp = tid >> 5;
-  const int K = P.K;
-  for (int k = 0;; ++k) {
-    const int s = k % P.stages;
-    const uint32_t ph = static_cast<uint32_t>(k / P.stages) & 1u;
-    const bool ok = warp_wait(&S.full[s], ph, lane);
-    const Tile tl = S.tile[s];
-    if (!ok || tl.kind == kTileSentinel) {
-      // the last warp to stop tells the control warp (after every event)
-      int last = 0;
-      if (lane == 0) last = last_warp(S, s);
-      if (__shfl_sync(0xffffffffu, last, 0) && lane == 0) post_event(S, P, kEvSentinel, 0);
-      if (!ok && lane == 0) atomicOr(P.header + kHStatus, SPECV_DEV_TIMEOUT);
-      break;
+  const Vecs vs = vecs_of<DT>(k);
+  const uint4* vec = reinterpret_cast<const uint4*>(slot);
+  float best = -INFINITY;
+  int bestv = INT_MAX;
+  if (lane == 0 && vs.va >= 0) {
+    float v[CH];
+    masked_vec<DT>(slot, vs, k, vs.va, v);
+    float m = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < CH; ++q) m = fmaxf(m, v[q]);
+    if (m > best) {
+      best = m;
+      bestv = vs.va;
     }
-    const unsigned char* buf0 = dyn + static_cast<size_t>(s) * kStageBytes;
-    const unsigned char* buf1 = buf0 + kSlotBytes;
+  }
+  int j = vs.vf0 + lane;
+  for (; j + 32 < vs.vf1; j += 64) {
+    const float m0 = E::vec_max(vec[j]);
+    const float m1 = E::vec_max(vec[j + 32]);
+    if (m0 > best) {
+      best = m0;
+      bestv = j;
+    }
+    if (m1 > best) {
+      best = m1;
+      bestv = j + 32;
+    }
+  }
+  if (j < vs.vf1) {
+    const float m0 = E::vec_max(vec[j]);
+    if (m0 > best) {
+      best = m0;
+      bestv = j;
+    }
+  }
+  if (lane == 1 && vs.vb >= 0) {
+    float v[CH];
+    masked_vec<DT>(slot, vs, k, vs.vb, v);
+    float m = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < CH; ++q) m = fmaxf(m, v[q]);
+    if (m > best) {
+      best = m;
+      bestv = vs.vb;
+    }
+  }
+  const float W = warp_max(best);
+  if (!(W > -INFINITY)) return make_float2(W, __int_as_float(k.e_lo));   // all -inf (or empty)
+  const int vstar = warp_min_int(best == W ? bestv : INT_MAX);
+  int idx = INT_MAX;
+  if (lane == 0) {
+    float v[CH];
+    masked_vec<DT>(slot, vs, k, vstar, v);
+#pragma unroll
+    for (int q = CH - 1; q >= 0; --q)
+      if (v[q] == W) idx = vs.e_base + vstar * CH + q;
+  }
+  idx = __shfl_sync(0xffffffffu, idx, 0);
+  return make_float2(W, __int_as_float(idx));
+}
 
-    if (tl.kind == kTileStats) {
-      const bool is_draft = tl.r > K;
-      const size_t row = is_draft ? static_cast<size_t>(tl.b) * K + tl.t
-                                  : static_cast<size_t>(tl.b) * (K + 1) + tl.t;
-      const unsigned char* rp = row_ptr<DT>(is_draft ? P.draft : P.target, row, P.V);
-      const Geo g = chunk_geo<DT>(P, rp, tl.c);
-      // interior vectors [jlo, jhi) hold only chunk elements; at most the
-      // first and the last vector are partial and are masked
-      const int jlo = g.h > 0 ? 1 : 0;
-      const int jhi = max(jlo, (g.h + g.cnt * E::kBytes) / 16);
-      const int edge0 = (jlo == 1) ? 0 : -1;                       // thread 0
-      const int edge1 = (jhi < g.nvec && jhi != edge0) ? jhi : -1;  // thread 1
-      const int my_edge = tid == 0 ? edge0 : (tid == 1 ? edge1 : -1);
-      float4 wpart;
-      if (tl.greedy) {
-        // ---- argmax, lowest index on ties ----------------------------------
-        typename E::MaxAcc acc;
-        for (int j = jlo + tid; j < jhi; j += kConsumers) acc.add(reinterpret_cast<const uint4*>(buf0)[j]);
-        float mx = acc.value();
-        if (my_edge >= 0) {
-          float v[CH];
-          smem_vec<DT>(buf0, g, my_edge, v);
+// Whole warp: (max, sum of exp((z - max)/T)) of a stats chunk.  The max
+// first, then exponents fma(z, sT, -c) against c = fl(max sT); the rounding
+// of c is taken out once at the end.
+template <int DT>
+__device__ __forceinline__ float2 chunk_softmax(const unsigned char* slot, const Chunk& k, float sT, int lane) {
+  using E = Elt<DT>;
+  constexpr int CH = E::kPerVec;
+  const Vecs vs = vecs_of<DT>(k);
+  const uint4* vec = reinterpret_cast<const uint4*>(slot);
+  float ev[CH];
+  const int my_edge = lane == 0 ? vs.va : (lane == 1 ? vs.vb : -1);
+  if (my_edge >= 0) masked_vec<DT>(slot, vs, k, my_edge, ev);
+  typename E::MaxAcc acc;
+  for (int j = vs.vf0 + lane; j < vs.vf1; j += 32) acc.add(vec[j]);
+  float m = acc.value();
+  if (my_edge >= 0) {
 #pragma unroll
-          for (int q = 0; q < CH; ++q) mx = fmaxf(mx, v[q]);
-        }
-        const float W = warp_max(mx);
-        // the first element equal to the warp's max, searched only by the
-        // lanes whose own maximum it is
-        int idx = INT_MAX;
-        if (mx == W && W > -INFINITY) {
-          if (my_edge == 0) {
-            float v[CH];
-            smem_vec<DT>(buf0, g, 0, v);
+    for (int q = 0; q < CH; ++q) m = fmaxf(m, ev[q]);
+  }
+  const float M = warp_max(m);
+  if (!(M > -INFINITY)) return make_float2(M, 0.0f);
+  const float c = __fmul_rn(M, sT);
+  float s0 = 0.0f, s1 = 0.0f;
+  for (int j = vs.vf0 + lane; j < vs.vf1; j += 32) {
+    float v[CH];
+    E::unpack(vec[j], v);
 #pragma unroll
-            for (int q = CH - 1; q >= 0; --q)
-              if (v[q] == W) idx = g.e0 + vec_base<DT>(g, 0) + q;
-          }
-          for (int j = jlo + tid; j < jhi && idx == INT_MAX; j += kConsumers) {
-            float v[CH];
-            E::unpack(reinterpret_cast<const uint4*>(buf0)[j], v);
+    for (int q = 0; q < CH; q += 2) {
+      s0 = __fadd_rn(s0, ex2(__fmaf_rn(v[q], sT, -c)));
+      s1 = __fadd_rn(s1, ex2(__fmaf_rn(v[q + 1], sT, -c)));
+    }
+  }
+  if (my_edge >= 0) {
 #pragma unroll
-            for (int q = CH - 1; q >= 0; --q)
-              if (v[q] == W) idx = g.e0 + vec_base<DT>(g, j) + q;
-          }
-          if (idx == INT_MAX && my_edge > 0) {
-            float v[CH];
-            smem_vec<DT>(buf0, g, my_edge, v);
+    for (int q = 0; q < CH; ++q) s0 = __fadd_rn(s0, ex2(__fmaf_rn(ev[q], sT, -c)));
+  }
+  const float S = warp_sum(__fadd_rn(s0, s1));
+  return make_float2(M, __fmul_rn(S, ex2(-__fmaf_rn(M, sT, -c))));
+}
+
+// Final-draw weights of one element: mode 0 = the residual (p - q)+ (or p at
+// the bonus position), mode 1 = p; both scaled by S_p.
+__device__ __forceinline__ void weights(float zp, float zq, bool residual, const float4& prm,
+                                        float& w0, float& w1) {
+  const float ep = scaled_exp(zp, prm.x, prm.z);
+  w1 = ep;
+  w0 = residual ? fmaxf(__fmaf_rn(-prm.w, scaled_exp(zq, prm.y, prm.z), ep), 0.0f) : ep;
+}
+
+// Final-draw weights of one element; elements whose target logit is not
+// above -inf (outside the chunk, -inf or NaN) weigh 0.
+__device__ __forceinline__ void element_weights(float zp, float zq, bool residual,
+                                                const float4& prm, float& w0, float& w1) {
+  weights(zp, zq, residual, prm, w0, w1);
+  if (!(zp > -INFINITY)) w0 = w1 = 0.0f;
+}
+
+// Final-draw weights of vector j of a chunk staged in a slot (target part
+// at slot byte 0, draft part at kDraftOff): mode 0 in w0, mode 1 in w1.
+// The draw items and the final search both form weights here, so their
+// sums agree bit for bit.
+template <int DT>
+__device__ __forceinline__ void vector_weights(const unsigned char* slot, const Vecs& vs,
+                                               const Chunk& kp, const Chunk& kq, bool residual,
+                                               bool same, const float4& prm, int j, float* w0,
+                                               float* w1) {
+  using E = Elt<DT>;
+  constexpr int CH = E::kPerVec, eb = E::kBytes;
+  const int e0 = vs.e_base + j * CH;
+  if (!(e0 + CH > kp.e_lo && e0 < kp.e_hi)) {
 #pragma unroll
-            for (int q = CH - 1; q >= 0; --q)
-              if (v[q] == W) idx = g.e0 + vec_base<DT>(g, my_edge) + q;
-          }
-        }
-        idx = warp_min_int(idx);
-        if (!(W > -INFINITY)) idx = g.e0;   // all -inf: the lowest index
-        wpart = make_float4(W, __int_as_float(idx), 0.0f, 0.0f);
-      } else {
-        // ---- one pass: chunk max and sum of exp((z - max)/T) ---------------
-        // exponents are fma(z, sT, -c) against c = fl(m sT), m the running
-        // max; the rounding of c is taken out once at the end
-        const float sT = tl.sT;
-        float m = -INFINITY, c = INFINITY, s0 = 0.0f, s1 = 0.0f;
-        for (int j = jlo + tid; j < jhi; j += kConsumers) {
-          const uint4 raw = reinterpret_cast<const uint4*>(buf0)[j];
-          const float cm = E::vec_max(raw);
-          if (cm > m) {
-            const float cn = __fmul_rn(cm, sT);
-            const float f = (m > -INFINITY) ? ex2(__fsub_rn(c, cn)) : 0.0f;
-            s0 = __fmul_rn(s0, f);
-            s1 = __fmul_rn(s1, f);
-            m = cm;
-            c = cn;
-          }
-          float v[CH];
-          E::unpack(raw, v);
-#pragma unroll
-          for (int q = 0; q < CH; q += 2) {
-            s0 = __fadd_rn(s0, ex2(__fmaf_rn(v[q], sT, -c)));
-            s1 = __fadd_rn(s1, ex2(__fmaf_rn(v[q + 1], sT, -c)));
-          }
-        }
-        if (my_edge >= 0) {
-          float v[CH];
-          smem_vec<DT>(buf0, g, my_edge, v);
-          float cm = -INFINITY;
-#pragma unroll
-          for (int q = 0; q < CH; ++q) cm = fmaxf(cm, v[q]);
-          if (cm > m) {
-            const float cn = __fmul_rn(cm, sT);
-            const float f = (m > -INFINITY) ? ex2(__fsub_rn(c, cn)) : 0.0f;
-            s0 = __fmul_rn(s0, f);
-            s1 = __fmul_rn(s1, f);
-            m = cm;
-            c = cn;
-          }
-#pragma unroll
-          for (int q = 0; q < CH; ++q) s0 = __fadd_rn(s0, ex2(__fmaf_rn(v[q], sT, -c)));
-        }
-        float sum = 0.0f;
-        if (m > -INFINITY) sum = __fmul_rn(__fadd_rn(s0, s1), ex2(-__fmaf_rn(m, sT, -c)));
-        warp_max_sum(m, sum, sT);
-        wpart = make_float4(m, sum, 0.0f, 0.0f);
-      }
-      // leave this warp's partial and count it.  Every warp counts before
-      // it releases the stage, and the last warp releases only after it has
-      // read the partials, so the next tile in this stage (which needs all
-      // eight releases) can reuse neither the count nor the partials early.
-      int last = 0;
-      if (lane == 0) {
-        S.wpart[s][warp] = wpart;
-        last = last_warp(S, s);
-        if (!last) mbar_arrive(&S.empty[s]);
-      }
-      if (__shfl_sync(0xffffffffu, last, 0)) {
-        // ---- last warp: combine the eight partials, post the tile ------------
-        float2 part;
-        float v = -INFINITY, a2 = 0.0f;
-        int i = INT_MAX;
-        if (lane < kConsumerWarps) {
-          const float4 w = S.wpart[s][lane];
-          v = w.x;
-          a2 = w.y;
-          i = __float_as_int(w.y);
-        }
-        if (tl.greedy) {
-          warp_argmax(v, i);
-          part = make_float2(v, __int_as_float(i));
-        } else {
-          warp_max_sum(v, a2, tl.sT);
-          part = make_float2(v, a2);
-          // the drafted token's logit, if this chunk holds it
-          if (lane == 0 && tl.x >= g.e0 && tl.x < g.e0 + g.cnt)
-            P.zx[static_cast<size_t>(tl.b) * P.R + tl.r] =
-                E::load(buf0 + g.h + (tl.x - g.e0) * E::kBytes);
-        }
-        __syncwarp();   // every lane has read the partials
-        if (lane == 0) {
-          mbar_arrive(&S.empty[s]);
-          P.part[(static_cast<size_t>(tl.b) * P.R + tl.r) * P.NC + tl.c] = part;
-          post_event(S, P, kEvStats, tl.b);
-        }
-      }
+    for (int q = 0; q < CH; ++q) w0[q] = w1[q] = 0.0f;
+    return;
+  }
+  const unsigned char* qbuf = slot + kDraftOff;
+  float vp[CH], vq[CH];
+  masked_vec<DT>(slot, vs, kp, j, vp);
+  if (residual) {
+    if (same) {
+      E::unpack(reinterpret_cast<const uint4*>(qbuf)[j], vq);
     } else {
-      // ---- draw tile: per-warp prefix sums of the final-draw weights ---------
-      const unsigned char* rp =
-          row_ptr<DT>(P.target, static_cast<size_t>(tl.b) * (K + 1) + tl.t, P.V);
-      const Geo gp = chunk_geo<DT>(P, rp, tl.c);
-      Geo gq = gp;
-      if (tl.residual)
-        gq = chunk_geo<DT>(P, row_ptr<DT>(P.draft, static_cast<size_t>(tl.b) * K + tl.t, P.V), tl.c);
-      float* out = P.dpart + (static_cast<size_t>(tl.b) * P.NC + tl.c) * 2 * kParts;
-      for (int sw = 0; sw < kSweeps; ++sw) {
-        const int j = sw * kConsumers + tid;
-        float s0 = 0.0f, s1 = 0.0f;
-        if (j < gp.nvec) {
-          float vp[CH], vq[CH], w0[CH], w1[CH];
-          smem_vec<DT>(buf0, gp, j, vp);
-          if (tl.residual) {
-            if (gq.h == gp.h) {
-              smem_vec<DT>(buf1, gq, j, vq);
-            } else {
-              const int i0 = vec_base<DT>(gp, j);
 #pragma unroll
-              for (int q = 0; q < CH; ++q) {
-                const int i = i0 + q;
-                vq[q] = (i >= 0 && i < gp.cnt) ? E::load(buf1 + gq.h + i * E::kBytes) : -INFINITY;
-              }
-            }
-          } else {
-#pragma unroll
-            for (int q = 0; q < CH; ++q) vq[q] = -INFINITY;
-          }
-          vec_weights<DT>(vp, vq, tl.residual, tl.Mp, tl.Mq, tl.sT, tl.ratio, w0, w1);
-#pragma unroll
-          for (int q = 0; q < CH; ++q) {
-            s0 = __fadd_rn(s0, w0[q]);
-            s1 = __fadd_rn(s1, w1[q]);
-          }
-        }
-        const float i0 = warp_incl_scan(s0, lane);
-        const float i1 = warp_incl_scan(s1, lane);
-        if (lane == 31) {
-          out[sw * kConsumerWarps + warp] = i0;
-          out[kParts + sw * kConsumerWarps + warp] = i1;
-        }
-      }
-      if (lane == 31) __threadfence();   // this warp's sums reach L2 before the post
-      __syncwarp();
-      if (lane == 0) {
-        const bool last = last_warp(S, s);   // count first, then release
-        mbar_arrive(&S.empty[s]);
-        if (last) post_event(S, P, kEvDraw, tl.b);
+      for (int q = 0; q < CH; ++q) {
+        const int e = e0 + q;
+        vq[q] = (e >= kq.e_lo && e < kq.e_hi) ? E::load(qbuf + kq.off0 + e * eb) : 0.0f;
       }
     }
+  } else {
+#pragma unroll
+    for (int q = 0; q < CH; ++q) vq[q] = 0.0f;
   }
+#pragma unroll
+  for (int q = 0; q < CH; ++q) element_weights(vp[q], vq[q], residual, prm, w0[q], w1[q]);
 }
 
-// ---------------------------------------------------------------- control
-
-// Whole warp: (max, sum) of rows [r0, r0 + nr) of request b's partials, row
-// r0 + i landing on lane lane0 + i.  The partials are staged into shared
-// memory with one lane-parallel sweep of loads, then each lane combines its
-// row in chunk order.
-__device__ void rows_combine(const Params& P, Ctl& S, const float2* part, int r0, int nr, int lane0,
-                             float sT, int lane, float& M, float& Ssum) {
-  const int NC = P.NC;
-  const int per_round = kCtlBuf / (2 * NC);
-  float2* buf = reinterpret_cast<float2*>(S.cbuf);
-  for (int g = 0; g < nr; g += per_round) {
-    const int cnt = min(per_round, nr - g);
-    for (int i = lane; i < cnt * NC; i += 32) buf[i] = __ldcg(part + static_cast<size_t>(r0 + g) * NC + i);
-    __syncwarp();
-    const int mine = lane - lane0 - g;
-    if (mine >= 0 && mine < cnt) {
-      M = -INFINITY;
-      Ssum = 0.0f;
-      for (int c = 0; c < NC; ++c) {
-        const float2 p = buf[mine * NC + c];
-        pair_combine(M, Ssum, p.x, p.y, sT);
-      }
-    }
-    __syncwarp();
-  }
-}
-
-// Whole warp: every stats tile of request b is done.  Validates the
-// request's tokens and uniforms, combines the partials of every row, runs
-// the rule's left-to-right test and either answers the request (greedy) or
-// publishes the decision for the owners of the final row's draw tiles.
+// Whole warp: the final-draw weights of a draw chunk, summed per sweep of 32
+// vectors (sweep s = vectors [32 s, 32 s + 32) of the target part), each
+// lane's elements in order, then across the warp.  Every lane returns the
+// sums in w[0..7] (mode 0) and w[8..15] (mode 1).
 template <int DT>
-__device__ void decide(const Params& P, Ctl& S, int b, int lane) {
-  const int K = P.K, R = P.R, NC = P.NC, V = P.V;
-  const int n = request_len(P, b);
-  const float T = __ldg(P.temperature + b);
-  const bool greedy = !(T > 0.0f);
-  int tok_bad = 0, u_bad = 0;
-  int x_lane = -1;
-  float u_lane = 0.0f;
-  if (lane < n) {
-    x_lane = __ldg(P.draft_tokens + static_cast<size_t>(b) * K + lane);
-    tok_bad = (x_lane < 0 || x_lane >= V);
-  }
-  if (lane <= n) {
-    u_lane = __ldg(P.uniforms + static_cast<size_t>(b) * (K + 1) + lane);
-    u_bad = !(u_lane >= 0.0f && u_lane < 1.0f);
-  }
-  const float ur = __ldg(P.uniforms_resample + b);
-  int bad = 0;
-  if (__any_sync(0xffffffffu, tok_bad)) bad |= SPECV_DEV_BAD_TOKEN;
-  if (__any_sync(0xffffffffu, u_bad) || !(ur >= 0.0f && ur < 1.0f)) bad |= SPECV_DEV_BAD_UNIFORM;
-  if (bad) {
-    finish_bad(P, b, bad, lane, S.tag);
-    return;
-  }
-  const float2* part = P.part + static_cast<size_t>(b) * R * NC;
-  float* rs = P.row_stats ? P.row_stats + static_cast<size_t>(b) * (K + 1) * 8 : nullptr;
-
-  if (greedy) {
-    // lane t: argmax of target row t (rows t <= n), chunk partials staged
-    float2* buf = reinterpret_cast<float2*>(S.cbuf);
-    const int per_round = kCtlBuf / (2 * NC);
-    float gv = -INFINITY;
-    int g = INT_MAX;
-    for (int r0 = 0; r0 <= n; r0 += per_round) {
-      const int cnt = min(per_round, n + 1 - r0);
-      for (int i = lane; i < cnt * NC; i += 32) buf[i] = __ldcg(part + static_cast<size_t>(r0) * NC + i);
-      __syncwarp();
-      const int mine = lane - r0;
-      if (mine >= 0 && mine < cnt) {
-        for (int c = 0; c < NC; ++c) {
-          const float2 p = buf[mine * NC + c];
-          const int i = __float_as_int(p.y);
-          if (better(p.x, i, gv, g)) {
-            gv = p.x;
-            g = i;
-          }
-        }
-      }
-      __syncwarp();
-    }
-    if (rs && lane <= n) {
-      rs[lane * 8 + 0] = gv;
-      rs[lane * 8 + 7] = static_cast<float>(g);
-    }
-    const unsigned miss = __ballot_sync(0xffffffffu, lane < n && g != x_lane);
-    const int j = miss ? __ffs(miss) - 1 : n;
-    const int gj = __shfl_sync(0xffffffffu, g, j);
-    if (gj < 0 || gj >= V) {
-      finish_bad(P, b, SPECV_DEV_BAD_ROW, lane, S.tag);
-      return;
-    }
-    if (lane == 0) set_state(P, b, S.tag, kStateNone);   // no draw tiles
-    finish_request(P, b, j, gj, lane);
-    return;
-  }
-
-  // ---- sampled: lane t holds target row t and draft row t ------------------
-  const float sT = temp_scale(T);
-  float Mp_l = -INFINITY, Sp_l = 0.0f, lp = 0.0f;
-  float Mq_l = -INFINITY, Sq_l = 0.0f, lq = 0.0f;
-  rows_combine(P, S, part, 0, n + 1, 0, sT, lane, Mp_l, Sp_l);
-  rows_combine(P, S, part, K + 1, n, 0, sT, lane, Mq_l, Sq_l);
-  if (lane < n) {
-    const float zp = __ldcg(P.zx + static_cast<size_t>(b) * R + lane);
-    const float zq = __ldcg(P.zx + static_cast<size_t>(b) * R + K + 1 + lane);
-    lp = __fsub_rn(__fmul_rn(__fsub_rn(zp, Mp_l), sT), log2f(Sp_l));
-    lq = __fsub_rn(__fmul_rn(__fsub_rn(zq, Mq_l), sT), log2f(Sq_l));
-  }
-  const bool row_bad = (lane <= n && !isfinite(Mp_l)) || (lane < n && !isfinite(Mq_l));
-  if (__any_sync(0xffffffffu, row_bad)) {
-    finish_bad(P, b, SPECV_DEV_BAD_ROW, lane, S.tag);
-    return;
-  }
-  bool accept = false;
-  if (lane < n) accept = __fadd_rn(log2f(u_lane), lq) < lp;
-  const unsigned rej = __ballot_sync(0xffffffffu, lane < n && !accept);
-  const int j = rej ? __ffs(rej) - 1 : n;
-  if (rs) {
-    if (lane <= n) {
-      rs[lane * 8 + 0] = Mp_l;
-      rs[lane * 8 + 1] = Sp_l;
-    }
-    if (lane < n) {
-      rs[lane * 8 + 2] = lp * kLn2;
-      rs[lane * 8 + 3] = Mq_l;
-      rs[lane * 8 + 4] = Sq_l;
-      rs[lane * 8 + 5] = lq * kLn2;
-    }
-  }
-  const float Mp = __shfl_sync(0xffffffffu, Mp_l, j);
-  const float Sp = __shfl_sync(0xffffffffu, Sp_l, j);
-  const float Mq = __shfl_sync(0xffffffffu, Mq_l, j);
-  const float Sq = __shfl_sync(0xffffffffu, Sq_l, j);
-  const float u_bonus = __shfl_sync(0xffffffffu, u_lane, n);
-  const bool residual = j < n;
-  if (lane == 0) {
-    Req& q = P.req[b];
-    q.j = j;
-    q.t_f = j;
-    q.residual = residual ? 1 : 0;
-    q.u = residual ? ur : u_bonus;
-    q.Mp = Mp;
-    q.Sp = Sp;
-    q.Mq = residual ? Mq : 0.0f;
-    q.Sq = residual ? Sq : 1.0f;
-    q.sT = sT;
-    q.ratio = residual ? __fdiv_rn(Sp, Sq) : 0.0f;
-    set_state(P, b, S.tag, kStateDraws);   // release: the fields above first
-  }
-  __syncwarp();
-}
-
-// Whole warp: totals of request b's NC chunks for weight mode `mode` into
-// S.ctot (chunk c = sum of its kParts per-warp partials, in order).
-__device__ void chunk_totals(const float* dp, int NC, int mode, Ctl& S, int lane) {
-  const int per_round = kCtlBuf / kParts;
-  for (int c0 = 0; c0 < NC; c0 += per_round) {
-    const int cnt = min(per_round, NC - c0);
-    for (int i = lane; i < cnt * kParts; i += 32) {
-      const int c = i / kParts, k = i - c * kParts;
-      S.cbuf[i] = __ldcg(dp + (static_cast<size_t>(c0 + c) * 2 + mode) * kParts + k);
-    }
-    __syncwarp();
-    for (int c = lane; c < cnt; c += 32) {
-      float tot = 0.0f;
-      for (int k = 0; k < kParts; ++k) tot = __fadd_rn(tot, S.cbuf[c * kParts + k]);
-      S.ctot[c0 + c] = tot;
-    }
-    __syncwarp();
-  }
-}
-
-// Whole warp: every draw tile of request b is done.  Locates the token from
-// the stored prefix sums and one re-read 32-vector segment.
-template <int DT>
-__device__ void search(const Params& P, Ctl& S, int b, int lane) {
-  using E = Elt<DT>;
-  constexpr int CH = E::kPerVec;
-  const int K = P.K, NC = P.NC;
-  Req q;
-  {
-    const Req* src = P.req + b;
-    q.j = __ldcg(&src->j);
-    q.t_f = __ldcg(&src->t_f);
-    q.residual = __ldcg(&src->residual);
-    q.u = __ldcg(&src->u);
-    q.Mp = __ldcg(&src->Mp);
-    q.Mq = __ldcg(&src->Mq);
-    q.sT = __ldcg(&src->sT);
-    q.ratio = __ldcg(&src->ratio);
-    q.Sp = __ldcg(&src->Sp);
-    q.Sq = __ldcg(&src->Sq);
-  }
-  const float* dp = P.dpart + static_cast<size_t>(b) * NC * 2 * kParts;
-  int mode = 0;
-  float W = 0.0f, W_report = 0.0f;
-  int owner = -1;
-  float tau_c = 0.0f;
-  for (int attempt = 0; attempt < 2; ++attempt) {
-    chunk_totals(dp, NC, mode, S, lane);
-    if (lane == 0) {
-      W = 0.0f;
-      for (int c = 0; c < NC; ++c) W = __fadd_rn(W, S.ctot[c]);
-      const float tau = __fmul_rn(q.u, W);
-      float acc = 0.0f, last_acc = 0.0f;
-      int last = -1;
-      owner = -1;
-      for (int c = 0; c < NC; ++c) {
-        const float tot = S.ctot[c];
-        if (tot > 0.0f) {
-          if (owner < 0 && __fadd_rn(acc, tot) > tau) {
-            owner = c;
-            tau_c = __fsub_rn(tau, acc);
-          }
-          last = c;
-          last_acc = acc;
-        }
-        acc = __fadd_rn(acc, tot);
-      }
-      if (owner < 0 && last >= 0) {
-        owner = last;
-        tau_c = __fsub_rn(tau, last_acc);
-      }
-    }
-    W = __shfl_sync(0xffffffffu, W, 0);
-    owner = __shfl_sync(0xffffffffu, owner, 0);
-    tau_c = __shfl_sync(0xffffffffu, tau_c, 0);
-    __syncwarp();
-    if (attempt == 0) W_report = W;
-    if (!(q.residual && !(W > 0.0f))) break;
-    mode = 1;   // a residual of exactly zero mass: draw from p
-  }
-  if (owner < 0) {
-    finish_bad(P, b, SPECV_DEV_BAD_ROW, lane, S.tag);
-    return;
-  }
-  // the (sweep, warp) segment of the owning chunk
-  for (int k = lane; k < kParts; k += 32)
-    S.cbuf[k] = __ldcg(dp + (static_cast<size_t>(owner) * 2 + mode) * kParts + k);
-  __syncwarp();
-  int sel = -1;
-  float tau_s = 0.0f;
-  if (lane == 0) {
-    float acc = 0.0f, last_acc = 0.0f;
-    int last = -1;
-    for (int k = 0; k < kParts; ++k) {
-      const float w = S.cbuf[k];
-      if (w > 0.0f) {
-        if (sel < 0 && __fadd_rn(acc, w) > tau_c) {
-          sel = k;
-          tau_s = __fsub_rn(tau_c, acc);
-        }
-        last = k;
-        last_acc = acc;
-      }
-      acc = __fadd_rn(acc, w);
-    }
-    if (sel < 0 && last >= 0) {
-      sel = last;
-      tau_s = __fsub_rn(tau_c, last_acc);
-    }
-  }
-  sel = __shfl_sync(0xffffffffu, sel, 0);
-  tau_s = __shfl_sync(0xffffffffu, tau_s, 0);
-  __syncwarp();
-  if (sel < 0) {
-    finish_bad(P, b, SPECV_DEV_BAD_ROW, lane, S.tag);
-    return;
-  }
-  // re-read the segment: lane l holds vector sweep*256 + warp*32 + l
-  const bool residual = q.residual && mode == 0;
-  const unsigned char* rp = row_ptr<DT>(P.target, static_cast<size_t>(b) * (K + 1) + q.t_f, P.V);
-  const unsigned char* rq =
-      q.residual ? row_ptr<DT>(P.draft, static_cast<size_t>(b) * K + q.t_f, P.V) : nullptr;
-  const Geo gp = chunk_geo<DT>(P, rp, owner);
-  const int j = (sel / kConsumerWarps) * kConsumers + (sel % kConsumerWarps) * 32 + lane;
-  float vp[CH], vq[CH], w0[CH], w1[CH];
-  const int i0 = vec_base<DT>(gp, j);
+__device__ __forceinline__ void chunk_draw(const unsigned char* slot, const Chunk& kp,
+                                           const Chunk& kq, bool residual, const float4& prm,
+                                           int lane, float* w) {
+  constexpr int CH = Elt<DT>::kPerVec;
+  const Vecs vs = vecs_of<DT>(kp);
+  const bool same = kq.off0 == kp.off0;   // draft elements at the target's positions
 #pragma unroll
-  for (int k = 0; k < CH; ++k) {
-    const int i = i0 + k;
-    const bool in = j < gp.nvec && i >= 0 && i < gp.cnt;
-    vp[k] = in ? E::ldg(rp + static_cast<size_t>(gp.e0 + i) * E::kBytes) : -INFINITY;
-    vq[k] = (in && residual) ? E::ldg(rq + static_cast<size_t>(gp.e0 + i) * E::kBytes) : -INFINITY;
+  for (int s = 0; s < kDrawSweeps; ++s) {
+    float w0[CH], w1[CH];
+    vector_weights<DT>(slot, vs, kp, kq, residual, same, prm, s * 32 + lane, w0, w1);
+    float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+    for (int q = 0; q < CH; ++q) {
+      s0 = __fadd_rn(s0, w0[q]);
+      s1 = __fadd_rn(s1, w1[q]);
+    }
+    w[s] = warp_sum(s0);
+    w[kDrawSweeps + s] = warp_sum(s1);
   }
-  vec_weights<DT>(vp, vq, residual, q.Mp, q.Mq, q.sT, q.ratio, w0, w1);
-  float* w = mode == 0 ? w0 : w1;
+}
+
+// Whole warp: the final draw's token inside a chunk staged in a slot.
+// `tau` is the target mass left for this chunk; sweeps (32 vectors each)
+// are summed in order as chunk_draw sums them, then lanes in order, then
+// the lane's elements.  Rounding that leaves tau beyond the chunk's mass
+// falls on the chunk's last positive element.  -1 if nothing weighs > 0.
+template <int DT>
+__device__ int draw_in_slot(const unsigned char* slot, const Chunk& kp, const Chunk& kq,
+                            bool residual, int mode, const float4& prm, float tau, int nsw,
+                            int lane) {
+  constexpr int CH = Elt<DT>::kPerVec;
+  const Vecs vs = vecs_of<DT>(kp);
+  const bool same = kq.off0 == kp.off0;
+  int found = -1, last = -1;
+  float tau_s = 0.0f, acc = 0.0f;
+  for (int s = 0; s < nsw && found < 0; ++s) {
+    float w0[CH], w1[CH];
+    vector_weights<DT>(slot, vs, kp, kq, residual, same, prm, s * 32 + lane, w0, w1);
+    float s0 = 0.0f;
+#pragma unroll
+    for (int q = 0; q < CH; ++q) s0 = __fadd_rn(s0, mode == 0 ? w0[q] : w1[q]);
+    const float sw = warp_sum(s0);
+    if (sw > 0.0f) {
+      if (__fadd_rn(acc, sw) > tau) {
+        found = s;
+        tau_s = __fsub_rn(tau, acc);
+      }
+      last = s;
+    }
+    acc = __fadd_rn(acc, sw);
+  }
+  if (found < 0) {
+    if (last < 0) return -1;
+    found = last;
+    tau_s = INFINITY;   // the sweep's last positive lane and element
+  }
+  const int j = found * 32 + lane;
+  float w0[CH], w1[CH], w[CH];
+  vector_weights<DT>(slot, vs, kp, kq, residual, same, prm, j, w0, w1);
   float sum = 0.0f;
 #pragma unroll
-  for (int k = 0; k < CH; ++k) {
-    if (!(vp[k] > -INFINITY)) w[k] = 0.0f;   // outside the chunk
-    sum = __fadd_rn(sum, w[k]);
+  for (int q = 0; q < CH; ++q) {
+    w[q] = mode == 0 ? w0[q] : w1[q];
+    sum = __fadd_rn(sum, w[q]);
   }
-  const float incl = warp_incl_scan(sum, lane);
-  const unsigned hit = __ballot_sync(0xffffffffu, sum > 0.0f && incl > tau_s);
+  const float sincl = warp_incl_scan(sum, lane);
+  const unsigned hit = __ballot_sync(0xffffffffu, sum > 0.0f && sincl > tau_s);
   const unsigned pos = __ballot_sync(0xffffffffu, sum > 0.0f);
   const int l = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : -1);
-  if (l < 0) {
-    finish_bad(P, b, SPECV_DEV_BAD_ROW, lane, S.tag);
-    return;
-  }
-  const float excl = __shfl_sync(0xffffffffu, incl - sum, l);
+  if (l < 0) return -1;
+  const float excl = __shfl_sync(0xffffffffu, __fsub_rn(sincl, sum), l);
   int tok = -1;
   if (lane == l) {
     const float tau3 = __fsub_rn(tau_s, excl);
     float run = 0.0f;
     int pick = -1, lastq = -1;
 #pragma unroll
-    for (int k = 0; k < CH; ++k) {
-      if (w[k] > 0.0f) {
-        run = __fadd_rn(run, w[k]);
-        if (pick < 0 && run > tau3) pick = k;
-        lastq = k;
+    for (int q = 0; q < CH; ++q) {
+      if (w[q] > 0.0f) {
+        run = __fadd_rn(run, w[q]);
+        if (pick < 0 && run > tau3) pick = q;
+        lastq = q;
       }
     }
     if (pick < 0) pick = lastq;
-    tok = gp.e0 + i0 + pick;
+    tok = vs.e_base + j * CH + pick;
   }
-  tok = __shfl_sync(0xffffffffu, tok, l);
+  return __shfl_sync(0xffffffffu, tok, l);
+}
+
+// ---------------------------------------------------------------- records
+
+__device__ __forceinline__ void st_record(uint2* p, uint32_t lo, uint32_t hi) {
+  const unsigned long long v = (static_cast<unsigned long long>(hi) << 32) | lo;
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ uint2 ld_record(const uint2* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return make_uint2(static_cast<uint32_t>(v), static_cast<uint32_t>(v >> 32));
+}
+
+// A nonnegative (or NaN) float with the ready bit, and back.
+__device__ __forceinline__ uint32_t ready_bits(float x) {
+  return (x != x ? 0x7FC00000u : __float_as_uint(x)) | kReady;
+}
+__device__ __forceinline__ float ready_value(uint32_t u) { return __uint_as_float(u & ~kReady); }
+
+// Whole warp: stages n records from src into dst, up to 16 loads in flight
+// per lane; true if every one of them is written.
+__device__ __forceinline__ bool stage_records(uint2* dst, const uint2* src, int n, int lane) {
+  bool ready = true;
+  for (int base = 0; base < n; base += 16 * 32) {
+    uint2 v[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const int i = base + k * 32 + lane;
+      if (i < n) v[k] = ld_record(src + i);
+    }
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const int i = base + k * 32 + lane;
+      if (i < n) {
+        dst[i] = v[k];
+        ready = ready && (v[k].y & kReady);
+      }
+    }
+  }
+  return __all_sync(0xffffffffu, ready);
+}
+
+// Whole warp: returns n records to "not written" for the next call.
+__device__ __forceinline__ void clear_records(uint2* p, int n, int lane) {
+  for (int i = lane; i < n; i += 32) p[i] = make_uint2(0u, 0u);
+}
+
+// ---------------------------------------------------------------- decisions
+
+// (max, sum) of one row from its NC staged stats records: the maximum
+// first, then the chunk sums rescaled to it, in chunk order.
+__device__ __forceinline__ void combine_row(const uint2* p, int NC, float sT, float& M, float& S) {
+  M = -INFINITY;
+  for (int c = 0; c < NC; ++c) M = fmaxf(M, __uint_as_float(p[c].x));
+  S = 0.0f;
+  if (M == -INFINITY) return;
+  for (int c = 0; c < NC; ++c) {
+    const float m = __uint_as_float(p[c].x);
+    if (m > -INFINITY) S = __fadd_rn(S, __fmul_rn(ready_value(p[c].y), scaled_exp(m, M, sT)));
+  }
+}
+
+// Argmax of one row from its staged records: chunks are in index order, so
+// the first chunk holding the maximum has the lowest index.
+__device__ __forceinline__ void argmax_row(const uint2* p, int NC, float& v, int& i) {
+  v = __uint_as_float(p[0].x);
+  i = static_cast<int>(p[0].y & ~kReady);
+  for (int c = 1; c < NC; ++c) {
+    const float m = __uint_as_float(p[c].x);
+    if (m > v) {
+      v = m;
+      i = static_cast<int>(p[c].y & ~kReady);
+    }
+  }
+}
+
+// Whole warp: stages request b's records of target rows [0, nt) and draft
+// rows [0, nd) pass by pass and combines them: lane t gets target row t
+// (Mp, Sp, or the argmax) and draft row t (Mq, Sq).  False if a record is
+// not written yet.
+__device__ bool combine_request(const Params& P, Smem& S, int b, int nt, int nd, bool greedy,
+                                float sT, int lane, float& Mp, float& Sp, float& Mq, float& Sq,
+                                int& arg) {
+  const int NC = P.NC, K = P.K;
+  uint2* buf = S.cbuf;
+  const int cap = max(1, kCtlRecords / NC);   // rows per pass
+  const uint2* rec = P.part + static_cast<size_t>(b) * P.R * NC;
+  Mp = Mq = -INFINITY;
+  Sp = Sq = 0.0f;
+  arg = INT_MAX;
+  for (int v0 = 0; v0 < nt + nd; v0 += cap) {
+    const int v1 = min(nt + nd, v0 + cap);
+    // virtual rows [v0, v1): target rows first, then draft rows
+    const int ta = v0, tb = min(v1, nt);
+    const int da = max(v0, nt) - nt, db = v1 - nt;
+    const int ntr = max(0, tb - ta);
+    bool ready = true;
+    if (ntr > 0) ready = stage_records(buf, rec + static_cast<size_t>(ta) * NC, ntr * NC, lane);
+    if (db > da)
+      ready = stage_records(buf + ntr * NC, rec + static_cast<size_t>(K + 1 + da) * NC,
+                            (db - da) * NC, lane) && ready;
+    __syncwarp();
+    if (!ready) return false;
+    if (lane >= ta && lane < tb) {
+      const uint2* p = buf + (lane - ta) * NC;
+      if (greedy) argmax_row(p, NC, Mp, arg);
+      else combine_row(p, NC, sT, Mp, Sp);
+    }
+    if (lane >= da && lane < db) combine_row(buf + (ntr + lane - da) * NC, NC, sT, Mq, Sq);
+    __syncwarp();
+  }
+  return true;
+}
+
+// Sum of one draw chunk's eight sweep sums, in sweep order.
+__device__ __forceinline__ float sweep_total(const float* w) {
+  float t = 0.0f;
+#pragma unroll
+  for (int s = 0; s < kDrawSweeps; ++s) t = __fadd_rn(t, w[s]);
+  return t;
+}
+
+// Whole warp: the chunk holding mass u * W of a draw, chunk masses
+// mass[0..n) in shared memory (lane l sums chunks [l m, l m + m) in order,
+// then the lanes are scanned).  Returns the chunk and, in rem, the target
+// mass left inside it; rounding that leaves the target beyond the total
+// falls on the last chunk with positive mass.  Sets W to the total.  -1:
+// no mass at all.
+__device__ int pick_chunk(const float* mass, int n, float u, int lane, float& W, float& rem) {
+  const int m = (n + 31) / 32;
+  const int c0 = min(n, lane * m), c1 = min(n, c0 + m);
+  float lane_tot = 0.0f;
+  for (int c = c0; c < c1; ++c) lane_tot = __fadd_rn(lane_tot, mass[c]);
+  const float incl = warp_incl_scan(lane_tot, lane);
+  W = __shfl_sync(0xffffffffu, incl, 31);
+  const float excl = __fsub_rn(incl, lane_tot);
+  const float tau = __fmul_rn(u, W);
+  const unsigned hit = __ballot_sync(0xffffffffu, lane_tot > 0.0f && incl > tau);
+  const unsigned pos = __ballot_sync(0xffffffffu, lane_tot > 0.0f);
+  const int ol = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : -1);
+  if (ol < 0) return -1;
+  int chunk = -1;
+  float r = 0.0f;
+  if (lane == ol) {
+    float acc = excl, last_acc = excl;
+    int last_c = -1;
+    for (int c = c0; c < c1 && chunk < 0; ++c) {
+      const float t = mass[c];
+      if (t > 0.0f) {
+        if (__fadd_rn(acc, t) > tau) {
+          chunk = c;
+          r = __fsub_rn(tau, acc);
+        }
+        last_c = c;
+        last_acc = acc;
+      }
+      acc = __fadd_rn(acc, t);
+    }
+    if (chunk < 0) {
+      chunk = last_c;
+      r = __fsub_rn(tau, last_acc);
+    }
+  }
+  rem = __shfl_sync(0xffffffffu, r, ol);
+  return __shfl_sync(0xffffffffu, chunk, ol);
+}
+
+// Whole warp (control): copies chunk c (of size CB) of target row rp, and
+// for a residual the matching draft elements of row rq, into the control
+// warp's buffer with bulk copies, and waits (bounded) for them.
+template <int DT>
+__device__ bool ctl_fetch(const Params& P, Smem& S, uint32_t& cphase, uintptr_t rp, uintptr_t rq,
+                          int c, int CB, bool residual, Chunk& kp, Chunk& kq, int lane) {
+  unsigned char* slot = reinterpret_cast<unsigned char*>(S.cbuf);
+  kp = chunk_of<DT>(rp, P.V, c, CB);
+  kq = residual ? draft_part<DT>(rq, kp) : kp;
+  __syncwarp();   // every lane is done with the buffer
+  if (lane == 0) {
+    uintptr_t s0 = 0, s1 = 0;
+    const uint32_t n0 = bulk_span<DT>(kp, P.t_lo, P.t_hi, &s0);
+    const uint32_t n1 = residual ? bulk_span<DT>(kq, P.d_lo, P.d_hi, &s1) : 0u;
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(&S.cbar, n0 + n1);
+    if (n0) bulk_copy_g2s(slot + (s0 - kp.g0), s0, n0, &S.cbar);
+    if (n1) bulk_copy_g2s(slot + kDraftOff + (s1 - kq.g0), s1, n1, &S.cbar);
+  }
+  const bool ok = warp_wait(&S.cbar, cphase & 1u);
+  ++cphase;
+  if (!ok && lane == 0) atomicOr(P.header + kHStatus, SPECV_DEV_TIMEOUT);
+  fix_edges<DT>(kp, P.t_lo, P.t_hi, slot, lane);
+  if (residual) fix_edges<DT>(kq, P.d_lo, P.d_hi, slot + kDraftOff, lane);
+  return ok;
+}
+
+// Whole warp: out_tokens[b] = x_0 .. x_{j-1}, tok at j (skipped if
+// skip_j), -1 after; accepted_len[b] = j.  Lane s < n holds x_s.
+__device__ __forceinline__ void write_outputs(const Params& P, int b, int j, int tok, int x_lane,
+                                              bool skip_j, int lane) {
+  if (lane <= P.K && !(skip_j && lane == j))
+    P.out_tokens[static_cast<size_t>(b) * (P.K + 1) + lane] = lane < j ? x_lane : (lane == j ? tok : -1);
+  if (lane == 0) P.accepted_len[b] = j;
+}
+
+// Whole warp (control): tries to decide request b.  Returns 0 if some of
+// its records are not written yet, 1 if the request is answered (greedy, a
+// bonus draw, or bad data), 2 if its rejected row is published for the
+// residual draw (pe filled, every output but the drawn token written).
+// Validates the request's tokens and uniforms, combines its records, runs
+// the rule's left-to-right test; a bonus draw (every draft accepted) is
+// taken at once from the final row's chunk masses, which its records give,
+// and one re-read chunk.
+template <int DT>
+__device__ __noinline__ int try_decide(const Params& P, Smem& S, uint32_t& cphase, int b, int n,
+                                       float T, int lane, uint32_t tag, Pend& pe) {
+  const int K = P.K, V = P.V, NC = P.NC, R = P.R;
+  const bool greedy = !(T > 0.0f);
+  const int nt = n + 1, nd = greedy ? 0 : n;
+  uint2* rec = P.part + static_cast<size_t>(b) * R * NC;
+  uint2* zrec = P.zx + static_cast<size_t>(b) * R;
+  int x_lane = -1;
+  float u_lane = 0.0f;
+  if (lane < n) x_lane = __ldg(P.draft_tokens + static_cast<size_t>(b) * K + lane);
+  if (lane <= n) u_lane = __ldg(P.uniforms + static_cast<size_t>(b) * (K + 1) + lane);
+  const float ur = __ldg(P.uniforms_resample + b);
+  // the drafted tokens' logits (sampled rows t < n)
+  uint2 zp_r = make_uint2(0u, kReady), zq_r = make_uint2(0u, kReady);
+  if (!greedy && lane < n) {
+    zp_r = ld_record(zrec + lane);
+    zq_r = ld_record(zrec + K + 1 + lane);
+  }
+  const float sT = greedy ? 0.0f : temp_scale(T);
+  float Mp_l, Sp_l, Mq_l, Sq_l;
+  int g;
+  if (!combine_request(P, S, b, nt, nd, greedy, sT, lane, Mp_l, Sp_l, Mq_l, Sq_l, g)) return 0;
+  const bool tok_bad = lane < n && (x_lane < 0 || x_lane >= V);
+  const bool u_bad = lane <= n && !(u_lane >= 0.0f && u_lane < 1.0f);
+  int bad = 0;
+  if (__any_sync(0xffffffffu, tok_bad)) bad |= SPECV_DEV_BAD_TOKEN;
+  if (__any_sync(0xffffffffu, u_bad) || !(ur >= 0.0f && ur < 1.0f)) bad |= SPECV_DEV_BAD_UNIFORM;
+  // a valid token's logit record is written by the item holding it
+  if (!bad && !__all_sync(0xffffffffu, (zp_r.y & kReady) && (zq_r.y & kReady))) return 0;
+
+  float* rs = P.row_stats ? P.row_stats + static_cast<size_t>(b) * (K + 1) * 8 : nullptr;
+  int result = 1;
+  if (bad) {
+    finish_bad(P, b, bad, lane, tag);
+  } else if (greedy) {
+    if (rs && lane <= n) {
+      rs[lane * 8 + 0] = Mp_l;
+      rs[lane * 8 + 7] = static_cast<float>(g);
+    }
+    const unsigned miss = __ballot_sync(0xffffffffu, lane < n && g != x_lane);
+    const int j = miss ? __ffs(miss) - 1 : n;
+    const int gj = __shfl_sync(0xffffffffu, g, j);
+    if (gj < 0 || gj >= V) {
+      finish_bad(P, b, SPECV_DEV_BAD_ROW, lane, tag);
+    } else {
+      if (lane == 0) set_state(P, b, tag, kStateNone);
+      write_outputs(P, b, j, gj, x_lane, false, lane);
+    }
+  } else {
+    // ---- sampled: lane t holds target row t and draft row t ----------------
+    const bool row_bad = (lane <= n && !isfinite(Mp_l)) || (lane < n && !isfinite(Mq_l));
+    if (__any_sync(0xffffffffu, row_bad)) {
+      finish_bad(P, b, SPECV_DEV_BAD_ROW, lane, tag);
+    } else {
+      float lp = 0.0f, lq = 0.0f;
+      if (lane < n) {
+        lp = __fsub_rn(__fmul_rn(__fsub_rn(__uint_as_float(zp_r.x), Mp_l), sT), log2f(Sp_l));
+        lq = __fsub_rn(__fmul_rn(__fsub_rn(__uint_as_float(zq_r.x), Mq_l), sT), log2f(Sq_l));
+      }
+      bool accept = false;
+      if (lane < n) accept = __fadd_rn(log2f(u_lane), lq) < lp;
+      const unsigned rej = __ballot_sync(0xffffffffu, lane < n && !accept);
+      const int j = rej ? __ffs(rej) - 1 : n;
+      if (rs) {
+        if (lane <= n) {
+          rs[lane * 8 + 0] = Mp_l;
+          rs[lane * 8 + 1] = Sp_l;
+        }
+        if (lane < n) {
+          rs[lane * 8 + 2] = lp * kLn2;
+          rs[lane * 8 + 3] = Mq_l;
+          rs[lane * 8 + 4] = Sq_l;
+          rs[lane * 8 + 5] = lq * kLn2;
+        }
+      }
+      const float Mp = __shfl_sync(0xffffffffu, Mp_l, j);
+      const float Sp = __shfl_sync(0xffffffffu, Sp_l, j);
+      const float Mq = __shfl_sync(0xffffffffu, Mq_l, j);
+      const float Sq = __shfl_sync(0xffffffffu, Sq_l, j);
+      const float u_bonus = __shfl_sync(0xffffffffu, u_lane, n);
+      if (j == n) {
+        // bonus draw from p_n: chunk masses s_c 2^((m_c - Mp) log2(e)/T)
+        const uint2* rn = rec + static_cast<size_t>(n) * NC;
+        for (int c = lane; c < NC; c += 32) {
+          const uint2 r = ld_record(rn + c);
+          const float m = __uint_as_float(r.x);
+          S.cmass[c] = m > -INFINITY ? __fmul_rn(ready_value(r.y), scaled_exp(m, Mp, sT)) : 0.0f;
+        }
+        __syncwarp();
+        float W, rem;
+        const int chunk = pick_chunk(S.cmass, NC, u_bonus, lane, W, rem);
+        const float4 prm = make_float4(Mp, 0.0f, sT, 0.0f);
+        const uintptr_t rp = row_addr<DT>(P.target, static_cast<size_t>(b) * (K + 1) + n, V);
+        int tok = -1;
+        if (chunk >= 0) {
+          Chunk kp, kq;
+          if (ctl_fetch<DT>(P, S, cphase, rp, 0, chunk, kChunkBytes, false, kp, kq, lane))
+            tok = draw_in_slot<DT>(reinterpret_cast<const unsigned char*>(S.cbuf), kp, kq, false, 0,
+                                   prm, rem, kChunkBytes / 512, lane);
+        }
+        if (rs && lane == 0) {
+          rs[n * 8 + 6] = __fdiv_rn(W, Sp);
+          rs[n * 8 + 7] = static_cast<float>(tok);
+        }
+        if (tok < 0 || tok >= V) {
+          finish_bad(P, b, SPECV_DEV_BAD_ROW, lane, tag);
+        } else {
+          if (lane == 0) set_state(P, b, tag, kStateNone);
+          write_outputs(P, b, n, tok, x_lane, false, lane);
+        }
+      } else {
+        pe.b = b;
+        pe.j = j;
+        pe.t_f = j;
+        pe.residual = 1;
+        pe.u = ur;
+        pe.Sp = Sp;
+        pe.pad0 = pe.pad1 = 0.0f;
+        pe.prm = make_float4(Mp, Mq, sT, __fdiv_rn(Sp, Sq));
+        write_outputs(P, b, j, -1, x_lane, true, lane);
+        if (lane == 0) {
+          P.req[b].prm = pe.prm;
+          set_state(P, b, tag, kStateDraws | 4u | (static_cast<uint32_t>(j) << 3));
+        }
+        result = 2;
+      }
+    }
+  }
+  // every record of the request is consumed: clear them for the next call
+  __syncwarp();
+  clear_records(rec, nt * NC, lane);
+  if (nd) clear_records(rec + static_cast<size_t>(K + 1) * NC, nd * NC, lane);
+  if (!greedy && lane < n) {
+    zrec[lane] = make_uint2(0u, 0u);
+    zrec[K + 1 + lane] = make_uint2(0u, 0u);
+  }
+  __syncwarp();
+  return result;
+}
+
+// Whole warp (control): tries to draw the final token of a request whose
+// rejected row is published.  Returns false if some of its draw records
+// are not written yet.  Picks the chunk from the records' masses (a
+// residual of exactly zero mass falls back to p, with the same uniform),
+// then re-reads that chunk and searches it.
+template <int DT>
+__device__ __noinline__ bool try_search(const Params& P, Smem& S, uint32_t& cphase, const Pend& pe,
+                                        int lane, uint32_t tag) {
+  const int K = P.K, NCd = P.NCd, b = pe.b;
+  uint2* rec = P.dpart + static_cast<size_t>(b) * NCd;
+  if (!stage_records(S.cbuf, rec, NCd, lane)) return false;
+  __syncwarp();
+  clear_records(rec, NCd, lane);
+  int mode = 0, chunk = -1;
+  float W = 0.0f, W_report = 0.0f, rem = 0.0f;
+  for (; mode < 2; ++mode) {
+    for (int c = lane; c < NCd; c += 32)
+      S.cmass[c] = mode == 0 ? ready_value(S.cbuf[c].y) : __uint_as_float(S.cbuf[c].x);
+    __syncwarp();
+    chunk = pick_chunk(S.cmass, NCd, pe.u, lane, W, rem);
+    __syncwarp();
+    if (mode == 0) W_report = W;
+    if (W > 0.0f) break;   // a residual of exactly zero mass: draw from p
+  }
+  const uintptr_t rp = row_addr<DT>(P.target, static_cast<size_t>(b) * (K + 1) + pe.t_f, P.V);
+  const uintptr_t rq = row_addr<DT>(P.draft, static_cast<size_t>(b) * K + pe.t_f, P.V);
+  int tok = -1;
+  if (chunk >= 0 && mode < 2) {
+    Chunk kp, kq;
+    if (ctl_fetch<DT>(P, S, cphase, rp, rq, chunk, kDrawBytes, true, kp, kq, lane))
+      tok = draw_in_slot<DT>(reinterpret_cast<const unsigned char*>(S.cbuf), kp, kq, true, mode,
+                             pe.prm, rem, kDrawSweeps, lane);
+  }
   if (P.row_stats && lane == 0) {
-    float* rs = P.row_stats + (static_cast<size_t>(b) * (K + 1) + q.t_f) * 8;
-    rs[6] = __fdiv_rn(W_report, q.Sp);
+    float* rs = P.row_stats + (static_cast<size_t>(b) * (K + 1) + pe.t_f) * 8;
+    rs[6] = __fdiv_rn(W_report, pe.Sp);
     rs[7] = static_cast<float>(tok);
   }
   if (tok < 0 || tok >= P.V) {
-    finish_bad(P, b, SPECV_DEV_BAD_ROW, lane, S.tag);
-    return;
+    finish_bad(P, b, SPECV_DEV_BAD_ROW, lane, tag);
+  } else if (lane == 0) {
+    P.out_tokens[static_cast<size_t>(b) * (K + 1) + pe.j] = tok;
   }
-  finish_request(P, b, q.j, tok, lane);
+  __syncwarp();
+  return true;
 }
 
-// The control warp: takes the consumers' events in runs (every event that is
-// already posted), adds each run's tiles to the request counters with one
-// atomic per request, and runs the decision or the search for a request
-// whose last tile it counted.
-template <int DT>
-__device__ void control(const Params& P, Ctl& S, int lane) {
-  int e = 0;
-  bool stop = false;
-  while (!stop) {
-    const int slot0 = e % kMailbox;
-    const uint32_t ph0 = static_cast<uint32_t>(e / kMailbox) & 1u;
-    if (!warp_wait(&S.mb_full[slot0], ph0, lane)) {
-      if (lane == 0) atomicOr(P.header + kHStatus, SPECV_DEV_TIMEOUT);
-      return;
+// ---------------------------------------------------------------- agent
+
+// Asynchronous copies global -> shared: 16 bytes from L2 (never a stale L1
+// line), 4 bytes of read-only input.  cp_async_arrive makes the barrier's
+// current phase wait for every copy this thread issued before it, as one
+// more arrival.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)),
+               "l"(__cvta_generic_to_global(src))
+               : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)),
+               "l"(__cvta_generic_to_global(src))
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// The request window of a stats cursor: lane l describes request w0 + l.
+struct Window {
+  int w0;        // first request of the window
+  int cnt;       // this lane's request: items
+  int end;       // items up to and including this lane's request (INT_MAX past B)
+  int n;         // draft length
+  float sT;      // log2(e)/T, 0 for a greedy request
+};
+
+__device__ void load_window(const Params& P, Window& w, int w0, int base, int lane) {
+  w.w0 = w0;
+  const int b = w0 + lane;
+  w.n = 0;
+  w.sT = 0.0f;
+  w.cnt = 0;
+  if (b < P.B) {
+    w.n = request_len(P, b);
+    const float T = __ldg(P.temperature + b);
+    w.cnt = request_items(P, w.n, T);
+    if (w.cnt > 0 && T > 0.0f) w.sT = temp_scale(T);
+  }
+  const int incl = warp_incl_scan_int(w.cnt, lane);
+  w.end = b < P.B ? base + incl : INT_MAX;
+}
+
+// Whole warp: maps stats item g to its request, row and chunk.  Returns
+// false when g is past the last item.
+__device__ bool map_item(const Params& P, Window& w, int g, int lane, Item& it) {
+  for (;;) {
+    const unsigned done = __ballot_sync(0xffffffffu, w.end <= g);
+    if (done != 0xffffffffu) {
+      const int i = __popc(done);   // ends are nondecreasing: `done` is a prefix
+      if (w.w0 + i >= P.B) return false;
+      const int end = __shfl_sync(0xffffffffu, w.end, i);
+      const int cnt = __shfl_sync(0xffffffffu, w.cnt, i);
+      const int n = __shfl_sync(0xffffffffu, w.n, i);
+      const float sT = __shfl_sync(0xffffffffu, w.sT, i);
+      const int local = g - (end - cnt);
+      int r = __float2int_rz(__int2float_rn(local) * P.inv_NC);   // local < 2^24: exact operands
+      if (r * P.NC > local) --r;
+      if ((r + 1) * P.NC <= local) ++r;
+      it.kind = kItemStats;
+      it.b = w.w0 + i;
+      it.c = local - r * P.NC;
+      it.row = r <= n ? r : (P.K + 1) + (r - n - 1);
+      it.mode = sT > 0.0f ? 0 : 1;
+      it.sT = sT;
+      const int t = r <= n ? r : r - n - 1;
+      it.xrow = (sT > 0.0f && t < n) ? t : -1;
+      return true;
     }
-    // gather the run (lane 0), release the mailbox slots
-    int runs = 0;
+    const int last_end = __shfl_sync(0xffffffffu, w.end, 31);
+    if (w.w0 + 32 >= P.B) return false;
+    load_window(P, w, w.w0 + 32, last_end, lane);
+  }
+}
+
+// Lane 0: stages an item into slot s of the agent's ring.  A draw item's
+// decision fields come with it (cp.async on the slot's barrier).
+template <int DT>
+__device__ void issue(const Params& P, AgentSmem& A, unsigned char* slot, int s, const Item& it) {
+  const int K = P.K;
+  uintptr_t src0 = 0, src1 = 0;
+  uint32_t n0 = 0, n1 = 0;
+  unsigned char *dst0 = slot, *dst1 = slot;
+  Item& dst = A.item[s];
+  dst.kind = it.kind;
+  dst.b = it.b;
+  dst.row = it.row;
+  dst.c = it.c;
+  dst.mode = it.mode;
+  dst.sT = it.sT;
+  dst.xrow = it.xrow;
+  dst.peek_b = it.peek_b;
+  fence_proxy_async_smem();
+  bool small = false;
+  if (it.peek_b >= 0) {   // a sample of the draw cursor's request state
+    cp_async16(&dst.peek, &P.req[it.peek_b].state);
+    small = true;
+  }
+  if (it.kind == kItemStats && it.xrow >= 0) {
+    cp_async4(&dst.x, P.draft_tokens + static_cast<size_t>(it.b) * K + it.xrow);
+    small = true;
+  }
+  if (it.kind == kItemDraw) {
+    cp_async16(&dst.prm, &P.req[it.b].prm);
+    small = true;
+  }
+  if (small) cp_async_arrive(&A.full[s]);
+  if (it.kind == kItemStats) {
+    const bool is_draft = it.row > K;
+    const uintptr_t row = is_draft
+        ? row_addr<DT>(P.draft, static_cast<size_t>(it.b) * K + (it.row - K - 1), P.V)
+        : row_addr<DT>(P.target, static_cast<size_t>(it.b) * (K + 1) + it.row, P.V);
+    const Chunk k = chunk_of<DT>(row, P.V, it.c, kChunkBytes);
+    n0 = bulk_span<DT>(k, is_draft ? P.d_lo : P.t_lo, is_draft ? P.d_hi : P.t_hi, &src0);
+    if (n0) dst0 = slot + (src0 - k.g0);
+  } else {
+    const uintptr_t rp = row_addr<DT>(P.target, static_cast<size_t>(it.b) * (K + 1) + it.row, P.V);
+    const Chunk kp = chunk_of<DT>(rp, P.V, it.c, kDrawBytes);
+    n0 = bulk_span<DT>(kp, P.t_lo, P.t_hi, &src0);
+    if (n0) dst0 = slot + (src0 - kp.g0);
+    if (it.mode) {
+      const uintptr_t rq = row_addr<DT>(P.draft, static_cast<size_t>(it.b) * K + it.row, P.V);
+      const Chunk kq = draft_part<DT>(rq, kp);
+      n1 = bulk_span<DT>(kq, P.d_lo, P.d_hi, &src1);
+      if (n1) dst1 = slot + kDraftOff + (src1 - kq.g0);
+    }
+  }
+  mbar_arrive_expect_tx(&A.full[s], n0 + n1);
+  if (n0) bulk_copy_g2s(dst0, src0, n0, &A.full[s]);
+  if (n1) bulk_copy_g2s(dst1, src1, n1, &A.full[s]);
+}
+
+// Whole warp: reduces the item in a slot and writes its record (lane 0).
+template <int DT>
+__device__ __forceinline__ void consume(const Params& P, unsigned char* slot, const Item& it,
+                                        int lane) {
+  const int K = P.K;
+  if (it.kind == kItemStats) {
+    const bool is_draft = it.row > K;
+    const uintptr_t row = is_draft
+        ? row_addr<DT>(P.draft, static_cast<size_t>(it.b) * K + (it.row - K - 1), P.V)
+        : row_addr<DT>(P.target, static_cast<size_t>(it.b) * (K + 1) + it.row, P.V);
+    const Chunk k = chunk_of<DT>(row, P.V, it.c, kChunkBytes);
+    fix_edges<DT>(k, is_draft ? P.d_lo : P.t_lo, is_draft ? P.d_hi : P.t_hi, slot, lane);
+    uint32_t lo, hi;
+    if (it.mode) {
+      const float2 r = chunk_argmax<DT>(slot, k, lane);
+      lo = __float_as_uint(r.x);
+      hi = __float_as_uint(r.y) | kReady;
+    } else {
+      const float2 r = chunk_softmax<DT>(slot, k, it.sT, lane);
+      lo = __float_as_uint(r.x);
+      hi = ready_bits(r.y);
+    }
     if (lane == 0) {
-      for (;;) {
-        const int slot = e % kMailbox;
-        const uint32_t ph = static_cast<uint32_t>(e / kMailbox) & 1u;
-        if (!mbar_test(&S.mb_full[slot], ph)) break;   // nothing more posted yet
-        const int2 evt = S.mb[slot];
-        mbar_arrive(&S.mb_empty[slot]);
-        ++e;
-        if (evt.x == kEvSentinel) {
-          stop = true;
+      st_record(P.part + (static_cast<size_t>(it.b) * P.R + it.row) * P.NC + it.c, lo, hi);
+      // the drafted token's logit, from the chunk that holds it
+      if (it.xrow >= 0 && it.x >= k.e_lo && it.x < k.e_hi)
+        st_record(P.zx + static_cast<size_t>(it.b) * P.R + it.row,
+                  __float_as_uint(Elt<DT>::load(slot + k.off0 + it.x * Elt<DT>::kBytes)), kReady);
+    }
+  } else {
+    const uintptr_t rp = row_addr<DT>(P.target, static_cast<size_t>(it.b) * (K + 1) + it.row, P.V);
+    const Chunk kp = chunk_of<DT>(rp, P.V, it.c, kDrawBytes);
+    fix_edges<DT>(kp, P.t_lo, P.t_hi, slot, lane);
+    Chunk kq = kp;
+    if (it.mode) {
+      const uintptr_t rq = row_addr<DT>(P.draft, static_cast<size_t>(it.b) * K + it.row, P.V);
+      kq = draft_part<DT>(rq, kp);
+      fix_edges<DT>(kq, P.d_lo, P.d_hi, slot + kDraftOff, lane);
+    }
+    float w[2 * kDrawSweeps];
+    chunk_draw<DT>(slot, kp, kq, it.mode != 0, it.prm, lane, w);
+    if (lane == 0)
+      st_record(P.dpart + static_cast<size_t>(it.b) * P.NCd + it.c,
+                __float_as_uint(sweep_total(w + kDrawSweeps)), ready_bits(sweep_total(w)));
+  }
+}
+
+template <int DT>
+__device__ void agent(const Params& P, AgentSmem& A, unsigned char* ring, int lane, int aid,
+                      int G, uint32_t tag) {
+  Window w;
+  load_window(P, w, 0, 0, lane);
+  int g = aid;                       // next stats item
+  bool stats_left = true;
+  const int Dtot = P.B * P.NCd;      // < 2^31 within the size limits
+  int d = aid;                       // next owned draw item
+  int cur_b = d < Dtot ? d / P.NCd : -1;   // its request
+  unsigned long long cur = 0;        // latest sample of that request's state
+  int issued = 0, consumed = 0;
+  bool ok = true;
+
+  for (;;) {
+    // ---- the draw cursor, from the latest state sample ------------------
+    bool draw_ready = false;
+    uint32_t payload = 0;
+    if (d < Dtot && (cur >> 32) == tag) {
+      const uint32_t pl = static_cast<uint32_t>(cur);
+      if ((pl & 3u) == kStateDraws) {
+        draw_ready = true;
+        payload = pl;
+        // the decision's fields were written before its state (release);
+        // the draw items read them from L2 after this
+        __threadfence();
+      } else {
+        // nothing to draw for this request: skip to an owned item past it
+        const int nb = (cur_b + 1) * P.NCd;
+        d += ((nb - d + G - 1) / G) * G;
+        cur_b = d < Dtot ? d / P.NCd : -1;
+        cur = 0;
+      }
+    }
+    // ---- top up the ring without waiting -------------------------------
+    while (issued - consumed < kSlots) {
+      Item it;
+      if (draw_ready) {
+        it.kind = kItemDraw;
+        it.b = cur_b;
+        it.row = static_cast<int>((payload >> 3) & 31u);
+        it.c = d - cur_b * P.NCd;
+        it.mode = static_cast<int>((payload >> 2) & 1u);
+        it.sT = 0.0f;
+        it.xrow = -1;
+        d += G;
+        if (d >= Dtot || d / P.NCd != cur_b) {
+          draw_ready = false;
+          cur_b = d < Dtot ? d / P.NCd : -1;
+          cur = 0;
+        }
+      } else if (stats_left) {
+        if (!map_item(P, w, g, lane, it)) {
+          stats_left = false;
+          continue;
+        }
+        g += G;
+      } else {
+        break;
+      }
+      it.peek_b = (cur_b >= 0 && !draw_ready) ? cur_b : -1;   // sample it with this item
+      const int s = issued % kSlots;
+      __syncwarp();
+      if (lane == 0) issue<DT>(P, A, ring + static_cast<size_t>(s) * kSlotBytes, s, it);
+      ++issued;
+    }
+
+    if (issued == consumed) {
+      // ring empty and no stats items left: poll the draw cursor's request
+      if (d >= Dtot) break;
+      const long long t0 = clock64();
+      cur = ld_relaxed_u64(&P.req[cur_b].state);
+      while ((cur >> 32) != tag) {
+        __nanosleep(200);
+        cur = ld_relaxed_u64(&P.req[cur_b].state);
+        if (clock64() - t0 > kWaitLimitCycles) {
+          ok = false;
           break;
         }
-        if (runs > 0 && S.run_kind[runs - 1] == evt.x && S.run_b[runs - 1] == evt.y) {
-          ++S.run_cnt[runs - 1];
-        } else {
-          S.run_kind[runs] = evt.x;
-          S.run_b[runs] = evt.y;
-          S.run_cnt[runs] = 1;
-          ++runs;
-          if (runs == kRunMax) break;
+      }
+      if (!ok) break;
+      continue;
+    }
+
+    // ---- consume the oldest slot -----------------------------------------
+    const int s = consumed % kSlots;
+    const uint32_t ph = static_cast<uint32_t>(consumed / kSlots) & 1u;
+    if (!warp_wait(&A.full[s], ph)) {
+      ok = false;
+      break;
+    }
+    const Item it = A.item[s];
+    if (it.peek_b >= 0 && it.peek_b == cur_b && (it.peek >> 32) == tag) cur = it.peek;
+    consume<DT>(P, ring + static_cast<size_t>(s) * kSlotBytes, it, lane);
+    ++consumed;
+  }
+  if (!ok && lane == 0) atomicOr(P.header + kHStatus, SPECV_DEV_TIMEOUT);
+}
+
+// ---------------------------------------------------------------- control
+
+// The control warp of CTA x decides requests x, x + grid, x + 2 grid, ... in
+// order, each once its stats records are all written, and draws the final
+// token of each decided sampled request once its draw records are written
+// (in decision order, up to kPend pending).  Requests whose length or
+// temperature is unusable are answered first.
+template <int DT>
+__device__ void control(const Params& P, Smem& S, int lane, uint32_t tag) {
+  const int x = static_cast<int>(blockIdx.x), grid = static_cast<int>(gridDim.x);
+  // this CTA's requests' tokens and uniforms into L2 now, while the memory
+  // system is idle; the decisions read them much later
+  for (int b = x + lane * grid; b < P.B; b += 32 * grid) {
+    prefetch_l2(P.draft_tokens + static_cast<size_t>(b) * P.K);
+    prefetch_l2(P.uniforms + static_cast<size_t>(b) * (P.K + 1));
+    prefetch_l2(P.uniforms_resample + b);
+  }
+  // unusable requests are answered now; greedy ones never have draw items,
+  // which their owners learn from the state
+  for (int base = x; base < P.B; base += 32 * grid) {
+    const int b = base + lane * grid;
+    int bad = 0;
+    if (b < P.B) {
+      const float T = __ldg(P.temperature + b);
+      bad = request_bad(P, request_len(P, b), T);
+      if (!bad && !(T > 0.0f)) set_state(P, b, tag, kStateNone);
+    }
+    for (unsigned m = __ballot_sync(0xffffffffu, bad != 0); m; m &= m - 1) {
+      const int i = __ffs(m) - 1;
+      finish_bad(P, base + i * grid, __shfl_sync(0xffffffffu, bad, i), lane, tag);
+    }
+  }
+  uint32_t cphase = 0;   // phases of the control warp's chunk barrier
+  int dec = x;              // next request to decide
+  int dn = 0;               // its length and temperature
+  float dT = 0.0f;
+  bool dvalid = false;
+  if (dec < P.B) {
+    dn = request_len(P, dec);
+    dT = __ldg(P.temperature + dec);
+  }
+  int ph = 0, pt = 0;       // pending draws [pt, ph)
+  long long idle_since = clock64();
+  bool ok = true;
+  while (dec < P.B || pt < ph) {
+    bool progress = false;
+    if (dec < P.B && ph - pt < kPend) {
+      dvalid = request_bad(P, dn, dT) == 0;
+      int r = 1;
+      if (dvalid) {
+        Pend pe;
+        r = try_decide<DT>(P, S, cphase, dec, dn, dT, lane, tag, pe);
+        if (r == 2) {
+          if (lane == 0) S.pend[ph % kPend] = pe;
+          ++ph;
         }
       }
-    }
-    runs = __shfl_sync(0xffffffffu, runs, 0);
-    stop = __shfl_sync(0xffffffffu, stop, 0);
-    e = __shfl_sync(0xffffffffu, e, 0);
-    __syncwarp();
-    // one atomic per run, the runs' atomics in flight together on their lanes
-    int last = 0;
-    if (lane < runs) {
-      const int kind = S.run_kind[lane], b = S.run_b[lane], cnt = S.run_cnt[lane];
-      if (kind == kEvStats) {
-        const int n = request_len(P, b);
-        const float T = __ldg(P.temperature + b);
-        const int prev = AtomicInt(P.req[b].stats_done).fetch_add(cnt, cuda::memory_order_acq_rel);
-        last = prev + cnt == request_tiles(P, n, T);
-      } else {
-        const int prev = AtomicInt(P.req[b].draw_done).fetch_add(cnt, cuda::memory_order_acq_rel);
-        last = prev + cnt == P.NC;
+      if (r) {
+        dec += grid;
+        if (dec < P.B) {
+          dn = request_len(P, dec);
+          dT = __ldg(P.temperature + dec);
+        }
+        progress = true;
       }
+      __syncwarp();
     }
-    const unsigned lasts = __ballot_sync(0xffffffffu, last);
-    __syncwarp();   // every lane reads after the acquiring lanes
-    for (int i = 0; i < runs; ++i) {
-      if (!((lasts >> i) & 1u)) continue;
-      const int kind = S.run_kind[i], b = S.run_b[i];
-      if (kind == kEvStats) decide<DT>(P, S, b, lane);
-      else search<DT>(P, S, b, lane);
+    if (pt < ph) {
+      const Pend pe = S.pend[pt % kPend];
+      if (try_search<DT>(P, S, cphase, pe, lane, tag)) {
+        ++pt;
+        progress = true;
+      }
+      __syncwarp();
     }
-    __syncwarp();
+    if (progress) {
+      idle_since = clock64();
+    } else {
+      if (clock64() - idle_since > kWaitLimitCycles) {
+        ok = false;
+        break;
+      }
+      __nanosleep(128);
+    }
   }
+  if (!ok && lane == 0) atomicOr(P.header + kHStatus, SPECV_DEV_TIMEOUT);
 }
 
 // ---------------------------------------------------------------- kernel
@@ -1360,38 +1583,32 @@ template <int DT>
 __global__ void __launch_bounds__(kThreads) verify_kernel(const Params P) {
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
-  __shared__ Ctl S;
+  __shared__ Smem S;
   extern __shared__ __align__(128) unsigned char dyn[];
 
+  if (tid < kAgents * kSlots) mbar_init(&S.ag[tid / kSlots].full[tid % kSlots], 1);
+  if (tid == 0) mbar_init(&S.cbar, 1);
   if (tid == 0) {
-    for (int s = 0; s < P.stages; ++s) {
-      mbar_init(&S.full[s], 1);
-      mbar_init(&S.empty[s], kConsumerWarps);   // each consumer warp releases
-      S.done_cnt[s] = 0;
-    }
-    S.mb_head = 0;
-    for (int i = 0; i < kMailbox; ++i) {
-      mbar_init(&S.mb_full[i], 1);
-      mbar_init(&S.mb_empty[i], 1);
-    }
-    S.tag = (static_cast<uint32_t>(P.header[kHEpoch]) + 1u) & 0x3FFFFFFFu;
+    S.tag = static_cast<uint32_t>(P.header[kHEpoch]) + 1u;
     mbar_init_fence();
   }
   __syncthreads();
 
-  if (warp == kProducerWarp)
-    producer<DT>(P, S, dyn, tid & 31);
-  else if (warp == kControlWarp)
-    control<DT>(P, S, tid & 31);
-  else
-    consumer<DT>(P, S, dyn, tid);
+  if (warp < kAgents) {
+    const int G = static_cast<int>(gridDim.x) * kAgents;
+    const int aid = warp * static_cast<int>(gridDim.x) + static_cast<int>(blockIdx.x);
+    agent<DT>(P, S.ag[warp], dyn + static_cast<size_t>(warp) * kSlots * kSlotBytes, tid & 31, aid,
+              G, S.tag);
+  } else {
+    control<DT>(P, S, tid & 31, S.tag);
+  }
 
   __syncthreads();
   if (tid == 0) {
     __threadfence();
     const int prev = atomicAdd(P.header + kHExit, 1);
     if (prev == static_cast<int>(gridDim.x) - 1) {
-      // last CTA of the launch: every ticket is taken and every request
+      // last CTA of the launch: every item is done and every request
       // answered; reset for the next call
       P.header[kHExit] = 0;
       P.header[kHEpoch] = P.header[kHEpoch] + 1;
@@ -1403,74 +1620,75 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(const Params P) {
 
 int elt_bytes(specv_dtype dt) { return dt == SPECV_BF16 ? 2 : 4; }
 
-int env_int(const char* name, int fallback) {
-  const char* v = std::getenv(name);
-  if (!v || !*v) return fallback;
-  const int x = std::atoi(v);
-  return x > 0 ? x : fallback;
-}
-
 struct Layout {
-  size_t header, req, part, zx, dpart, total;
+  size_t header, req, part, dpart, zx, total;
 };
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
-Layout ws_layout(int B, int K, int NC) {
+// Chunks per row for chunk size CB, for any 16-byte phase of the row.
+int chunks_per_row(int V, specv_dtype dt, int CB) {
+  return static_cast<int>((15 + static_cast<long long>(V) * elt_bytes(dt) + CB - 1) / CB);
+}
+
+Layout ws_layout(int B, int K, int V, specv_dtype dt) {
   const size_t R = 2 * static_cast<size_t>(K) + 1;
+  const size_t NC = chunks_per_row(V, dt, kChunkBytes);
+  const size_t NCd = chunks_per_row(V, dt, kDrawBytes);
   Layout L;
   L.header = 0;
   L.req = kHeaderBytes;
   L.part = align256(L.req + sizeof(Req) * static_cast<size_t>(B));
-  L.zx = align256(L.part + sizeof(float2) * B * R * NC);
-  L.dpart = align256(L.zx + sizeof(float) * B * R);
-  L.total = align256(L.dpart + sizeof(float) * static_cast<size_t>(B) * NC * 2 * kParts);
+  L.dpart = align256(L.part + sizeof(uint2) * B * R * NC);
+  L.zx = align256(L.dpart + sizeof(uint2) * static_cast<size_t>(B) * NCd);
+  L.total = align256(L.zx + sizeof(uint2) * static_cast<size_t>(B) * R);
   return L;
 }
 
-int chunks_per_row(int V, specv_dtype dt) {
-  const int ce = kChunkBytes / elt_bytes(dt);
-  return (V + ce - 1) / ce;
-}
-
-int stage_count() {
-  int s = env_int("SPECV_STAGES", 3);
-  if (s < 1) s = 1;
-  if (s > kMaxStages) s = kMaxStages;
-  return s;
-}
-
-// Resident CTAs per SM for a stage count, cached per device.
+// Resident CTAs of the kernel on the current device, cached per device.
 template <int DT>
-cudaError_t resident_ctas(int stages, int* out) {
+cudaError_t resident_ctas(int* out) {
   static std::mutex mu;
-  static int cache[64][kMaxStages + 1];
-  static bool attr_done[64];
+  static int cache[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(mu);
-  if (!attr_done[dev]) {
+  if (!cache[dev]) {
     e = cudaFuncSetAttribute(verify_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kMaxStages * kStageBytes);
+                             kRingBytes);
     if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
-  }
-  if (!cache[dev][stages]) {
     int per_sm = 0, sms = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, verify_kernel<DT>, kThreads,
-                                                      static_cast<size_t>(stages) * kStageBytes);
+                                                      kRingBytes);
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    cache[dev][stages] = per_sm * sms;
+    cache[dev] = per_sm * sms;
   }
-  *out = cache[dev][stages];
+  *out = cache[dev];
   return cudaSuccess;
 }
 
+cudaError_t resident_ctas_for(specv_dtype dtype, int* out) {
+  return dtype == SPECV_BF16 ? resident_ctas<SPECV_BF16>(out) : resident_ctas<SPECV_F32>(out);
+}
+
+// CTAs for a call: enough agents for the stats items of every row, at most
+// the resident count.
+int grid_for(int B, int K, int V, specv_dtype dtype, int ctas) {
+  const long long items =
+      static_cast<long long>(B) * (2 * K + 1) * chunks_per_row(V, dtype, kChunkBytes);
+  long long want = (items + kAgents - 1) / kAgents;
+  if (want < 1) want = 1;
+  return static_cast<int>(want < ctas ? want : ctas);
+}
+
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+uintptr_t up16(uintptr_t x) { return (x + 15) & ~static_cast<uintptr_t>(15); }
+uintptr_t down16(uintptr_t x) { return x & ~static_cast<uintptr_t>(15); }
 
 specv_status launch(const void* target, const void* draft, specv_dtype dtype,
                     const int32_t* draft_tokens, const int32_t* draft_len,
@@ -1493,20 +1711,15 @@ specv_status launch(const void* target, const void* draft, specv_dtype dtype,
     return SPECV_ERR_INVALID_ARG;
   if (workspace_bytes < specv_workspace_bytes(B, K, V, dtype)) return SPECV_ERR_WORKSPACE;
 
-  const int NC = chunks_per_row(V, dtype);
-  const int stages = stage_count();
   int ctas = 0;
-  cudaError_t e = dtype == SPECV_BF16 ? resident_ctas<SPECV_BF16>(stages, &ctas)
-                                      : resident_ctas<SPECV_F32>(stages, &ctas);
-  if (e != cudaSuccess || ctas < 1) return SPECV_ERR_CUDA;
-  const long long groups = static_cast<long long>(B) * (2 * K + 1) * ((NC + kGroup - 1) / kGroup);
-  const int grid = static_cast<int>(groups < ctas ? groups : ctas);
+  if (resident_ctas_for(dtype, &ctas) != cudaSuccess || ctas < 1) return SPECV_ERR_CUDA;
+  const int grid = grid_for(B, K, V, dtype, ctas);
 
-  const Layout L = ws_layout(B, K, NC);
+  const Layout L = ws_layout(B, K, V, dtype);
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   Params P;
-  P.target = target;
-  P.draft = draft;
+  P.target = static_cast<const unsigned char*>(target);
+  P.draft = static_cast<const unsigned char*>(draft);
   P.draft_tokens = draft_tokens;
   P.draft_len = draft_len;
   P.temperature = temperature;
@@ -1516,24 +1729,28 @@ specv_status launch(const void* target, const void* draft, specv_dtype dtype,
   P.K = K;
   P.V = V;
   P.R = 2 * K + 1;
-  P.NC = NC;
-  P.NG = (NC + kGroup - 1) / kGroup;
-  P.CE = kChunkBytes / static_cast<int>(eb);
-  P.stages = stages;
+  P.NC = chunks_per_row(V, dtype, kChunkBytes);
+  P.NCd = chunks_per_row(V, dtype, kDrawBytes);
+  P.inv_NC = 1.0f / static_cast<float>(P.NC);
+  const uintptr_t t0 = reinterpret_cast<uintptr_t>(target);
+  const uintptr_t d0 = reinterpret_cast<uintptr_t>(draft);
+  P.t_lo = up16(t0);
+  P.t_hi = down16(t0 + static_cast<size_t>(B) * (K + 1) * V * eb);
+  P.d_lo = draft ? up16(d0) : 0;
+  P.d_hi = draft ? down16(d0 + static_cast<size_t>(B) * K * V * eb) : 0;
   P.accepted_len = accepted_len;
   P.out_tokens = out_tokens;
   P.header = reinterpret_cast<int32_t*>(ws + L.header);
   P.req = reinterpret_cast<Req*>(ws + L.req);
-  P.part = reinterpret_cast<float2*>(ws + L.part);
-  P.zx = reinterpret_cast<float*>(ws + L.zx);
-  P.dpart = reinterpret_cast<float*>(ws + L.dpart);
+  P.part = reinterpret_cast<uint2*>(ws + L.part);
+  P.dpart = reinterpret_cast<uint2*>(ws + L.dpart);
+  P.zx = reinterpret_cast<uint2*>(ws + L.zx);
   P.row_stats = row_stats;
 
-  const size_t smem = static_cast<size_t>(stages) * kStageBytes;
   if (dtype == SPECV_BF16)
-    verify_kernel<SPECV_BF16><<<grid, kThreads, smem, stream>>>(P);
+    verify_kernel<SPECV_BF16><<<grid, kThreads, kRingBytes, stream>>>(P);
   else
-    verify_kernel<SPECV_F32><<<grid, kThreads, smem, stream>>>(P);
+    verify_kernel<SPECV_F32><<<grid, kThreads, kRingBytes, stream>>>(P);
   return cudaGetLastError() == cudaSuccess ? SPECV_OK : SPECV_ERR_CUDA;
 }
 
@@ -1575,11 +1792,11 @@ cudaError_t noalloc_scratch(void** out) {
 
 extern "C" {
 
-int specv_version(void) { return 300; }
+int specv_version(void) { return 400; }
 
 int specv_max_vocab(specv_dtype dtype) {
   if (dtype != SPECV_F32 && dtype != SPECV_BF16) return 0;
-  return kMaxChunks * (kChunkBytes / elt_bytes(dtype));
+  return kMaxRowBytes / elt_bytes(dtype);
 }
 
 const char* specv_status_string(specv_status status) {
@@ -1598,7 +1815,7 @@ size_t specv_workspace_bytes(int B, int K, int V, specv_dtype dtype) {
   if (B < 1 || K < 1 || V < 1 || B > SPECV_MAX_BATCH || K > SPECV_MAX_DRAFT ||
       (dtype != SPECV_F32 && dtype != SPECV_BF16) || V > specv_max_vocab(dtype))
     return 0;
-  return ws_layout(B, K, chunks_per_row(V, dtype)).total;
+  return ws_layout(B, K, V, dtype).total;
 }
 
 specv_status specv_workspace_init(void* workspace, size_t workspace_bytes, specv_stream_t stream) {
@@ -1722,18 +1939,13 @@ specv_status specv_launch_plan(int B, int K, int V, specv_dtype dtype, int with_
                                int32_t* out) {
   (void)with_draft;
   if (!out || specv_workspace_bytes(B, K, V, dtype) == 0) return SPECV_ERR_INVALID_ARG;
-  const int stages = stage_count();
   int ctas = 0;
-  const cudaError_t e = dtype == SPECV_BF16 ? resident_ctas<SPECV_BF16>(stages, &ctas)
-                                            : resident_ctas<SPECV_F32>(stages, &ctas);
-  if (e != cudaSuccess) return SPECV_ERR_CUDA;
-  const int NC = chunks_per_row(V, dtype);
-  const long long groups = static_cast<long long>(B) * (2 * K + 1) * ((NC + kGroup - 1) / kGroup);
-  out[0] = static_cast<int32_t>(groups < ctas ? groups : ctas);
+  if (resident_ctas_for(dtype, &ctas) != cudaSuccess) return SPECV_ERR_CUDA;
+  out[0] = grid_for(B, K, V, dtype, ctas);
   out[1] = kChunkBytes / elt_bytes(dtype);
-  out[2] = stages;
-  out[3] = NC;
-  out[4] = stages * kStageBytes;
+  out[2] = kSlots;
+  out[3] = chunks_per_row(V, dtype, kChunkBytes);
+  out[4] = kRingBytes;
   out[5] = kThreads;
   return SPECV_OK;
 }

@@ -96,3 +96,12 @@ def test_binding_refuses_cpu_tensors():
     with pytest.raises(ValueError):
         sv.spec_verify_sample(t, None, torch.zeros(2, 2, dtype=torch.int32), None,
                               torch.zeros(2), torch.zeros(2, 3), torch.zeros(2))
+
+
+def test_noalloc_rejects_shapes_beyond_its_array(L):
+    # the size check runs on the host before any pointer is used
+    B, K, V = 2048, 16, 50000
+    assert L.specv_workspace_bytes(B, K, V, 1) > _native.NOALLOC_SCRATCH_BYTES
+    rc = L.spec_verify_sample_noalloc(FAKE, FAKE, 1, FAKE, FAKE, FAKE, FAKE, FAKE, B, K, V, FAKE,
+                                      FAKE, None)
+    assert rc == 2
