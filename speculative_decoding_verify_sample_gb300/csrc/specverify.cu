@@ -118,7 +118,7 @@ struct Params {
   int32_t* header;
   Req* req;         // [B]
   uint2* part;      // [B][R][NC] stats records: (max, sum | ready) or (max, index | ready)
-  uint2* dpart;     // [B][NCd] draw records: (p mass, final-draw mass | ready)
+  uint2* dpart;     // [B][NCd] draw records: (0, residual mass | ready)
   uint2* zx;        // [B][R] records of the drafted token's logit in rows t < n: (z, ready)
   float* row_stats; // [B][K+1][8] or null
 };
@@ -433,12 +433,26 @@ __device__ __forceinline__ uint32_t bulk_span(const Chunk& k, uintptr_t lo, uint
 // Whole warp: elements of the chunk that lie outside the tensor's aligned
 // range (at most 15 bytes at either end of a tensor) are loaded by lanes.
 template <int DT>
+__device__ __noinline__ void fix_edges_slow(const Chunk& k, uintptr_t g_first, uintptr_t g_end,
+                                            uintptr_t lo, uintptr_t hi, unsigned char* slot,
+                                            int lane);
+
+template <int DT>
 __device__ __forceinline__ void fix_edges(const Chunk& k, uintptr_t lo, uintptr_t hi,
                                           unsigned char* slot, int lane) {
   constexpr int eb = Elt<DT>::kBytes;
   if (k.e_hi <= k.e_lo) return;
   const uintptr_t g_first = k.g0 + static_cast<intptr_t>(k.off0) + static_cast<intptr_t>(k.e_lo) * eb;
   const uintptr_t g_end = k.g0 + static_cast<intptr_t>(k.off0) + static_cast<intptr_t>(k.e_hi) * eb;
+  if (g_first >= lo && g_end <= hi) return;   // the common case: nothing outside
+  fix_edges_slow<DT>(k, g_first, g_end, lo, hi, slot, lane);
+}
+
+template <int DT>
+__device__ __noinline__ void fix_edges_slow(const Chunk& k, uintptr_t g_first, uintptr_t g_end,
+                                            uintptr_t lo, uintptr_t hi, unsigned char* slot,
+                                            int lane) {
+  constexpr int eb = Elt<DT>::kBytes;
   const uintptr_t h1 = g_end < lo ? g_end : lo;                 // head [g_first, h1)
   uintptr_t t0 = g_first > hi ? g_first : hi;                   // tail [t0, g_end)
   if (t0 < h1) t0 = h1;
@@ -633,6 +647,7 @@ __device__ __forceinline__ float2 chunk_softmax(const unsigned char* slot, const
   const int my_edge = lane == 0 ? vs.va : (lane == 1 ? vs.vb : -1);
   if (my_edge >= 0) masked_vec<DT>(slot, vs, k, my_edge, ev);
   typename E::MaxAcc acc;
+#pragma unroll 4
   for (int j = vs.vf0 + lane; j < vs.vf1; j += 32) acc.add(vec[j]);
   float m = acc.value();
   if (my_edge >= 0) {
@@ -643,6 +658,7 @@ __device__ __forceinline__ float2 chunk_softmax(const unsigned char* slot, const
   if (!(M > -INFINITY)) return make_float2(M, 0.0f);
   const float c = __fmul_rn(M, sT);
   float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll 2
   for (int j = vs.vf0 + lane; j < vs.vf1; j += 32) {
     float v[CH];
     E::unpack(vec[j], v);
@@ -660,43 +676,34 @@ __device__ __forceinline__ float2 chunk_softmax(const unsigned char* slot, const
   return make_float2(M, __fmul_rn(S, ex2(-__fmaf_rn(M, sT, -c))));
 }
 
-// Final-draw weights of one element: mode 0 = the residual (p - q)+ (or p at
-// the bonus position), mode 1 = p; both scaled by S_p.
-__device__ __forceinline__ void weights(float zp, float zq, bool residual, const float4& prm,
-                                        float& w0, float& w1) {
+// Final-draw weight of one element, scaled by S_p: the residual
+// (p - q)+ = max(2^((z - Mp) s) - (S_p/S_q) 2^((y - Mq) s), 0), or p =
+// 2^((z - Mp) s) (s = log2(e)/T).  A target logit of -inf (or outside the
+// chunk, where slots read -inf) weighs 0; the max with 0 also sends NaN to 0.
+__device__ __forceinline__ float weight(float zp, float zq, bool residual, const float4& prm) {
   const float ep = scaled_exp(zp, prm.x, prm.z);
-  w1 = ep;
-  w0 = residual ? fmaxf(__fmaf_rn(-prm.w, scaled_exp(zq, prm.y, prm.z), ep), 0.0f) : ep;
-}
-
-// Final-draw weights of one element; elements whose target logit is not
-// above -inf (outside the chunk, -inf or NaN) weigh 0.
-__device__ __forceinline__ void element_weights(float zp, float zq, bool residual,
-                                                const float4& prm, float& w0, float& w1) {
-  weights(zp, zq, residual, prm, w0, w1);
-  if (!(zp > -INFINITY)) w0 = w1 = 0.0f;
+  return fmaxf(residual ? __fmaf_rn(-prm.w, scaled_exp(zq, prm.y, prm.z), ep) : ep, 0.0f);
 }
 
 // Final-draw weights of vector j of a chunk staged in a slot (target part
-// at slot byte 0, draft part at kDraftOff): mode 0 in w0, mode 1 in w1.
-// The draw items and the final search both form weights here, so their
-// sums agree bit for bit.
+// at slot byte 0, draft part at kDraftOff).  The draw items and the final
+// search both form weights here, so their sums agree bit for bit.
 template <int DT>
 __device__ __forceinline__ void vector_weights(const unsigned char* slot, const Vecs& vs,
                                                const Chunk& kp, const Chunk& kq, bool residual,
-                                               bool same, const float4& prm, int j, float* w0,
-                                               float* w1) {
+                                               bool same, const float4& prm, int j, float* w) {
   using E = Elt<DT>;
   constexpr int CH = E::kPerVec, eb = E::kBytes;
   const int e0 = vs.e_base + j * CH;
   if (!(e0 + CH > kp.e_lo && e0 < kp.e_hi)) {
 #pragma unroll
-    for (int q = 0; q < CH; ++q) w0[q] = w1[q] = 0.0f;
+    for (int q = 0; q < CH; ++q) w[q] = 0.0f;
     return;
   }
   const unsigned char* qbuf = slot + kDraftOff;
   float vp[CH], vq[CH];
-  masked_vec<DT>(slot, vs, kp, j, vp);
+  if (e0 >= kp.e_lo && e0 + CH <= kp.e_hi) E::unpack(reinterpret_cast<const uint4*>(slot)[j], vp);
+  else masked_vec<DT>(slot, vs, kp, j, vp);
   if (residual) {
     if (same) {
       E::unpack(reinterpret_cast<const uint4*>(qbuf)[j], vq);
@@ -712,33 +719,31 @@ __device__ __forceinline__ void vector_weights(const unsigned char* slot, const 
     for (int q = 0; q < CH; ++q) vq[q] = 0.0f;
   }
 #pragma unroll
-  for (int q = 0; q < CH; ++q) element_weights(vp[q], vq[q], residual, prm, w0[q], w1[q]);
+  for (int q = 0; q < CH; ++q) w[q] = weight(vp[q], vq[q], residual, prm);
 }
 
-// Whole warp: the final-draw weights of a draw chunk, summed per sweep of 32
-// vectors (sweep s = vectors [32 s, 32 s + 32) of the target part), each
-// lane's elements in order, then across the warp.  Every lane returns the
-// sums in w[0..7] (mode 0) and w[8..15] (mode 1).
+// Whole warp: the final-draw mass of a draw chunk: per sweep of 32 vectors
+// (sweep s = vectors [32 s, 32 s + 32) of the target part) each lane's
+// elements in order, then across the warp, then the sweeps in order (as
+// draw_in_slot walks them).
 template <int DT>
-__device__ __forceinline__ void chunk_draw(const unsigned char* slot, const Chunk& kp,
-                                           const Chunk& kq, bool residual, const float4& prm,
-                                           int lane, float* w) {
+__device__ __forceinline__ float chunk_draw(const unsigned char* slot, const Chunk& kp,
+                                            const Chunk& kq, bool residual, const float4& prm,
+                                            int lane) {
   constexpr int CH = Elt<DT>::kPerVec;
   const Vecs vs = vecs_of<DT>(kp);
   const bool same = kq.off0 == kp.off0;   // draft elements at the target's positions
-#pragma unroll
+  float t = 0.0f;
+#pragma unroll 1
   for (int s = 0; s < kDrawSweeps; ++s) {
-    float w0[CH], w1[CH];
-    vector_weights<DT>(slot, vs, kp, kq, residual, same, prm, s * 32 + lane, w0, w1);
-    float s0 = 0.0f, s1 = 0.0f;
+    float w[CH];
+    vector_weights<DT>(slot, vs, kp, kq, residual, same, prm, s * 32 + lane, w);
+    float s0 = 0.0f;
 #pragma unroll
-    for (int q = 0; q < CH; ++q) {
-      s0 = __fadd_rn(s0, w0[q]);
-      s1 = __fadd_rn(s1, w1[q]);
-    }
-    w[s] = warp_sum(s0);
-    w[kDrawSweeps + s] = warp_sum(s1);
+    for (int q = 0; q < CH; ++q) s0 = __fadd_rn(s0, w[q]);
+    t = __fadd_rn(t, warp_sum(s0));
   }
+  return t;
 }
 
 // Whole warp: the final draw's token inside a chunk staged in a slot.
@@ -748,19 +753,18 @@ __device__ __forceinline__ void chunk_draw(const unsigned char* slot, const Chun
 // falls on the chunk's last positive element.  -1 if nothing weighs > 0.
 template <int DT>
 __device__ int draw_in_slot(const unsigned char* slot, const Chunk& kp, const Chunk& kq,
-                            bool residual, int mode, const float4& prm, float tau, int nsw,
-                            int lane) {
+                            bool residual, const float4& prm, float tau, int nsw, int lane) {
   constexpr int CH = Elt<DT>::kPerVec;
   const Vecs vs = vecs_of<DT>(kp);
   const bool same = kq.off0 == kp.off0;
   int found = -1, last = -1;
   float tau_s = 0.0f, acc = 0.0f;
   for (int s = 0; s < nsw && found < 0; ++s) {
-    float w0[CH], w1[CH];
-    vector_weights<DT>(slot, vs, kp, kq, residual, same, prm, s * 32 + lane, w0, w1);
+    float w[CH];
+    vector_weights<DT>(slot, vs, kp, kq, residual, same, prm, s * 32 + lane, w);
     float s0 = 0.0f;
 #pragma unroll
-    for (int q = 0; q < CH; ++q) s0 = __fadd_rn(s0, mode == 0 ? w0[q] : w1[q]);
+    for (int q = 0; q < CH; ++q) s0 = __fadd_rn(s0, w[q]);
     const float sw = warp_sum(s0);
     if (sw > 0.0f) {
       if (__fadd_rn(acc, sw) > tau) {
@@ -777,14 +781,11 @@ __device__ int draw_in_slot(const unsigned char* slot, const Chunk& kp, const Ch
     tau_s = INFINITY;   // the sweep's last positive lane and element
   }
   const int j = found * 32 + lane;
-  float w0[CH], w1[CH], w[CH];
-  vector_weights<DT>(slot, vs, kp, kq, residual, same, prm, j, w0, w1);
+  float w[CH];
+  vector_weights<DT>(slot, vs, kp, kq, residual, same, prm, j, w);
   float sum = 0.0f;
 #pragma unroll
-  for (int q = 0; q < CH; ++q) {
-    w[q] = mode == 0 ? w0[q] : w1[q];
-    sum = __fadd_rn(sum, w[q]);
-  }
+  for (int q = 0; q < CH; ++q) sum = __fadd_rn(sum, w[q]);
   const float sincl = warp_incl_scan(sum, lane);
   const unsigned hit = __ballot_sync(0xffffffffu, sum > 0.0f && sincl > tau_s);
   const unsigned pos = __ballot_sync(0xffffffffu, sum > 0.0f);
@@ -922,14 +923,6 @@ __device__ bool combine_request(const Params& P, Smem& S, int b, int nt, int nd,
     __syncwarp();
   }
   return true;
-}
-
-// Sum of one draw chunk's eight sweep sums, in sweep order.
-__device__ __forceinline__ float sweep_total(const float* w) {
-  float t = 0.0f;
-#pragma unroll
-  for (int s = 0; s < kDrawSweeps; ++s) t = __fadd_rn(t, w[s]);
-  return t;
 }
 
 // Whole warp: the chunk holding mass u * W of a draw, chunk masses
@@ -1119,7 +1112,7 @@ __device__ __noinline__ int try_decide(const Params& P, Smem& S, uint32_t& cphas
         if (chunk >= 0) {
           Chunk kp, kq;
           if (ctl_fetch<DT>(P, S, cphase, rp, 0, chunk, kChunkBytes, false, kp, kq, lane))
-            tok = draw_in_slot<DT>(reinterpret_cast<const unsigned char*>(S.cbuf), kp, kq, false, 0,
+            tok = draw_in_slot<DT>(reinterpret_cast<const unsigned char*>(S.cbuf), kp, kq, false,
                                    prm, rem, kChunkBytes / 512, lane);
         }
         if (rs && lane == 0) {
@@ -1151,8 +1144,14 @@ __device__ __noinline__ int try_decide(const Params& P, Smem& S, uint32_t& cphas
     }
   }
   // every record of the request is consumed: clear them for the next call
+  // (a residual draw keeps its target row's, for the search's fallback to p)
   __syncwarp();
-  clear_records(rec, nt * NC, lane);
+  if (result == 2) {
+    clear_records(rec, pe.t_f * NC, lane);
+    clear_records(rec + static_cast<size_t>(pe.t_f + 1) * NC, (nt - pe.t_f - 1) * NC, lane);
+  } else {
+    clear_records(rec, nt * NC, lane);
+  }
   if (nd) clear_records(rec + static_cast<size_t>(K + 1) * NC, nd * NC, lane);
   if (!greedy && lane < n) {
     zrec[lane] = make_uint2(0u, 0u);
@@ -1164,37 +1163,51 @@ __device__ __noinline__ int try_decide(const Params& P, Smem& S, uint32_t& cphas
 
 // Whole warp (control): tries to draw the final token of a request whose
 // rejected row is published.  Returns false if some of its draw records
-// are not written yet.  Picks the chunk from the records' masses (a
-// residual of exactly zero mass falls back to p, with the same uniform),
-// then re-reads that chunk and searches it.
+// are not written yet.  Picks the chunk from the records' residual masses
+// and searches it, re-read; a residual of exactly zero mass falls back to
+// drawing from p with the same uniform, its chunk masses taken from the
+// row's stats records (kept for this) and a stats-sized chunk re-read.
 template <int DT>
 __device__ __noinline__ bool try_search(const Params& P, Smem& S, uint32_t& cphase, const Pend& pe,
                                         int lane, uint32_t tag) {
-  const int K = P.K, NCd = P.NCd, b = pe.b;
+  const int K = P.K, NCd = P.NCd, NC = P.NC, b = pe.b;
   uint2* rec = P.dpart + static_cast<size_t>(b) * NCd;
   if (!stage_records(S.cbuf, rec, NCd, lane)) return false;
   __syncwarp();
   clear_records(rec, NCd, lane);
-  int mode = 0, chunk = -1;
-  float W = 0.0f, W_report = 0.0f, rem = 0.0f;
-  for (; mode < 2; ++mode) {
-    for (int c = lane; c < NCd; c += 32)
-      S.cmass[c] = mode == 0 ? ready_value(S.cbuf[c].y) : __uint_as_float(S.cbuf[c].x);
-    __syncwarp();
-    chunk = pick_chunk(S.cmass, NCd, pe.u, lane, W, rem);
-    __syncwarp();
-    if (mode == 0) W_report = W;
-    if (W > 0.0f) break;   // a residual of exactly zero mass: draw from p
-  }
+  for (int c = lane; c < NCd; c += 32) S.cmass[c] = ready_value(S.cbuf[c].y);
+  __syncwarp();
+  float W, rem;
+  int chunk = pick_chunk(S.cmass, NCd, pe.u, lane, W, rem);
+  __syncwarp();
+  const float W_report = W;
   const uintptr_t rp = row_addr<DT>(P.target, static_cast<size_t>(b) * (K + 1) + pe.t_f, P.V);
   const uintptr_t rq = row_addr<DT>(P.draft, static_cast<size_t>(b) * K + pe.t_f, P.V);
+  uint2* srec = P.part + (static_cast<size_t>(b) * P.R + pe.t_f) * NC;
   int tok = -1;
-  if (chunk >= 0 && mode < 2) {
-    Chunk kp, kq;
-    if (ctl_fetch<DT>(P, S, cphase, rp, rq, chunk, kDrawBytes, true, kp, kq, lane))
-      tok = draw_in_slot<DT>(reinterpret_cast<const unsigned char*>(S.cbuf), kp, kq, true, mode,
-                             pe.prm, rem, kDrawSweeps, lane);
+  Chunk kp, kq;
+  if (W > 0.0f) {
+    if (chunk >= 0 && ctl_fetch<DT>(P, S, cphase, rp, rq, chunk, kDrawBytes, true, kp, kq, lane))
+      tok = draw_in_slot<DT>(reinterpret_cast<const unsigned char*>(S.cbuf), kp, kq, true, pe.prm,
+                             rem, kDrawSweeps, lane);
+  } else {
+    // a residual of exactly zero mass: p's chunk masses from the stats records
+    const float Mp = pe.prm.x, sT = pe.prm.z;
+    for (int c = lane; c < NC; c += 32) {
+      const uint2 r = ld_record(srec + c);
+      const float m = __uint_as_float(r.x);
+      S.cmass[c] = m > -INFINITY ? __fmul_rn(ready_value(r.y), scaled_exp(m, Mp, sT)) : 0.0f;
+    }
+    __syncwarp();
+    float Wp;
+    chunk = pick_chunk(S.cmass, NC, pe.u, lane, Wp, rem);
+    const float4 prm = make_float4(Mp, 0.0f, sT, 0.0f);
+    if (chunk >= 0 && ctl_fetch<DT>(P, S, cphase, rp, 0, chunk, kChunkBytes, false, kp, kq, lane))
+      tok = draw_in_slot<DT>(reinterpret_cast<const unsigned char*>(S.cbuf), kp, kq, false, prm,
+                             rem, kChunkBytes / 512, lane);
   }
+  __syncwarp();
+  clear_records(srec, NC, lane);
   if (P.row_stats && lane == 0) {
     float* rs = P.row_stats + (static_cast<size_t>(b) * (K + 1) + pe.t_f) * 8;
     rs[6] = __fdiv_rn(W_report, pe.Sp);
@@ -1382,11 +1395,8 @@ __device__ __forceinline__ void consume(const Params& P, unsigned char* slot, co
       kq = draft_part<DT>(rq, kp);
       fix_edges<DT>(kq, P.d_lo, P.d_hi, slot + kDraftOff, lane);
     }
-    float w[2 * kDrawSweeps];
-    chunk_draw<DT>(slot, kp, kq, it.mode != 0, it.prm, lane, w);
-    if (lane == 0)
-      st_record(P.dpart + static_cast<size_t>(it.b) * P.NCd + it.c,
-                __float_as_uint(sweep_total(w + kDrawSweeps)), ready_bits(sweep_total(w)));
+    const float t = chunk_draw<DT>(slot, kp, kq, it.mode != 0, it.prm, lane);
+    if (lane == 0) st_record(P.dpart + static_cast<size_t>(it.b) * P.NCd + it.c, 0u, ready_bits(t));
   }
 }
 
