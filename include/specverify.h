@@ -106,10 +106,12 @@ int specv_max_vocab(specv_dtype dtype);
 const char* specv_status_string(specv_status status);
 
 /* Bytes of device workspace one call over B requests of up to K drafts of
- * a V-entry vocabulary needs: a header (status word, tile tickets, draw
- * queue counters, a call counter), 64 bytes of state per request, one
- * partial per (row, 16 KB chunk), the final-draw partial sums and the draw
- * queue.  Returns 0 for sizes out of range. */
+ * a V-entry vocabulary needs: a header (status word, ticket and exit
+ * counters, the residual list's length), 32 bytes of state per request, one
+ * record per (row, 12 KB chunk), the drafted tokens' logits, the residual
+ * list and one residual sum per (request, 6 KB piece).  Batches of more than
+ * 1024 requests run as consecutive launch sequences that share it, so it is
+ * sized for at most 1024 requests.  Returns 0 for sizes out of range. */
 size_t specv_workspace_bytes(int B, int K, int V, specv_dtype dtype);
 
 /* Zero a workspace on `stream` (cudaMemsetAsync).  Must run once before the
@@ -136,7 +138,9 @@ specv_status specv_workspace_init(void* workspace, size_t workspace_bytes, specv
  *   workspace         specv_workspace_bytes(B, K, V, dtype) bytes, 256-byte aligned,
  *                     zeroed once with specv_workspace_init.  Calls that may
  *                     run concurrently need separate workspaces.
- * Enqueues one kernel on `stream`; no host synchronisation.
+ * Enqueues three kernels on `stream` per 1024 requests (row statistics,
+ * decisions, residual draws; the second and third as programmatic dependent
+ * launches); no host synchronisation.
  */
 specv_status spec_verify_sample(const void* target_logits, const void* draft_logits,
                                 specv_dtype dtype, const int32_t* draft_tokens,
@@ -198,7 +202,7 @@ specv_status spec_verify_sample_host(const void* target_logits, const void* draf
                                      specv_stream_t stream);
 
 /* The launch shape the library picks for these sizes (diagnostics): out[0]
- * CTAs launched (persistent), out[1] vocabulary elements per chunk (tile),
+ * CTAs of the row-statistics kernel, out[1] vocabulary elements per chunk,
  * out[2] shared-memory stages per CTA, out[3] chunks per row, out[4]
  * dynamic shared memory per CTA (bytes), out[5] threads per CTA.  Queries
  * the current device's occupancy; launches nothing. */

@@ -8,33 +8,32 @@
 // draft is accepted draw a bonus token from p at the next position; at
 // temperature 0 compare argmax(p) with the draft instead.
 //
-// Design.  Every warp of the grid is an independent agent.  The logits a
-// call needs are cut into items of one 8 KB chunk of one row ("stats"
-// items), numbered request by request, and agent a takes items a, a + G,
-// a + 2G, ... (G agents).  An agent streams its items through a private ring
-// of three shared-memory slots with TMA bulk copies, each slot completing on
-// its own mbarrier, and reduces each chunk alone to a partial: the chunk's
-// maximum and sum of exp((z - max)/T), or at T = 0 its maximum and the
-// lowest index holding it.  It then counts the item on the request's
-// counter in global memory.  The agent whose count completes a request
-// combines the request's partials, runs the left-to-right accept test and
-// either answers the request (greedy, or bad data) or publishes the final
-// row for the draw.  The final row (the residual (p - q)+ at a rejected
-// position, p at the bonus position) is read again as "draw" items of 4 KB
-// of target and draft each; draw item d of the request-major draw space
-// belongs to agent d mod G, which polls the request's state between its
-// stats items.  A draw item stores per-sweep sums of the final-draw weights;
-// the agent whose count completes the draw locates the token from them,
-// re-reading one 512-byte segment, and writes the outputs.
+// Design: three kernels on the caller's stream, the second and third
+// launched as programmatic dependents so their launch overlaps the previous
+// kernel's tail.
 //
-// No agent waits on another while it still has stats items: a wait for a
-// decision happens only once its own ring is empty and its counts are
-// flushed, so every wait ends.  Every wait is also bounded in time and sets
-// a status bit when it gives up.  Each needed logit is read from HBM once;
-// the final row of a sampled request is read a second time, normally from
-// L2, because items run request by request.
+//  1. stats_kernel streams every row a request needs (target rows t <= n,
+//     draft rows t < n when sampled) once from HBM with TMA bulk copies,
+//     in 12 KB chunks.  Each warp is an agent with a private ring of two
+//     shared-memory slots; a CTA's warps take chunks in order from a
+//     shared-memory queue that one warp at a time refills by claiming a
+//     block of tickets from a global counter and decoding it, one ticket
+//     per lane.  A chunk is reduced to a record: its maximum and sum of
+//     exp((z - max)/T), or at T = 0 its maximum and lowest argmax.  The
+//     chunk holding a drafted token also records that token's logit.
+//  2. decide_kernel, one warp per request, combines the records, runs the
+//     left-to-right accept test (or the greedy comparison) and writes the
+//     outputs.  A bonus draw is taken here: the chunk from the row's
+//     records, the token from one re-read chunk.  A rejected sampled
+//     request is appended to a list for the residual draw.
+//  3. residual_kernel reads the rejected rows again (target and draft, in
+//     6 KB pieces), sums (p - q)+ per piece, and the warp that completes a
+//     request's pieces draws its token: the piece from the sums, the token
+//     from one re-read piece pair.
+//
+// Every wait (a bulk copy, the queue, a record another warp writes) is
+// bounded in time and sets a status bit when it gives up.
 
-#include <cuda/atomic>
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -49,54 +48,56 @@
 namespace {
 
 constexpr int kAgents = 8;                              // agent warps per CTA
-constexpr int kThreads = (kAgents + 1) * 32;            // + the control warp
+constexpr int kThreads = kAgents * 32;
 constexpr int kSlots = 2;                               // ring slots per agent
-constexpr int kChunkBytes = 12288;                      // stats item: one chunk of one row
-constexpr int kDrawBytes = 4096;                        // draw item: this much of the target row
+constexpr int kChunkBytes = 12288;                      // deciding / bonus item: one chunk of one row
+constexpr int kDrawBytes = 6144;                        // residual item: this much of each row
 constexpr int kDrawSweeps = kDrawBytes / 512;           // 32 lanes x 16 bytes per sweep
-constexpr int kDraftOff = kDrawBytes;                   // draft part of a draw slot
-constexpr int kSlotBytes = kChunkBytes + 32;            // >= kDraftOff + kDrawBytes + 16
-constexpr int kMassMax = 520;                           // chunks per row, either size
+constexpr int kDraftOff = kDrawBytes;                   // draft part of a residual slot
+constexpr int kSlotBytes = kChunkBytes + 32;
 constexpr int kRingBytes = kAgents * kSlots * kSlotBytes;
-constexpr int kCtlRecords = 2080;                       // control-warp staging (8-byte records)
-constexpr int kPend = 16;                               // decided requests awaiting their draw
+constexpr int kPlanMax = 1024;                          // requests per launch (the host splits)
+constexpr int kDecideWarps = 8;                         // decide_kernel: one warp per request
+constexpr int kBlockMax = 32;                           // tickets a warp claims at once, at most
 constexpr int kMaxRowBytes = 1 << 21;                   // 2 MB per row of logits
+constexpr int kMaxChunks = (kMaxRowBytes + 15 + kChunkBytes - 1) / kChunkBytes;
+constexpr int kMaxDrawChunks = (kMaxRowBytes + 15 + kDrawBytes - 1) / kDrawBytes;
 constexpr long long kWaitLimitCycles = 4000000000ll;    // ~2 s at 2 GHz
 constexpr uint32_t kSuspendHintNs = 20000;
 
-static_assert(kSlotBytes >= kDraftOff + kDrawBytes + 16, "draw slot too small");
+static_assert(kSlotBytes >= kDraftOff + kDrawBytes + 16, "residual slot too small");
 static_assert(kSlotBytes % 16 == 0, "slots must keep 16-byte alignment");
-static_assert(kDrawSweeps == 8, "a draw chunk has eight sweeps");
-static_assert(kCtlRecords >= 513, "the draw records of a 2 MB row fit the staging buffer");
-static_assert(kCtlRecords * 8 >= kChunkBytes + 16 && kCtlRecords * 8 >= kDraftOff + kDrawBytes + 16,
-              "a chunk of logits fits the control warp's buffer");
-static_assert(kMassMax >= (kMaxRowBytes + 15) / kDrawBytes + 1, "chunk masses of a 2 MB row fit");
+static_assert(kMaxChunks * 8 <= kSlotBytes, "the records of one row fit a slot");
+static_assert(kMaxChunks <= 6 * 32, "the chunk masses of a row fit six per lane");
+static_assert(kMaxDrawChunks * 4 <= kSlotBytes, "the residual masses of one row fit a slot");
+static_assert(kMaxDrawChunks < 512 && kMaxChunks < 512, "a chunk index fits 9 bits");
+static_assert(kPlanMax <= 1024 && 2 * SPECV_MAX_DRAFT + 1 < 64, "a request fits 10 bits, a row 6");
 
-// workspace header words, one 128-byte line each
-constexpr int kHStatus = 0, kHExit = 32, kHEpoch = 64;
-constexpr int kHeaderBytes = 512;
+// workspace header words (int32 index), one 128-byte line each
+constexpr int kHStatus = 0, kHExit = 32, kHTicket = 64, kHResid = 96, kHExit3 = 128;
+constexpr int kHeaderBytes = 1024;
+static_assert((kHExit3 + 1) * 4 <= kHeaderBytes, "header words fit the header");
 
-// per-request decision state: (call tag << 32) | payload, payload =
-// kind | residual << 2 | final row << 3
-constexpr uint32_t kStateDraws = 1, kStateNone = 2;
-
-// A record is one 8-byte word written at once; bit 31 of its high half is
-// set in every written record, so a zero record is "not written yet".
+// Residual mass records are written with one store each, and bit 31 is set
+// in every written record, so a zero record is "not written yet".  The
+// warp that reads them returns them to zero.
 constexpr uint32_t kReady = 0x80000000u;
 
-constexpr int kItemStats = 1, kItemDraw = 2;
+constexpr int kItemA = 1, kItemR = 3;
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-// Per-request record in the workspace (64 bytes).
+// Per-request state in the workspace (32 bytes): the residual draw's
+// parameters, written by the decision.
 struct __align__(16) Req {
-  unsigned long long state;   // decision, tagged with the call
-  int pad0[6];
-  float4 prm;                 // final row: Mp, Mq, log2(e)/T, S_p/S_q
-  float pad1[4];
+  int j;          // the rejected row
+  int cnt;        // residual pieces summed (returns to zero)
+  float Sp_j;     // S_p of the rejected row
+  int pad;
+  float4 prm;     // Mp, Mq, log2(e)/T, S_p/S_q of the rejected row
 };
-static_assert(sizeof(Req) == 64, "Req is one 64-byte record");
+static_assert(sizeof(Req) == 32, "Req is one 32-byte record");
 
 struct Params {
   const unsigned char* target;
@@ -109,7 +110,7 @@ struct Params {
   int B, K, V;
   int R;            // record rows per request: K+1 target, then K draft
   int NC;           // stats chunks per row
-  int NCd;          // draw chunks per row
+  int NCd;          // residual pieces per row
   float inv_NC;     // 1 / NC
   // 16-byte-aligned address ranges the bulk copies may read
   uintptr_t t_lo, t_hi, d_lo, d_hi;
@@ -117,49 +118,58 @@ struct Params {
   int32_t* out_tokens;
   int32_t* header;
   Req* req;         // [B]
-  uint2* part;      // [B][R][NC] stats records: (max, sum | ready) or (max, index | ready)
-  uint2* dpart;     // [B][NCd] draw records: (0, residual mass | ready)
-  uint2* zx;        // [B][R] records of the drafted token's logit in rows t < n: (z, ready)
+  uint2* part;      // [B][R][NC] chunk records: (max, sum) or (max, index)
+  float* zx;        // [B][R] the drafted token's logit in rows t < n
+  int32_t* rlist;   // [B] requests waiting for a residual draw (count: header[kHResid])
+  uint32_t* dmass;  // [B][NCd] residual mass records: mass | ready
   float* row_stats; // [B][K+1][8] or null
 };
 
-// One item as its agent staged it (48 bytes).
+// The call's plan, built by every CTA of the stats kernel: the rows each
+// request needs (prefix sums) and its length.
+struct Plan {
+  int rb[kPlanMax + 1];       // rows before request b
+  uint8_t info[kPlanMax];     // draft length | 0x80 if the request samples (0: unusable)
+  int total;                  // tickets: chunks of every needed row
+};
+
+// One item as its agent staged it.
 struct __align__(16) Item {
-  int kind;     // kItemStats / kItemDraw
+  int kind;     // kItemA (a stats chunk) / kItemR (a residual piece pair)
   int b;
-  int row;      // stats: t (target) or K+1+t (draft); draw: final row t
+  int row;      // record row: t (target) or K+1+t (draft); residual: the rejected t
   int c;        // chunk
-  int mode;     // stats: greedy; draw: residual
-  float sT;     // stats: log2(e)/T
-  int xrow;     // stats: t if the row's drafted token x_t is needed, else -1
-  int peek_b;   // request whose state `peek` samples (-1: none)
-  // copied in with the slot (cp.async on the slot's barrier):
-  unsigned long long peek;   // state of request peek_b when the item was staged
-  unsigned long long peek_pad;
-  int x;                     // x_t (when xrow >= 0)
-  int pad[3];
-  float4 prm;   // draw: the decision's Mp, Mq, log2(e)/T, S_p/S_q
+  int n;        // the request's draft length
+  float sT;     // log2(e)/T (0: greedy)
+  int x;        // drafted token of the row (rows t < n of sampled requests), else -1
+  int pad;
+  float4 prm;   // residual: the decision's Mp, Mq, log2(e)/T, S_p/S_q
 };
 
 struct AgentSmem {
-  uint64_t full[kSlots];
-  Item item[kSlots];
+  uint64_t bar[kSlots];
+  Item item[kSlots];   // the items in the slots
 };
 
-// A decided request whose final draw is pending (the control warp's).
-struct __align__(16) Pend {
-  int b, j, t_f, residual;
-  float u, Sp, pad0, pad1;
-  float4 prm;
+// The CTA's queue of decoded items, in ticket order.  A warp that finds it
+// short takes the lock, claims the next block of tickets from the global
+// counter and decodes it, one ticket per lane.
+constexpr int kFifo = 64;
+constexpr int kFifoLow = 16;   // refill when fewer items than this are ready
+struct Fifo {
+  uint4 e[kFifo];
+  int head;     // entries reserved by warps
+  int tail;     // entries published
+  int lock;     // a warp is refilling
+  int closed;   // the last ticket is claimed
+  int last;     // first ticket of this CTA's last claim
 };
 
 struct Smem {
+  Plan plan;
+  Fifo fifo;
   AgentSmem ag[kAgents];
-  alignas(128) uint2 cbuf[kCtlRecords];   // control warp: staged records, or a chunk of logits
-  uint64_t cbar;                          // control warp: its chunk copies
-  float cmass[kMassMax];     // control warp: chunk masses of a final draw
-  Pend pend[kPend];
-  uint32_t tag;
+  int red[kAgents * 2];
 };
 
 // ---------------------------------------------------------------- elements
@@ -301,16 +311,6 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, uintptr_t src, uint32_t
           "r"(smem_addr(dst)),
       "l"(gsrc), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
-}
-
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(__cvta_generic_to_global(p)));
-}
-
-__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
-  unsigned long long v;
-  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
 }
 
 // 2^x on the MUFU unit (PTX ex2.approx.ftz.f32); -inf -> +0.
@@ -523,46 +523,129 @@ __device__ __forceinline__ int request_bad(const Params& P, int n, float T) {
   return 0;
 }
 
-// Stats items of a request: target rows t <= n, draft rows t < n when
-// sampled, every chunk; none if its length or temperature is unusable.
-__device__ __forceinline__ int request_items(const Params& P, int n, float T) {
-  if (request_bad(P, n, T)) return 0;
-  return ((n + 1) + (T > 0.0f ? n : 0)) * P.NC;
-}
-
 __device__ __forceinline__ int request_len(const Params& P, int b) {
   return P.draft_len ? __ldg(P.draft_len + b) : P.K;
 }
 
-// Whole warp: writes a request's outputs.
-__device__ void finish_request(const Params& P, int b, int j, int tok, int lane) {
-  const int K = P.K;
-  int32_t* out = P.out_tokens + static_cast<size_t>(b) * (K + 1);
-  for (int s = lane; s <= K; s += 32) {
-    int v = -1;
-    if (j < 0) v = -1;
-    else if (s < j) v = __ldg(P.draft_tokens + static_cast<size_t>(b) * K + s);
-    else if (s == j) v = tok;
-    out[s] = v;
-  }
+// Rows a usable request needs: target rows t <= n, and draft rows t < n
+// when it samples.
+__device__ __forceinline__ int request_rows(int n, float T) { return T > 0.0f ? 2 * n + 1 : n + 1; }
+
+// Record row of a request's row slot: a sampled request's first 2n slots
+// alternate target row t and draft row t, slot 2n is target row n; a greedy
+// request's slots are its target rows.
+__device__ __forceinline__ int slot_row(int slot, bool sampled, int n, int K) {
+  if (!sampled || slot == 2 * n) return sampled ? n : slot;
+  return (slot & 1) ? K + 1 + (slot >> 1) : (slot >> 1);
+}
+
+// Whole warp: out_tokens[b] = x_0 .. x_{j-1}, tok at j, -1 after;
+// accepted_len[b] = j (j = -1: every entry -1).  Lane s < j holds x_s.
+__device__ __forceinline__ void write_outputs(const Params& P, int b, int j, int tok, int x_lane,
+                                              int lane) {
+  for (int s = lane; s <= P.K; s += 32)
+    P.out_tokens[static_cast<size_t>(b) * (P.K + 1) + s] =
+        j < 0 ? -1 : (s < j ? x_lane : (s == j ? tok : -1));
   if (lane == 0) P.accepted_len[b] = j;
-  __syncwarp();
 }
 
-// Publishes request b's decision for the agents that own its draw items.
-__device__ __forceinline__ void set_state(const Params& P, int b, uint32_t tag, uint32_t payload) {
-  cuda::atomic_ref<unsigned long long, cuda::thread_scope_device>(P.req[b].state)
-      .store((static_cast<unsigned long long>(tag) << 32) | payload, cuda::memory_order_release);
-}
+// ---------------------------------------------------------------- plan
 
-__device__ void finish_bad(const Params& P, int b, int bits, int lane, uint32_t tag) {
-  if (lane == 0) {
-    atomicOr(P.header + kHStatus, bits);
-    set_state(P, b, tag, kStateNone);
+// Whole CTA: builds the call's plan: the rows each request needs, as
+// prefix sums.  A request whose length or temperature is unusable needs no
+// rows (the decision kernel answers it).
+__device__ void build_plan(const Params& P, Plan& pl, int* red) {
+  const int tid = static_cast<int>(threadIdx.x), lane = tid & 31, w = tid >> 5;
+  const int B = P.B;
+  const int per = (B + kThreads - 1) / kThreads;
+  const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
+  int rows = 0;
+  for (int b = b0; b < b1; ++b) {
+    const int n = request_len(P, b);
+    const float T = __ldg(P.temperature + b);
+    if (!request_bad(P, n, T)) rows += request_rows(n, T);
   }
-  finish_request(P, b, -1, -1, lane);
+  const int ir = warp_incl_scan_int(rows, lane);
+  if (lane == 31) red[w] = ir;
+  __syncthreads();
+  int r = ir - rows, tr = 0;
+#pragma unroll
+  for (int k = 0; k < kAgents; ++k) {
+    if (k < w) r += red[k];
+    tr += red[k];
+  }
+  for (int b = b0; b < b1; ++b) {
+    const int n = request_len(P, b);
+    const float T = __ldg(P.temperature + b);
+    const bool bad = request_bad(P, n, T) != 0;
+    pl.rb[b] = r;
+    pl.info[b] = static_cast<uint8_t>(bad ? 0 : (n | (T > 0.0f ? 0x80 : 0)));
+    if (!bad) r += request_rows(n, T);
+  }
+  if (tid == 0) {
+    pl.rb[B] = tr;
+    pl.total = tr * P.NC;
+  }
+  __syncthreads();
 }
 
+// m / NC for 0 <= m < 2^24: a float estimate (exact operands) corrected by
+// one either way.
+__device__ __forceinline__ int div_nc(const Params& P, int m) {
+  int r = __float2int_rz(__int2float_rn(m) * P.inv_NC);
+  if (r * P.NC > m) --r;
+  if ((r + 1) * P.NC <= m) ++r;
+  return r;
+}
+
+// Number of entries of a[0, n) that are <= x, for nondecreasing a.
+__device__ __forceinline__ int count_le(const int* a, int n, int x) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (a[mid] <= x) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
+}
+
+// A decoded item in 16 bytes: kind << 28 | b << 15 | row << 9 | chunk, the
+// drafted token of the row (or -1), log2(e)/T (0: greedy), draft length.
+__device__ __forceinline__ uint4 pack_item(int kind, int b, int row, int c, int x, float sT, int n) {
+  return make_uint4((static_cast<uint32_t>(kind) << 28) | (static_cast<uint32_t>(b) << 15) |
+                        (static_cast<uint32_t>(row) << 9) | static_cast<uint32_t>(c),
+                    static_cast<uint32_t>(x), __float_as_uint(sT), static_cast<uint32_t>(n));
+}
+__device__ __forceinline__ Item unpack_item(uint4 e) {
+  Item it;
+  it.kind = static_cast<int>(e.x >> 28);
+  it.b = static_cast<int>((e.x >> 15) & 0x3FFu);
+  it.row = static_cast<int>((e.x >> 9) & 0x3Fu);
+  it.c = static_cast<int>(e.x & 0x1FFu);
+  it.x = static_cast<int>(e.y);
+  it.sT = __uint_as_float(e.z);
+  it.n = static_cast<int>(e.w);
+  it.pad = 0;
+  it.prm = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  return it;
+}
+
+// One lane: the item of ticket t < pl.total, packed: tickets run request
+// by request, row slot by row slot, chunk by chunk.
+__device__ uint4 decode_ticket(const Params& P, const Plan& pl, int t) {
+  const int r = div_nc(P, t);
+  const int b = count_le(pl.rb, P.B, r) - 1;
+  const int slot = r - pl.rb[b];
+  const int c = t - r * P.NC;
+  const int info = pl.info[b];
+  const bool sampled = (info & 0x80) != 0;
+  const int n = info & 0x3F;
+  const float sT = sampled ? temp_scale(__ldg(P.temperature + b)) : 0.0f;
+  const int row = slot_row(slot, sampled, n, P.K);
+  int x = -1;
+  if (sampled && slot < 2 * n) x = __ldg(P.draft_tokens + static_cast<size_t>(b) * P.K + (slot >> 1));
+  return pack_item(kItemA, b, row, c, x, sT, n);
+}
 // ---------------------------------------------------------------- chunk reductions
 
 // Whole warp: argmax of a stats chunk, lowest index on ties.  Each lane
@@ -811,119 +894,8 @@ __device__ int draw_in_slot(const unsigned char* slot, const Chunk& kp, const Ch
   return __shfl_sync(0xffffffffu, tok, l);
 }
 
-// ---------------------------------------------------------------- records
 
-__device__ __forceinline__ void st_record(uint2* p, uint32_t lo, uint32_t hi) {
-  const unsigned long long v = (static_cast<unsigned long long>(hi) << 32) | lo;
-  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-
-__device__ __forceinline__ uint2 ld_record(const uint2* p) {
-  unsigned long long v;
-  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return make_uint2(static_cast<uint32_t>(v), static_cast<uint32_t>(v >> 32));
-}
-
-// A nonnegative (or NaN) float with the ready bit, and back.
-__device__ __forceinline__ uint32_t ready_bits(float x) {
-  return (x != x ? 0x7FC00000u : __float_as_uint(x)) | kReady;
-}
-__device__ __forceinline__ float ready_value(uint32_t u) { return __uint_as_float(u & ~kReady); }
-
-// Whole warp: stages n records from src into dst, up to 16 loads in flight
-// per lane; true if every one of them is written.
-__device__ __forceinline__ bool stage_records(uint2* dst, const uint2* src, int n, int lane) {
-  bool ready = true;
-  for (int base = 0; base < n; base += 16 * 32) {
-    uint2 v[16];
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      const int i = base + k * 32 + lane;
-      if (i < n) v[k] = ld_record(src + i);
-    }
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      const int i = base + k * 32 + lane;
-      if (i < n) {
-        dst[i] = v[k];
-        ready = ready && (v[k].y & kReady);
-      }
-    }
-  }
-  return __all_sync(0xffffffffu, ready);
-}
-
-// Whole warp: returns n records to "not written" for the next call.
-__device__ __forceinline__ void clear_records(uint2* p, int n, int lane) {
-  for (int i = lane; i < n; i += 32) p[i] = make_uint2(0u, 0u);
-}
-
-// ---------------------------------------------------------------- decisions
-
-// (max, sum) of one row from its NC staged stats records: the maximum
-// first, then the chunk sums rescaled to it, in chunk order.
-__device__ __forceinline__ void combine_row(const uint2* p, int NC, float sT, float& M, float& S) {
-  M = -INFINITY;
-  for (int c = 0; c < NC; ++c) M = fmaxf(M, __uint_as_float(p[c].x));
-  S = 0.0f;
-  if (M == -INFINITY) return;
-  for (int c = 0; c < NC; ++c) {
-    const float m = __uint_as_float(p[c].x);
-    if (m > -INFINITY) S = __fadd_rn(S, __fmul_rn(ready_value(p[c].y), scaled_exp(m, M, sT)));
-  }
-}
-
-// Argmax of one row from its staged records: chunks are in index order, so
-// the first chunk holding the maximum has the lowest index.
-__device__ __forceinline__ void argmax_row(const uint2* p, int NC, float& v, int& i) {
-  v = __uint_as_float(p[0].x);
-  i = static_cast<int>(p[0].y & ~kReady);
-  for (int c = 1; c < NC; ++c) {
-    const float m = __uint_as_float(p[c].x);
-    if (m > v) {
-      v = m;
-      i = static_cast<int>(p[c].y & ~kReady);
-    }
-  }
-}
-
-// Whole warp: stages request b's records of target rows [0, nt) and draft
-// rows [0, nd) pass by pass and combines them: lane t gets target row t
-// (Mp, Sp, or the argmax) and draft row t (Mq, Sq).  False if a record is
-// not written yet.
-__device__ bool combine_request(const Params& P, Smem& S, int b, int nt, int nd, bool greedy,
-                                float sT, int lane, float& Mp, float& Sp, float& Mq, float& Sq,
-                                int& arg) {
-  const int NC = P.NC, K = P.K;
-  uint2* buf = S.cbuf;
-  const int cap = max(1, kCtlRecords / NC);   // rows per pass
-  const uint2* rec = P.part + static_cast<size_t>(b) * P.R * NC;
-  Mp = Mq = -INFINITY;
-  Sp = Sq = 0.0f;
-  arg = INT_MAX;
-  for (int v0 = 0; v0 < nt + nd; v0 += cap) {
-    const int v1 = min(nt + nd, v0 + cap);
-    // virtual rows [v0, v1): target rows first, then draft rows
-    const int ta = v0, tb = min(v1, nt);
-    const int da = max(v0, nt) - nt, db = v1 - nt;
-    const int ntr = max(0, tb - ta);
-    bool ready = true;
-    if (ntr > 0) ready = stage_records(buf, rec + static_cast<size_t>(ta) * NC, ntr * NC, lane);
-    if (db > da)
-      ready = stage_records(buf + ntr * NC, rec + static_cast<size_t>(K + 1 + da) * NC,
-                            (db - da) * NC, lane) && ready;
-    __syncwarp();
-    if (!ready) return false;
-    if (lane >= ta && lane < tb) {
-      const uint2* p = buf + (lane - ta) * NC;
-      if (greedy) argmax_row(p, NC, Mp, arg);
-      else combine_row(p, NC, sT, Mp, Sp);
-    }
-    if (lane >= da && lane < db) combine_row(buf + (ntr + lane - da) * NC, NC, sT, Mq, Sq);
-    __syncwarp();
-  }
-  return true;
-}
+// ---------------------------------------------------------------- draws
 
 // Whole warp: the chunk holding mass u * W of a draw, chunk masses
 // mass[0..n) in shared memory (lane l sums chunks [l m, l m + m) in order,
@@ -973,665 +945,708 @@ __device__ int pick_chunk(const float* mass, int n, float u, int lane, float& W,
 // Whole warp (control): copies chunk c (of size CB) of target row rp, and
 // for a residual the matching draft elements of row rq, into the control
 // warp's buffer with bulk copies, and waits (bounded) for them.
+// ---------------------------------------------------------------- agents
+
+// A warp's ring: slot s of kSlotBytes at ring + s * kSlotBytes, completing
+// on bar[s]; bit s of ph is the parity slot s waits for next.  A slot whose
+// item is consumed serves as the warp's scratch until it is refilled.
+struct Agent {
+  AgentSmem* A;
+  unsigned char* ring;
+  uint32_t ph;
+  int lane;
+  __device__ unsigned char* slot(int s) const { return ring + static_cast<size_t>(s) * kSlotBytes; }
+};
+
 template <int DT>
-__device__ bool ctl_fetch(const Params& P, Smem& S, uint32_t& cphase, uintptr_t rp, uintptr_t rq,
-                          int c, int CB, bool residual, Chunk& kp, Chunk& kq, int lane) {
-  unsigned char* slot = reinterpret_cast<unsigned char*>(S.cbuf);
+__device__ __forceinline__ uintptr_t target_row(const Params& P, int b, int t) {
+  return row_addr<DT>(P.target, static_cast<size_t>(b) * (P.K + 1) + t, P.V);
+}
+template <int DT>
+__device__ __forceinline__ uintptr_t draft_row(const Params& P, int b, int t) {
+  return row_addr<DT>(P.draft, static_cast<size_t>(b) * P.K + t, P.V);
+}
+template <int DT>
+__device__ __forceinline__ uintptr_t record_row_addr(const Params& P, int b, int row) {
+  return row > P.K ? draft_row<DT>(P, b, row - P.K - 1) : target_row<DT>(P, b, row);
+}
+
+// Whole warp: waits (bounded) for slot s's copies and flips its parity.
+__device__ __forceinline__ bool wait_slot(const Params& P, Agent& ag, int s) {
+  const bool ok = warp_wait(&ag.A->bar[s], (ag.ph >> s) & 1u);
+  ag.ph ^= 1u << s;
+  if (!ok && ag.lane == 0) atomicOr(P.header + kHStatus, SPECV_DEV_TIMEOUT);
+  return ok;
+}
+
+// Lane 0: stages an item into slot s (descriptor, then the bulk copies).
+template <int DT>
+__device__ void issue(const Params& P, Agent& ag, int s, const Item& it) {
+  unsigned char* slot = ag.slot(s);
+  uint64_t* bar = &ag.A->bar[s];
+  ag.A->item[s] = it;
+  uintptr_t src0 = 0, src1 = 0;
+  uint32_t n0 = 0, n1 = 0;
+  unsigned char *dst0 = slot, *dst1 = slot;
+  if (it.kind != kItemR) {
+    const bool is_draft = it.row > P.K;
+    const Chunk k = chunk_of<DT>(record_row_addr<DT>(P, it.b, it.row), P.V, it.c, kChunkBytes);
+    n0 = bulk_span<DT>(k, is_draft ? P.d_lo : P.t_lo, is_draft ? P.d_hi : P.t_hi, &src0);
+    if (n0) dst0 = slot + (src0 - k.g0);
+  } else {
+    const Chunk kp = chunk_of<DT>(target_row<DT>(P, it.b, it.row), P.V, it.c, kDrawBytes);
+    n0 = bulk_span<DT>(kp, P.t_lo, P.t_hi, &src0);
+    if (n0) dst0 = slot + (src0 - kp.g0);
+    const Chunk kq = draft_part<DT>(draft_row<DT>(P, it.b, it.row), kp);
+    n1 = bulk_span<DT>(kq, P.d_lo, P.d_hi, &src1);
+    if (n1) dst1 = slot + kDraftOff + (src1 - kq.g0);
+  }
+  fence_proxy_async_smem();
+  mbar_arrive_expect_tx(bar, n0 + n1);
+  if (n0) bulk_copy_g2s(dst0, src0, n0, bar);
+  if (n1) bulk_copy_g2s(dst1, src1, n1, bar);
+}
+
+// Whole warp: copies chunk c (size CB) of target row rp, and for a residual
+// the same elements of draft row rq, into scratch slot s and waits for them.
+template <int DT>
+__device__ bool fetch(const Params& P, Agent& ag, int s, uintptr_t rp, uintptr_t rq, int c, int CB,
+                      bool residual, Chunk& kp, Chunk& kq) {
+  unsigned char* slot = ag.slot(s);
   kp = chunk_of<DT>(rp, P.V, c, CB);
   kq = residual ? draft_part<DT>(rq, kp) : kp;
-  __syncwarp();   // every lane is done with the buffer
-  if (lane == 0) {
+  __syncwarp();   // every lane is done with the scratch
+  if (ag.lane == 0) {
+    uint64_t* bar = &ag.A->bar[s];
     uintptr_t s0 = 0, s1 = 0;
     const uint32_t n0 = bulk_span<DT>(kp, P.t_lo, P.t_hi, &s0);
     const uint32_t n1 = residual ? bulk_span<DT>(kq, P.d_lo, P.d_hi, &s1) : 0u;
     fence_proxy_async_smem();
-    mbar_arrive_expect_tx(&S.cbar, n0 + n1);
-    if (n0) bulk_copy_g2s(slot + (s0 - kp.g0), s0, n0, &S.cbar);
-    if (n1) bulk_copy_g2s(slot + kDraftOff + (s1 - kq.g0), s1, n1, &S.cbar);
+    mbar_arrive_expect_tx(bar, n0 + n1);
+    if (n0) bulk_copy_g2s(slot + (s0 - kp.g0), s0, n0, bar);
+    if (n1) bulk_copy_g2s(slot + kDraftOff + (s1 - kq.g0), s1, n1, bar);
   }
-  const bool ok = warp_wait(&S.cbar, cphase & 1u);
-  ++cphase;
-  if (!ok && lane == 0) atomicOr(P.header + kHStatus, SPECV_DEV_TIMEOUT);
-  fix_edges<DT>(kp, P.t_lo, P.t_hi, slot, lane);
-  if (residual) fix_edges<DT>(kq, P.d_lo, P.d_hi, slot + kDraftOff, lane);
+  const bool ok = wait_slot(P, ag, s);
+  fix_edges<DT>(kp, P.t_lo, P.t_hi, slot, ag.lane);
+  if (residual) fix_edges<DT>(kq, P.d_lo, P.d_hi, slot + kDraftOff, ag.lane);
   return ok;
 }
 
-// Whole warp: out_tokens[b] = x_0 .. x_{j-1}, tok at j (skipped if
-// skip_j), -1 after; accepted_len[b] = j.  Lane s < n holds x_s.
-__device__ __forceinline__ void write_outputs(const Params& P, int b, int j, int tok, int x_lane,
-                                              bool skip_j, int lane) {
-  if (lane <= P.K && !(skip_j && lane == j))
-    P.out_tokens[static_cast<size_t>(b) * (P.K + 1) + lane] = lane < j ? x_lane : (lane == j ? tok : -1);
-  if (lane == 0) P.accepted_len[b] = j;
+// ---------------------------------------------------------------- records
+
+__device__ __forceinline__ void st_word(uint32_t* p, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// Whole warp (control): tries to decide request b.  Returns 0 if some of
-// its records are not written yet, 1 if the request is answered (greedy, a
-// bonus draw, or bad data), 2 if its rejected row is published for the
-// residual draw (pe filled, every output but the drawn token written).
-// Validates the request's tokens and uniforms, combines its records, runs
-// the rule's left-to-right test; a bonus draw (every draft accepted) is
-// taken at once from the final row's chunk masses, which its records give,
-// and one re-read chunk.
+__device__ __forceinline__ uint32_t ld_word(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// A nonnegative (or NaN) float with the ready bit, and back.
+__device__ __forceinline__ uint32_t ready_bits(float x) {
+  return (x != x ? 0x7FC00000u : __float_as_uint(x)) | kReady;
+}
+__device__ __forceinline__ float ready_value(uint32_t u) { return __uint_as_float(u & ~kReady); }
+
+// Whole warp: stages n records (written by an earlier kernel) into shared
+// memory, eight loads in flight per lane.
+__device__ __forceinline__ void stage_records(uint2* dst, const uint2* src, int n, int lane) {
+  for (int base = 0; base < n; base += 8 * 32) {
+    uint2 v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int i = base + k * 32 + lane;
+      if (i < n) v[k] = __ldcg(src + i);
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int i = base + k * 32 + lane;
+      if (i < n) dst[i] = v[k];
+    }
+  }
+}
+
+// (max, sum) of one row from its NC staged records: the maximum first, then
+// the chunk sums rescaled to it, in chunk order.
+__device__ __forceinline__ void combine_row(const uint2* p, int NC, float sT, float& M, float& S) {
+  M = -INFINITY;
+  for (int c = 0; c < NC; ++c) M = fmaxf(M, __uint_as_float(p[c].x));
+  S = 0.0f;
+  if (M == -INFINITY) return;
+  for (int c = 0; c < NC; ++c) {
+    const float m = __uint_as_float(p[c].x);
+    if (m > -INFINITY) S = __fadd_rn(S, __fmul_rn(__uint_as_float(p[c].y), scaled_exp(m, M, sT)));
+  }
+}
+
+// Argmax of one row from its staged records: chunks are in index order, so
+// the first chunk holding the maximum has the lowest index.
+__device__ __forceinline__ void argmax_row(const uint2* p, int NC, float& v, int& i) {
+  v = __uint_as_float(p[0].x);
+  i = static_cast<int>(p[0].y);
+  for (int c = 1; c < NC; ++c) {
+    const float m = __uint_as_float(p[c].x);
+    if (m > v) {
+      v = m;
+      i = static_cast<int>(p[c].y);
+    }
+  }
+}
+
+// Whole warp: combines request b's records of target rows [0, nt) and
+// draft rows [0, nd), staged pass by pass through scratch (kSlotBytes):
+// lane t gets target row t (Mp, Sp, or the argmax) and draft row t (Mq, Sq).
+__device__ void combine_request(const Params& P, unsigned char* scratch, int b, int nt, int nd,
+                                bool greedy, float sT, int lane, float& Mp, float& Sp, float& Mq,
+                                float& Sq, int& arg) {
+  const int NC = P.NC, K = P.K;
+  uint2* buf = reinterpret_cast<uint2*>(scratch);
+  const int cap = max(1, kSlotBytes / (8 * NC));   // rows per pass
+  const uint2* rec = P.part + static_cast<size_t>(b) * P.R * NC;
+  Mp = Mq = -INFINITY;
+  Sp = Sq = 0.0f;
+  arg = INT_MAX;
+  for (int v0 = 0; v0 < nt + nd; v0 += cap) {
+    const int v1 = min(nt + nd, v0 + cap);
+    // virtual rows [v0, v1): target rows first, then draft rows
+    const int ta = v0, tb = min(v1, nt);
+    const int da = max(v0, nt) - nt, db = v1 - nt;
+    const int ntr = max(0, tb - ta);
+    __syncwarp();
+    if (ntr > 0) stage_records(buf, rec + static_cast<size_t>(ta) * NC, ntr * NC, lane);
+    if (db > da)
+      stage_records(buf + ntr * NC, rec + static_cast<size_t>(K + 1 + da) * NC, (db - da) * NC,
+                    lane);
+    __syncwarp();
+    if (lane >= ta && lane < tb) {
+      const uint2* p = buf + (lane - ta) * NC;
+      if (greedy) argmax_row(p, NC, Mp, arg);
+      else combine_row(p, NC, sT, Mp, Sp);
+    }
+    if (lane >= da && lane < db) combine_row(buf + (ntr + lane - da) * NC, NC, sT, Mq, Sq);
+  }
+  __syncwarp();
+}
+
+// Whole warp: chunk masses of a draw from p (one row's records rescaled to
+// the row maximum Mp) into scratch.
+__device__ __forceinline__ void p_masses(const uint2* rec, int NC, float Mp, float sT, float* mass,
+                                         int lane) {
+  __syncwarp();
+  for (int c = lane; c < NC; c += 32) {
+    const uint2 r = __ldcg(rec + c);
+    const float m = __uint_as_float(r.x);
+    mass[c] = m > -INFINITY ? __fmul_rn(__uint_as_float(r.y), scaled_exp(m, Mp, sT)) : 0.0f;
+  }
+  __syncwarp();
+}
+
+// ---------------------------------------------------------------- decisions
+
+// Whole warp: decides request b from the stats kernel's records and writes
+// its outputs.  Greedy: the argmax of target rows t <= n against the
+// drafts.  Sampled: the left-to-right test u_t q(x_t) < p(x_t) in log2 form;
+// every draft accepted draws the bonus token from p_n here (the chunk from
+// row n's records, the token from one re-read chunk); a rejection at j
+// stores the residual draw's parameters and lists the request for the
+// residual kernel, which writes out_tokens[b, j].  Slot 0 of the warp's
+// ring is its scratch.
 template <int DT>
-__device__ __noinline__ int try_decide(const Params& P, Smem& S, uint32_t& cphase, int b, int n,
-                                       float T, int lane, uint32_t tag, Pend& pe) {
-  const int K = P.K, V = P.V, NC = P.NC, R = P.R;
+__device__ void decide_request(const Params& P, Agent& ag, int b) {
+  const int lane = ag.lane, K = P.K, V = P.V, R = P.R, NC = P.NC;
+  const int n = request_len(P, b);
+  const float T = __ldg(P.temperature + b);
+  int bad = request_bad(P, n, T);
+  if (bad) {
+    if (lane == 0) atomicOr(P.header + kHStatus, bad);
+    write_outputs(P, b, -1, -1, -1, lane);
+    return;
+  }
   const bool greedy = !(T > 0.0f);
-  const int nt = n + 1, nd = greedy ? 0 : n;
-  uint2* rec = P.part + static_cast<size_t>(b) * R * NC;
-  uint2* zrec = P.zx + static_cast<size_t>(b) * R;
+  const float sT = greedy ? 0.0f : temp_scale(T);
   int x_lane = -1;
   float u_lane = 0.0f;
   if (lane < n) x_lane = __ldg(P.draft_tokens + static_cast<size_t>(b) * K + lane);
   if (lane <= n) u_lane = __ldg(P.uniforms + static_cast<size_t>(b) * (K + 1) + lane);
   const float ur = __ldg(P.uniforms_resample + b);
-  // the drafted tokens' logits (sampled rows t < n)
-  uint2 zp_r = make_uint2(0u, kReady), zq_r = make_uint2(0u, kReady);
+  float zp = 0.0f, zq = 0.0f;
   if (!greedy && lane < n) {
-    zp_r = ld_record(zrec + lane);
-    zq_r = ld_record(zrec + K + 1 + lane);
+    zp = __ldcg(P.zx + static_cast<size_t>(b) * R + lane);
+    zq = __ldcg(P.zx + static_cast<size_t>(b) * R + K + 1 + lane);
   }
-  const float sT = greedy ? 0.0f : temp_scale(T);
   float Mp_l, Sp_l, Mq_l, Sq_l;
   int g;
-  if (!combine_request(P, S, b, nt, nd, greedy, sT, lane, Mp_l, Sp_l, Mq_l, Sq_l, g)) return 0;
-  const bool tok_bad = lane < n && (x_lane < 0 || x_lane >= V);
-  const bool u_bad = lane <= n && !(u_lane >= 0.0f && u_lane < 1.0f);
-  int bad = 0;
-  if (__any_sync(0xffffffffu, tok_bad)) bad |= SPECV_DEV_BAD_TOKEN;
-  if (__any_sync(0xffffffffu, u_bad) || !(ur >= 0.0f && ur < 1.0f)) bad |= SPECV_DEV_BAD_UNIFORM;
-  // a valid token's logit record is written by the item holding it
-  if (!bad && !__all_sync(0xffffffffu, (zp_r.y & kReady) && (zq_r.y & kReady))) return 0;
-
+  combine_request(P, ag.slot(0), b, n + 1, greedy ? 0 : n, greedy, sT, lane, Mp_l, Sp_l, Mq_l,
+                  Sq_l, g);
+  if (__any_sync(0xffffffffu, lane < n && (x_lane < 0 || x_lane >= V))) bad |= SPECV_DEV_BAD_TOKEN;
+  if (__any_sync(0xffffffffu, lane <= n && !(u_lane >= 0.0f && u_lane < 1.0f)) ||
+      !(ur >= 0.0f && ur < 1.0f))
+    bad |= SPECV_DEV_BAD_UNIFORM;
   float* rs = P.row_stats ? P.row_stats + static_cast<size_t>(b) * (K + 1) * 8 : nullptr;
-  int result = 1;
+
+  if (greedy) {
+    if (!bad) {
+      if (rs && lane <= n) {
+        rs[lane * 8 + 0] = Mp_l;
+        rs[lane * 8 + 7] = static_cast<float>(g);
+      }
+      const unsigned miss = __ballot_sync(0xffffffffu, lane < n && g != x_lane);
+      const int j = miss ? __ffs(miss) - 1 : n;
+      const int gj = __shfl_sync(0xffffffffu, g, j);
+      if (gj >= 0 && gj < V) {
+        write_outputs(P, b, j, gj, x_lane, lane);
+        return;
+      }
+      bad = SPECV_DEV_BAD_ROW;
+    }
+    if (lane == 0) atomicOr(P.header + kHStatus, bad);
+    write_outputs(P, b, -1, -1, x_lane, lane);
+    return;
+  }
+
+  // every row a sampled request needs must have a finite maximum
+  if (!bad && __any_sync(0xffffffffu, (lane < n && !(isfinite(Mp_l) && isfinite(Mq_l))) ||
+                                          (lane == n && !isfinite(Mp_l))))
+    bad = SPECV_DEV_BAD_ROW;
   if (bad) {
-    finish_bad(P, b, bad, lane, tag);
-  } else if (greedy) {
-    if (rs && lane <= n) {
+    if (lane == 0) atomicOr(P.header + kHStatus, bad);
+    write_outputs(P, b, -1, -1, x_lane, lane);
+    return;
+  }
+  float lp = 0.0f, lq = 0.0f;
+  bool accept = false;
+  if (lane < n) {
+    lp = __fsub_rn(__fmul_rn(__fsub_rn(zp, Mp_l), sT), log2f(Sp_l));
+    lq = __fsub_rn(__fmul_rn(__fsub_rn(zq, Mq_l), sT), log2f(Sq_l));
+    accept = __fadd_rn(log2f(u_lane), lq) < lp;
+  }
+  const unsigned rej = __ballot_sync(0xffffffffu, lane < n && !accept);
+  const int j = rej ? __ffs(rej) - 1 : n;
+  if (rs) {
+    if (lane <= n) {
       rs[lane * 8 + 0] = Mp_l;
-      rs[lane * 8 + 7] = static_cast<float>(g);
+      rs[lane * 8 + 1] = Sp_l;
     }
-    const unsigned miss = __ballot_sync(0xffffffffu, lane < n && g != x_lane);
-    const int j = miss ? __ffs(miss) - 1 : n;
-    const int gj = __shfl_sync(0xffffffffu, g, j);
-    if (gj < 0 || gj >= V) {
-      finish_bad(P, b, SPECV_DEV_BAD_ROW, lane, tag);
-    } else {
-      if (lane == 0) set_state(P, b, tag, kStateNone);
-      write_outputs(P, b, j, gj, x_lane, false, lane);
+    if (lane < n) {
+      rs[lane * 8 + 2] = lp * kLn2;
+      rs[lane * 8 + 3] = Mq_l;
+      rs[lane * 8 + 4] = Sq_l;
+      rs[lane * 8 + 5] = lq * kLn2;
     }
+  }
+  const float Mp = __shfl_sync(0xffffffffu, Mp_l, j);
+  const float Sp = __shfl_sync(0xffffffffu, Sp_l, j);
+  if (j < n) {
+    const float Mq = __shfl_sync(0xffffffffu, Mq_l, j);
+    const float Sq = __shfl_sync(0xffffffffu, Sq_l, j);
+    if (lane == 0) {
+      Req* q = P.req + b;
+      q->j = j;
+      q->Sp_j = Sp;
+      q->prm = make_float4(Mp, Mq, sT, __fdiv_rn(Sp, Sq));
+      P.rlist[atomicAdd(P.header + kHResid, 1)] = b;
+    }
+    write_outputs(P, b, j, -1, x_lane, lane);   // the residual kernel writes the token
+    return;
+  }
+  // every draft accepted: the bonus token from p_n with uniforms[b, n]
+  const float u = __shfl_sync(0xffffffffu, u_lane, n);
+  float* mass = reinterpret_cast<float*>(ag.slot(0));
+  p_masses(P.part + (static_cast<size_t>(b) * R + n) * NC, NC, Mp, sT, mass, lane);
+  float W, rem;
+  const int chunk = pick_chunk(mass, NC, u, lane, W, rem);
+  int tok = -1;
+  if (chunk >= 0) {
+    Chunk kp, kq;
+    if (fetch<DT>(P, ag, 0, target_row<DT>(P, b, n), 0, chunk, kChunkBytes, false, kp, kq))
+      tok = draw_in_slot<DT>(ag.slot(0), kp, kq, false, make_float4(Mp, 0.0f, sT, 0.0f), rem,
+                             kChunkBytes / 512, lane);
+  }
+  if (rs && lane == 0) {
+    rs[n * 8 + 6] = __fdiv_rn(W, Sp);
+    rs[n * 8 + 7] = static_cast<float>(tok);
+  }
+  if (tok < 0 || tok >= V) {
+    if (lane == 0) atomicOr(P.header + kHStatus, SPECV_DEV_BAD_ROW);
+    write_outputs(P, b, -1, -1, x_lane, lane);
   } else {
-    // ---- sampled: lane t holds target row t and draft row t ----------------
-    const bool row_bad = (lane <= n && !isfinite(Mp_l)) || (lane < n && !isfinite(Mq_l));
-    if (__any_sync(0xffffffffu, row_bad)) {
-      finish_bad(P, b, SPECV_DEV_BAD_ROW, lane, tag);
-    } else {
-      float lp = 0.0f, lq = 0.0f;
-      if (lane < n) {
-        lp = __fsub_rn(__fmul_rn(__fsub_rn(__uint_as_float(zp_r.x), Mp_l), sT), log2f(Sp_l));
-        lq = __fsub_rn(__fmul_rn(__fsub_rn(__uint_as_float(zq_r.x), Mq_l), sT), log2f(Sq_l));
-      }
-      bool accept = false;
-      if (lane < n) accept = __fadd_rn(log2f(u_lane), lq) < lp;
-      const unsigned rej = __ballot_sync(0xffffffffu, lane < n && !accept);
-      const int j = rej ? __ffs(rej) - 1 : n;
-      if (rs) {
-        if (lane <= n) {
-          rs[lane * 8 + 0] = Mp_l;
-          rs[lane * 8 + 1] = Sp_l;
-        }
-        if (lane < n) {
-          rs[lane * 8 + 2] = lp * kLn2;
-          rs[lane * 8 + 3] = Mq_l;
-          rs[lane * 8 + 4] = Sq_l;
-          rs[lane * 8 + 5] = lq * kLn2;
-        }
-      }
-      const float Mp = __shfl_sync(0xffffffffu, Mp_l, j);
-      const float Sp = __shfl_sync(0xffffffffu, Sp_l, j);
-      const float Mq = __shfl_sync(0xffffffffu, Mq_l, j);
-      const float Sq = __shfl_sync(0xffffffffu, Sq_l, j);
-      const float u_bonus = __shfl_sync(0xffffffffu, u_lane, n);
-      if (j == n) {
-        // bonus draw from p_n: chunk masses s_c 2^((m_c - Mp) log2(e)/T)
-        const uint2* rn = rec + static_cast<size_t>(n) * NC;
-        for (int c = lane; c < NC; c += 32) {
-          const uint2 r = ld_record(rn + c);
-          const float m = __uint_as_float(r.x);
-          S.cmass[c] = m > -INFINITY ? __fmul_rn(ready_value(r.y), scaled_exp(m, Mp, sT)) : 0.0f;
-        }
-        __syncwarp();
-        float W, rem;
-        const int chunk = pick_chunk(S.cmass, NC, u_bonus, lane, W, rem);
-        const float4 prm = make_float4(Mp, 0.0f, sT, 0.0f);
-        const uintptr_t rp = row_addr<DT>(P.target, static_cast<size_t>(b) * (K + 1) + n, V);
-        int tok = -1;
-        if (chunk >= 0) {
-          Chunk kp, kq;
-          if (ctl_fetch<DT>(P, S, cphase, rp, 0, chunk, kChunkBytes, false, kp, kq, lane))
-            tok = draw_in_slot<DT>(reinterpret_cast<const unsigned char*>(S.cbuf), kp, kq, false,
-                                   prm, rem, kChunkBytes / 512, lane);
-        }
-        if (rs && lane == 0) {
-          rs[n * 8 + 6] = __fdiv_rn(W, Sp);
-          rs[n * 8 + 7] = static_cast<float>(tok);
-        }
-        if (tok < 0 || tok >= V) {
-          finish_bad(P, b, SPECV_DEV_BAD_ROW, lane, tag);
-        } else {
-          if (lane == 0) set_state(P, b, tag, kStateNone);
-          write_outputs(P, b, n, tok, x_lane, false, lane);
-        }
-      } else {
-        pe.b = b;
-        pe.j = j;
-        pe.t_f = j;
-        pe.residual = 1;
-        pe.u = ur;
-        pe.Sp = Sp;
-        pe.pad0 = pe.pad1 = 0.0f;
-        pe.prm = make_float4(Mp, Mq, sT, __fdiv_rn(Sp, Sq));
-        write_outputs(P, b, j, -1, x_lane, true, lane);
-        if (lane == 0) {
-          P.req[b].prm = pe.prm;
-          set_state(P, b, tag, kStateDraws | 4u | (static_cast<uint32_t>(j) << 3));
-        }
-        result = 2;
-      }
-    }
+    write_outputs(P, b, n, tok, x_lane, lane);
   }
-  // every record of the request is consumed: clear them for the next call
-  // (a residual draw keeps its target row's, for the search's fallback to p)
-  __syncwarp();
-  if (result == 2) {
-    clear_records(rec, pe.t_f * NC, lane);
-    clear_records(rec + static_cast<size_t>(pe.t_f + 1) * NC, (nt - pe.t_f - 1) * NC, lane);
-  } else {
-    clear_records(rec, nt * NC, lane);
-  }
-  if (nd) clear_records(rec + static_cast<size_t>(K + 1) * NC, nd * NC, lane);
-  if (!greedy && lane < n) {
-    zrec[lane] = make_uint2(0u, 0u);
-    zrec[K + 1 + lane] = make_uint2(0u, 0u);
-  }
-  __syncwarp();
-  return result;
 }
 
-// Whole warp (control): tries to draw the final token of a request whose
-// rejected row is published.  Returns false if some of its draw records
-// are not written yet.  Picks the chunk from the records' residual masses
-// and searches it, re-read; a residual of exactly zero mass falls back to
-// drawing from p with the same uniform, its chunk masses taken from the
-// row's stats records (kept for this) and a stats-sized chunk re-read.
+// Whole warp: the residual draw of listed request b (entry e, rejected at
+// row j) once all its pieces are summed: the piece from their sums, the
+// token from one re-read piece pair, with uniforms_resample[b].  A residual
+// of exactly zero mass falls back to drawing from p_j with the same uniform
+// (its chunk masses from row j's records).  Slot s is the scratch.
 template <int DT>
-__device__ __noinline__ bool try_search(const Params& P, Smem& S, uint32_t& cphase, const Pend& pe,
-                                        int lane, uint32_t tag) {
-  const int K = P.K, NCd = P.NCd, NC = P.NC, b = pe.b;
-  uint2* rec = P.dpart + static_cast<size_t>(b) * NCd;
-  if (!stage_records(S.cbuf, rec, NCd, lane)) return false;
+__device__ void residual_search(const Params& P, Agent& ag, int s, int e, int b, int j,
+                                const float4& prm) {
+  const int lane = ag.lane, K = P.K, V = P.V, NC = P.NC, NCd = P.NCd;
+  float* mass = reinterpret_cast<float*>(ag.slot(s));
+  uint32_t* drec = P.dmass + static_cast<size_t>(e) * NCd;
+  // a count completes once every piece has stored its sum, but a store may
+  // become visible after the count: sums are read until written (bounded)
+  bool staged = true;
+  const long long t0 = clock64();
   __syncwarp();
-  clear_records(rec, NCd, lane);
-  for (int c = lane; c < NCd; c += 32) S.cmass[c] = ready_value(S.cbuf[c].y);
+  for (int c0 = 0; c0 < NCd; c0 += 32) {
+    const int c = c0 + lane;
+    uint32_t w = c < NCd ? ld_word(drec + c) : kReady;
+    while (!__all_sync(0xffffffffu, (w & kReady) != 0u)) {
+      if (clock64() - t0 > kWaitLimitCycles) {
+        staged = false;
+        break;
+      }
+      __nanosleep(64);
+      if (!(w & kReady)) w = ld_word(drec + c);
+    }
+    if (c < NCd) {
+      mass[c] = ready_value(w);
+      drec[c] = 0u;   // ready for the next call
+    }
+  }
   __syncwarp();
-  float W, rem;
-  int chunk = pick_chunk(S.cmass, NCd, pe.u, lane, W, rem);
-  __syncwarp();
-  const float W_report = W;
-  const uintptr_t rp = row_addr<DT>(P.target, static_cast<size_t>(b) * (K + 1) + pe.t_f, P.V);
-  const uintptr_t rq = row_addr<DT>(P.draft, static_cast<size_t>(b) * K + pe.t_f, P.V);
-  uint2* srec = P.part + (static_cast<size_t>(b) * P.R + pe.t_f) * NC;
+  const float ur = __ldg(P.uniforms_resample + b);
+  float W = 0.0f, rem = 0.0f;
+  int chunk = staged ? pick_chunk(mass, NCd, ur, lane, W, rem) : -1;
+  const uintptr_t rp = target_row<DT>(P, b, j);
   int tok = -1;
   Chunk kp, kq;
-  if (W > 0.0f) {
-    if (chunk >= 0 && ctl_fetch<DT>(P, S, cphase, rp, rq, chunk, kDrawBytes, true, kp, kq, lane))
-      tok = draw_in_slot<DT>(reinterpret_cast<const unsigned char*>(S.cbuf), kp, kq, true, pe.prm,
-                             rem, kDrawSweeps, lane);
+  if (!staged) {
+    // a wait gave up: flagged below
+  } else if (W > 0.0f) {
+    if (chunk >= 0 &&
+        fetch<DT>(P, ag, s, rp, draft_row<DT>(P, b, j), chunk, kDrawBytes, true, kp, kq))
+      tok = draw_in_slot<DT>(ag.slot(s), kp, kq, true, prm, rem, kDrawSweeps, lane);
   } else {
-    // a residual of exactly zero mass: p's chunk masses from the stats records
-    const float Mp = pe.prm.x, sT = pe.prm.z;
-    for (int c = lane; c < NC; c += 32) {
-      const uint2 r = ld_record(srec + c);
-      const float m = __uint_as_float(r.x);
-      S.cmass[c] = m > -INFINITY ? __fmul_rn(ready_value(r.y), scaled_exp(m, Mp, sT)) : 0.0f;
-    }
-    __syncwarp();
+    p_masses(P.part + (static_cast<size_t>(b) * P.R + j) * NC, NC, prm.x, prm.z, mass, lane);
     float Wp;
-    chunk = pick_chunk(S.cmass, NC, pe.u, lane, Wp, rem);
-    const float4 prm = make_float4(Mp, 0.0f, sT, 0.0f);
-    if (chunk >= 0 && ctl_fetch<DT>(P, S, cphase, rp, 0, chunk, kChunkBytes, false, kp, kq, lane))
-      tok = draw_in_slot<DT>(reinterpret_cast<const unsigned char*>(S.cbuf), kp, kq, false, prm,
+    chunk = pick_chunk(mass, NC, ur, lane, Wp, rem);
+    if (chunk >= 0 && fetch<DT>(P, ag, s, rp, 0, chunk, kChunkBytes, false, kp, kq))
+      tok = draw_in_slot<DT>(ag.slot(s), kp, kq, false, make_float4(prm.x, 0.0f, prm.z, 0.0f),
                              rem, kChunkBytes / 512, lane);
   }
-  __syncwarp();
-  clear_records(srec, NC, lane);
   if (P.row_stats && lane == 0) {
-    float* rs = P.row_stats + (static_cast<size_t>(b) * (K + 1) + pe.t_f) * 8;
-    rs[6] = __fdiv_rn(W_report, pe.Sp);
+    float* rs = P.row_stats + (static_cast<size_t>(b) * (K + 1) + j) * 8;
+    rs[6] = __fdiv_rn(W, __ldcg(&P.req[b].Sp_j));
     rs[7] = static_cast<float>(tok);
   }
-  if (tok < 0 || tok >= P.V) {
-    finish_bad(P, b, SPECV_DEV_BAD_ROW, lane, tag);
+  if (tok < 0 || tok >= V) {
+    if (lane == 0) atomicOr(P.header + kHStatus, staged ? SPECV_DEV_BAD_ROW : SPECV_DEV_TIMEOUT);
+    write_outputs(P, b, -1, -1, -1, lane);
   } else if (lane == 0) {
-    P.out_tokens[static_cast<size_t>(b) * (K + 1) + pe.j] = tok;
+    P.out_tokens[static_cast<size_t>(b) * (K + 1) + j] = tok;
+  }
+}
+
+// ---------------------------------------------------------------- programmatic launch
+
+// The next kernel on the stream may start launching (its prologue overlaps
+// this kernel's tail; it waits for this kernel's results before reading).
+__device__ __forceinline__ void allow_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Waits until the previous kernel on the stream has completed and its
+// writes are visible.
+__device__ __forceinline__ void wait_previous() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ---------------------------------------------------------------- stats kernel
+
+// Whole warp: reduces the chunk in slot s to its record; the chunk holding
+// the row's drafted token also records that token's logit.
+template <int DT>
+__device__ void consume_stats(const Params& P, Agent& ag, int s, const Item& it) {
+  const int lane = ag.lane;
+  unsigned char* slot = ag.slot(s);
+  const bool is_draft = it.row > P.K;
+  const Chunk k = chunk_of<DT>(record_row_addr<DT>(P, it.b, it.row), P.V, it.c, kChunkBytes);
+  fix_edges<DT>(k, is_draft ? P.d_lo : P.t_lo, is_draft ? P.d_hi : P.t_hi, slot, lane);
+  float2 r;
+  if (it.sT > 0.0f) r = chunk_softmax<DT>(slot, k, it.sT, lane);
+  else r = chunk_argmax<DT>(slot, k, lane);
+  if (lane == 0) {
+    P.part[(static_cast<size_t>(it.b) * P.R + it.row) * P.NC + it.c] =
+        make_uint2(__float_as_uint(r.x), __float_as_uint(r.y));
+    if (it.x >= k.e_lo && it.x < k.e_hi)
+      P.zx[static_cast<size_t>(it.b) * P.R + it.row] =
+          Elt<DT>::load(slot + k.off0 + it.x * Elt<DT>::kBytes);
+  }
+}
+
+// Whole warp, holding the queue's lock: claims the next block of tickets
+// (about half of what is left per CTA, at most kBlockMax, at least one) and
+// publishes their decoded items.  With `force` false it does nothing while
+// enough items are ready.
+__device__ void refill(const Params& P, const Plan& pl, Fifo& f, int lane, bool force) {
+  int base = 0, k = 0, tail = 0, go = 0;
+  if (lane == 0) {
+    tail = *reinterpret_cast<volatile int*>(&f.tail);
+    const int head = *reinterpret_cast<volatile int*>(&f.head);
+    go = !*reinterpret_cast<volatile int*>(&f.closed) && (force || tail - head < kFifoLow);
+    if (go) {
+      const int rem = pl.total - f.last;
+      k = min(kBlockMax, max(1, rem / (2 * static_cast<int>(gridDim.x))));
+      base = static_cast<int>(atomicAdd(reinterpret_cast<unsigned int*>(P.header + kHTicket),
+                                        static_cast<unsigned int>(k)));
+      f.last = base;
+    }
+  }
+  if (!__shfl_sync(0xffffffffu, go, 0)) return;
+  base = __shfl_sync(0xffffffffu, base, 0);
+  k = __shfl_sync(0xffffffffu, k, 0);
+  tail = __shfl_sync(0xffffffffu, tail, 0);
+  const int n = base >= pl.total ? 0 : min(k, pl.total - base);
+  if (lane < n) f.e[(tail + lane) % kFifo] = decode_ticket(P, pl, base + lane);
+  __syncwarp();
+  if (lane == 0) {
+    __threadfence_block();
+    *reinterpret_cast<volatile int*>(&f.tail) = tail + n;
+    if (base + k >= pl.total) {
+      __threadfence_block();
+      *reinterpret_cast<volatile int*>(&f.closed) = 1;
+    }
   }
   __syncwarp();
-  return true;
 }
 
-// ---------------------------------------------------------------- agent
-
-// Asynchronous copies global -> shared: 16 bytes from L2 (never a stale L1
-// line), 4 bytes of read-only input.  cp_async_arrive makes the barrier's
-// current phase wait for every copy this thread issued before it, as one
-// more arrival.
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)),
-               "l"(__cvta_generic_to_global(src))
-               : "memory");
-}
-__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)),
-               "l"(__cvta_generic_to_global(src))
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
-// The request window of a stats cursor: lane l describes request w0 + l.
-struct Window {
-  int w0;        // first request of the window
-  int cnt;       // this lane's request: items
-  int end;       // items up to and including this lane's request (INT_MAX past B)
-  int n;         // draft length
-  float sT;      // log2(e)/T, 0 for a greedy request
-};
-
-__device__ void load_window(const Params& P, Window& w, int w0, int base, int lane) {
-  w.w0 = w0;
-  const int b = w0 + lane;
-  w.n = 0;
-  w.sT = 0.0f;
-  w.cnt = 0;
-  if (b < P.B) {
-    w.n = request_len(P, b);
-    const float T = __ldg(P.temperature + b);
-    w.cnt = request_items(P, w.n, T);
-    if (w.cnt > 0 && T > 0.0f) w.sT = temp_scale(T);
+// Whole warp: tries the queue's lock and refills.
+__device__ __forceinline__ bool try_refill(const Params& P, const Plan& pl, Fifo& f, int lane,
+                                           bool force) {
+  int got = 0;
+  if (lane == 0) got = atomicCAS(&f.lock, 0, 1) == 0;
+  got = __shfl_sync(0xffffffffu, got, 0);
+  if (got) {
+    refill(P, pl, f, lane, force);
+    if (lane == 0) {
+      __threadfence_block();
+      atomicExch(&f.lock, 0);
+    }
   }
-  const int incl = warp_incl_scan_int(w.cnt, lane);
-  w.end = b < P.B ? base + incl : INT_MAX;
+  return got != 0;
 }
 
-// Whole warp: maps stats item g to its request, row and chunk.  Returns
-// false when g is past the last item.
-__device__ bool map_item(const Params& P, Window& w, int g, int lane, Item& it) {
+// Whole warp: the next item of the CTA, in ticket order; false when no
+// ticket is left.
+__device__ bool pop_item(const Params& P, const Plan& pl, Fifo& f, int lane, Item& it) {
+  int idx = 0;
+  if (lane == 0) idx = atomicAdd(&f.head, 1);
+  idx = __shfl_sync(0xffffffffu, idx, 0);
+  const long long t0 = clock64();
   for (;;) {
-    const unsigned done = __ballot_sync(0xffffffffu, w.end <= g);
-    if (done != 0xffffffffu) {
-      const int i = __popc(done);   // ends are nondecreasing: `done` is a prefix
-      if (w.w0 + i >= P.B) return false;
-      const int end = __shfl_sync(0xffffffffu, w.end, i);
-      const int cnt = __shfl_sync(0xffffffffu, w.cnt, i);
-      const int n = __shfl_sync(0xffffffffu, w.n, i);
-      const float sT = __shfl_sync(0xffffffffu, w.sT, i);
-      const int local = g - (end - cnt);
-      int r = __float2int_rz(__int2float_rn(local) * P.inv_NC);   // local < 2^24: exact operands
-      if (r * P.NC > local) --r;
-      if ((r + 1) * P.NC <= local) ++r;
-      it.kind = kItemStats;
-      it.b = w.w0 + i;
-      it.c = local - r * P.NC;
-      it.row = r <= n ? r : (P.K + 1) + (r - n - 1);
-      it.mode = sT > 0.0f ? 0 : 1;
-      it.sT = sT;
-      const int t = r <= n ? r : r - n - 1;
-      it.xrow = (sT > 0.0f && t < n) ? t : -1;
+    int closed = 0, tail = 0;
+    if (lane == 0) {
+      closed = *reinterpret_cast<volatile int*>(&f.closed);
+      __threadfence_block();
+      tail = *reinterpret_cast<volatile int*>(&f.tail);
+    }
+    closed = __shfl_sync(0xffffffffu, closed, 0);
+    tail = __shfl_sync(0xffffffffu, tail, 0);
+    if (idx < tail) {
+      it = unpack_item(f.e[idx % kFifo]);
+      if (!closed && tail - idx <= kFifoLow) try_refill(P, pl, f, lane, false);
       return true;
     }
-    const int last_end = __shfl_sync(0xffffffffu, w.end, 31);
-    if (w.w0 + 32 >= P.B) return false;
-    load_window(P, w, w.w0 + 32, last_end, lane);
+    if (closed) return false;
+    if (!try_refill(P, pl, f, lane, true)) __nanosleep(32);
+    if (clock64() - t0 > kWaitLimitCycles) {
+      if (lane == 0) atomicOr(P.header + kHStatus, SPECV_DEV_TIMEOUT);
+      return false;
+    }
   }
 }
 
-// Lane 0: stages an item into slot s of the agent's ring.  A draw item's
-// decision fields come with it (cp.async on the slot's barrier).
+// Whole warp: one agent of the stats kernel.  It keeps one item ahead of
+// its ring and issues it as soon as a slot frees.
 template <int DT>
-__device__ void issue(const Params& P, AgentSmem& A, unsigned char* slot, int s, const Item& it) {
-  const int K = P.K;
-  uintptr_t src0 = 0, src1 = 0;
-  uint32_t n0 = 0, n1 = 0;
-  unsigned char *dst0 = slot, *dst1 = slot;
-  Item& dst = A.item[s];
-  dst.kind = it.kind;
-  dst.b = it.b;
-  dst.row = it.row;
-  dst.c = it.c;
-  dst.mode = it.mode;
-  dst.sT = it.sT;
-  dst.xrow = it.xrow;
-  dst.peek_b = it.peek_b;
-  fence_proxy_async_smem();
-  bool small = false;
-  if (it.peek_b >= 0) {   // a sample of the draw cursor's request state
-    cp_async16(&dst.peek, &P.req[it.peek_b].state);
-    small = true;
-  }
-  if (it.kind == kItemStats && it.xrow >= 0) {
-    cp_async4(&dst.x, P.draft_tokens + static_cast<size_t>(it.b) * K + it.xrow);
-    small = true;
-  }
-  if (it.kind == kItemDraw) {
-    cp_async16(&dst.prm, &P.req[it.b].prm);
-    small = true;
-  }
-  if (small) cp_async_arrive(&A.full[s]);
-  if (it.kind == kItemStats) {
-    const bool is_draft = it.row > K;
-    const uintptr_t row = is_draft
-        ? row_addr<DT>(P.draft, static_cast<size_t>(it.b) * K + (it.row - K - 1), P.V)
-        : row_addr<DT>(P.target, static_cast<size_t>(it.b) * (K + 1) + it.row, P.V);
-    const Chunk k = chunk_of<DT>(row, P.V, it.c, kChunkBytes);
-    n0 = bulk_span<DT>(k, is_draft ? P.d_lo : P.t_lo, is_draft ? P.d_hi : P.t_hi, &src0);
-    if (n0) dst0 = slot + (src0 - k.g0);
-  } else {
-    const uintptr_t rp = row_addr<DT>(P.target, static_cast<size_t>(it.b) * (K + 1) + it.row, P.V);
-    const Chunk kp = chunk_of<DT>(rp, P.V, it.c, kDrawBytes);
-    n0 = bulk_span<DT>(kp, P.t_lo, P.t_hi, &src0);
-    if (n0) dst0 = slot + (src0 - kp.g0);
-    if (it.mode) {
-      const uintptr_t rq = row_addr<DT>(P.draft, static_cast<size_t>(it.b) * K + it.row, P.V);
-      const Chunk kq = draft_part<DT>(rq, kp);
-      n1 = bulk_span<DT>(kq, P.d_lo, P.d_hi, &src1);
-      if (n1) dst1 = slot + kDraftOff + (src1 - kq.g0);
-    }
-  }
-  mbar_arrive_expect_tx(&A.full[s], n0 + n1);
-  if (n0) bulk_copy_g2s(dst0, src0, n0, &A.full[s]);
-  if (n1) bulk_copy_g2s(dst1, src1, n1, &A.full[s]);
-}
-
-// Whole warp: reduces the item in a slot and writes its record (lane 0).
-template <int DT>
-__device__ __forceinline__ void consume(const Params& P, unsigned char* slot, const Item& it,
-                                        int lane) {
-  const int K = P.K;
-  if (it.kind == kItemStats) {
-    const bool is_draft = it.row > K;
-    const uintptr_t row = is_draft
-        ? row_addr<DT>(P.draft, static_cast<size_t>(it.b) * K + (it.row - K - 1), P.V)
-        : row_addr<DT>(P.target, static_cast<size_t>(it.b) * (K + 1) + it.row, P.V);
-    const Chunk k = chunk_of<DT>(row, P.V, it.c, kChunkBytes);
-    fix_edges<DT>(k, is_draft ? P.d_lo : P.t_lo, is_draft ? P.d_hi : P.t_hi, slot, lane);
-    uint32_t lo, hi;
-    if (it.mode) {
-      const float2 r = chunk_argmax<DT>(slot, k, lane);
-      lo = __float_as_uint(r.x);
-      hi = __float_as_uint(r.y) | kReady;
-    } else {
-      const float2 r = chunk_softmax<DT>(slot, k, it.sT, lane);
-      lo = __float_as_uint(r.x);
-      hi = ready_bits(r.y);
-    }
-    if (lane == 0) {
-      st_record(P.part + (static_cast<size_t>(it.b) * P.R + it.row) * P.NC + it.c, lo, hi);
-      // the drafted token's logit, from the chunk that holds it
-      if (it.xrow >= 0 && it.x >= k.e_lo && it.x < k.e_hi)
-        st_record(P.zx + static_cast<size_t>(it.b) * P.R + it.row,
-                  __float_as_uint(Elt<DT>::load(slot + k.off0 + it.x * Elt<DT>::kBytes)), kReady);
-    }
-  } else {
-    const uintptr_t rp = row_addr<DT>(P.target, static_cast<size_t>(it.b) * (K + 1) + it.row, P.V);
-    const Chunk kp = chunk_of<DT>(rp, P.V, it.c, kDrawBytes);
-    fix_edges<DT>(kp, P.t_lo, P.t_hi, slot, lane);
-    Chunk kq = kp;
-    if (it.mode) {
-      const uintptr_t rq = row_addr<DT>(P.draft, static_cast<size_t>(it.b) * K + it.row, P.V);
-      kq = draft_part<DT>(rq, kp);
-      fix_edges<DT>(kq, P.d_lo, P.d_hi, slot + kDraftOff, lane);
-    }
-    const float t = chunk_draw<DT>(slot, kp, kq, it.mode != 0, it.prm, lane);
-    if (lane == 0) st_record(P.dpart + static_cast<size_t>(it.b) * P.NCd + it.c, 0u, ready_bits(t));
-  }
-}
-
-template <int DT>
-__device__ void agent(const Params& P, AgentSmem& A, unsigned char* ring, int lane, int aid,
-                      int G, uint32_t tag) {
-  Window w;
-  load_window(P, w, 0, 0, lane);
-  int g = aid;                       // next stats item
-  bool stats_left = true;
-  const int Dtot = P.B * P.NCd;      // < 2^31 within the size limits
-  int d = aid;                       // next owned draw item
-  int cur_b = d < Dtot ? d / P.NCd : -1;   // its request
-  unsigned long long cur = 0;        // latest sample of that request's state
+__device__ void stats_agent(const Params& P, const Plan& pl, Agent& ag, Fifo& fifo) {
+  const int lane = ag.lane;
   int issued = 0, consumed = 0;
-  bool ok = true;
-
+  bool more = true, have = false;
+  Item pend;
   for (;;) {
-    // ---- the draw cursor, from the latest state sample ------------------
-    bool draw_ready = false;
-    uint32_t payload = 0;
-    if (d < Dtot && (cur >> 32) == tag) {
-      const uint32_t pl = static_cast<uint32_t>(cur);
-      if ((pl & 3u) == kStateDraws) {
-        draw_ready = true;
-        payload = pl;
-        // the decision's fields were written before its state (release);
-        // the draw items read them from L2 after this
-        __threadfence();
-      } else {
-        // nothing to draw for this request: skip to an owned item past it
-        const int nb = (cur_b + 1) * P.NCd;
-        d += ((nb - d + G - 1) / G) * G;
-        cur_b = d < Dtot ? d / P.NCd : -1;
-        cur = 0;
-      }
-    }
-    // ---- top up the ring without waiting -------------------------------
     while (issued - consumed < kSlots) {
-      Item it;
-      if (draw_ready) {
-        it.kind = kItemDraw;
-        it.b = cur_b;
-        it.row = static_cast<int>((payload >> 3) & 31u);
-        it.c = d - cur_b * P.NCd;
-        it.mode = static_cast<int>((payload >> 2) & 1u);
-        it.sT = 0.0f;
-        it.xrow = -1;
-        d += G;
-        if (d >= Dtot || d / P.NCd != cur_b) {
-          draw_ready = false;
-          cur_b = d < Dtot ? d / P.NCd : -1;
-          cur = 0;
-        }
-      } else if (stats_left) {
-        if (!map_item(P, w, g, lane, it)) {
-          stats_left = false;
-          continue;
-        }
-        g += G;
-      } else {
-        break;
-      }
-      it.peek_b = (cur_b >= 0 && !draw_ready) ? cur_b : -1;   // sample it with this item
-      const int s = issued % kSlots;
-      __syncwarp();
-      if (lane == 0) issue<DT>(P, A, ring + static_cast<size_t>(s) * kSlotBytes, s, it);
-      ++issued;
-    }
-
-    if (issued == consumed) {
-      // ring empty and no stats items left: poll the draw cursor's request
-      if (d >= Dtot) break;
-      const long long t0 = clock64();
-      cur = ld_relaxed_u64(&P.req[cur_b].state);
-      while ((cur >> 32) != tag) {
-        __nanosleep(200);
-        cur = ld_relaxed_u64(&P.req[cur_b].state);
-        if (clock64() - t0 > kWaitLimitCycles) {
-          ok = false;
+      if (!have) {
+        if (!more || !pop_item(P, pl, fifo, lane, pend)) {
+          more = false;
           break;
         }
+        have = true;
       }
-      if (!ok) break;
-      continue;
+      __syncwarp();
+      if (lane == 0) issue<DT>(P, ag, issued % kSlots, pend);
+      ++issued;
+      have = false;
     }
-
-    // ---- consume the oldest slot -----------------------------------------
+    if (issued == consumed) break;   // no tickets left and nothing in flight
+    if (more && !have) have = pop_item(P, pl, fifo, lane, pend);   // decode ahead
+    if (!have) more = false;
     const int s = consumed % kSlots;
-    const uint32_t ph = static_cast<uint32_t>(consumed / kSlots) & 1u;
-    if (!warp_wait(&A.full[s], ph)) {
-      ok = false;
-      break;
-    }
-    const Item it = A.item[s];
-    if (it.peek_b >= 0 && it.peek_b == cur_b && (it.peek >> 32) == tag) cur = it.peek;
-    consume<DT>(P, ring + static_cast<size_t>(s) * kSlotBytes, it, lane);
+    if (!wait_slot(P, ag, s)) return;
+    consume_stats<DT>(P, ag, s, ag.A->item[s]);
     ++consumed;
   }
-  if (!ok && lane == 0) atomicOr(P.header + kHStatus, SPECV_DEV_TIMEOUT);
 }
 
-// ---------------------------------------------------------------- control
-
-// The control warp of CTA x decides requests x, x + grid, x + 2 grid, ... in
-// order, each once its stats records are all written, and draws the final
-// token of each decided sampled request once its draw records are written
-// (in decision order, up to kPend pending).  Requests whose length or
-// temperature is unusable are answered first.
 template <int DT>
-__device__ void control(const Params& P, Smem& S, int lane, uint32_t tag) {
-  const int x = static_cast<int>(blockIdx.x), grid = static_cast<int>(gridDim.x);
-  // this CTA's requests' tokens and uniforms into L2 now, while the memory
-  // system is idle; the decisions read them much later
-  for (int b = x + lane * grid; b < P.B; b += 32 * grid) {
-    prefetch_l2(P.draft_tokens + static_cast<size_t>(b) * P.K);
-    prefetch_l2(P.uniforms + static_cast<size_t>(b) * (P.K + 1));
-    prefetch_l2(P.uniforms_resample + b);
-  }
-  // unusable requests are answered now; greedy ones never have draw items,
-  // which their owners learn from the state
-  for (int base = x; base < P.B; base += 32 * grid) {
-    const int b = base + lane * grid;
-    int bad = 0;
-    if (b < P.B) {
-      const float T = __ldg(P.temperature + b);
-      bad = request_bad(P, request_len(P, b), T);
-      if (!bad && !(T > 0.0f)) set_state(P, b, tag, kStateNone);
-    }
-    for (unsigned m = __ballot_sync(0xffffffffu, bad != 0); m; m &= m - 1) {
-      const int i = __ffs(m) - 1;
-      finish_bad(P, base + i * grid, __shfl_sync(0xffffffffu, bad, i), lane, tag);
-    }
-  }
-  uint32_t cphase = 0;   // phases of the control warp's chunk barrier
-  int dec = x;              // next request to decide
-  int dn = 0;               // its length and temperature
-  float dT = 0.0f;
-  bool dvalid = false;
-  if (dec < P.B) {
-    dn = request_len(P, dec);
-    dT = __ldg(P.temperature + dec);
-  }
-  int ph = 0, pt = 0;       // pending draws [pt, ph)
-  long long idle_since = clock64();
-  bool ok = true;
-  while (dec < P.B || pt < ph) {
-    bool progress = false;
-    if (dec < P.B && ph - pt < kPend) {
-      dvalid = request_bad(P, dn, dT) == 0;
-      int r = 1;
-      if (dvalid) {
-        Pend pe;
-        r = try_decide<DT>(P, S, cphase, dec, dn, dT, lane, tag, pe);
-        if (r == 2) {
-          if (lane == 0) S.pend[ph % kPend] = pe;
-          ++ph;
-        }
-      }
-      if (r) {
-        dec += grid;
-        if (dec < P.B) {
-          dn = request_len(P, dec);
-          dT = __ldg(P.temperature + dec);
-        }
-        progress = true;
-      }
-      __syncwarp();
-    }
-    if (pt < ph) {
-      const Pend pe = S.pend[pt % kPend];
-      if (try_search<DT>(P, S, cphase, pe, lane, tag)) {
-        ++pt;
-        progress = true;
-      }
-      __syncwarp();
-    }
-    if (progress) {
-      idle_since = clock64();
-    } else {
-      if (clock64() - idle_since > kWaitLimitCycles) {
-        ok = false;
-        break;
-      }
-      __nanosleep(128);
-    }
-  }
-  if (!ok && lane == 0) atomicOr(P.header + kHStatus, SPECV_DEV_TIMEOUT);
-}
-
-// ---------------------------------------------------------------- kernel
-
-template <int DT>
-__global__ void __launch_bounds__(kThreads) verify_kernel(const Params P) {
+__global__ void __launch_bounds__(kThreads, 1) stats_kernel(const Params P) {
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   __shared__ Smem S;
   extern __shared__ __align__(128) unsigned char dyn[];
 
-  if (tid < kAgents * kSlots) mbar_init(&S.ag[tid / kSlots].full[tid % kSlots], 1);
-  if (tid == 0) mbar_init(&S.cbar, 1);
-  if (tid == 0) {
-    S.tag = static_cast<uint32_t>(P.header[kHEpoch]) + 1u;
+  if (tid < kAgents * kSlots) {
+    mbar_init(&S.ag[tid / kSlots].bar[tid % kSlots], 1);
     mbar_init_fence();
   }
-  __syncthreads();
+  if (tid == 0) S.fifo.head = S.fifo.tail = S.fifo.lock = S.fifo.closed = S.fifo.last = 0;
+  build_plan(P, S.plan, S.red);   // ends with a CTA barrier
+  allow_dependents();
 
-  if (warp < kAgents) {
-    const int G = static_cast<int>(gridDim.x) * kAgents;
-    const int aid = warp * static_cast<int>(gridDim.x) + static_cast<int>(blockIdx.x);
-    agent<DT>(P, S.ag[warp], dyn + static_cast<size_t>(warp) * kSlots * kSlotBytes, tid & 31, aid,
-              G, S.tag);
-  } else {
-    control<DT>(P, S, tid & 31, S.tag);
-  }
+  Agent ag;
+  ag.A = &S.ag[warp];
+  ag.ring = dyn + static_cast<size_t>(warp) * kSlots * kSlotBytes;
+  ag.ph = 0;
+  ag.lane = tid & 31;
+  stats_agent<DT>(P, S.plan, ag, S.fifo);
 
   __syncthreads();
   if (tid == 0) {
     __threadfence();
     const int prev = atomicAdd(P.header + kHExit, 1);
     if (prev == static_cast<int>(gridDim.x) - 1) {
-      // last CTA of the launch: every item is done and every request
-      // answered; reset for the next call
+      // last CTA: every ticket is taken; reset for the next call
       P.header[kHExit] = 0;
-      P.header[kHEpoch] = P.header[kHEpoch] + 1;
+      P.header[kHTicket] = 0;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- decide kernel
+
+template <int DT>
+__global__ void __launch_bounds__(kDecideWarps * 32) decide_kernel(const Params P) {
+  __shared__ AgentSmem A[kDecideWarps];
+  extern __shared__ __align__(128) unsigned char dyn[];
+  const int tid = threadIdx.x, warp = tid >> 5;
+  if ((tid & 31) == 0) {
+    mbar_init(&A[warp].bar[0], 1);
+    mbar_init_fence();
+  }
+  __syncwarp();
+  wait_previous();
+  allow_dependents();
+  Agent ag;
+  ag.A = &A[warp];
+  ag.ring = dyn + static_cast<size_t>(warp) * kSlotBytes;
+  ag.ph = 0;
+  ag.lane = tid & 31;
+  for (int b = blockIdx.x * kDecideWarps + warp; b < P.B; b += gridDim.x * kDecideWarps)
+    decide_request<DT>(P, ag, b);
+}
+
+// ---------------------------------------------------------------- residual kernel
+
+// Whole warp: sums the residual (p - q)+ of the piece pair in slot s and
+// counts it; the warp completing the request's pieces draws its token.
+template <int DT>
+__device__ void consume_residual(const Params& P, Agent& ag, int s, const Item& it) {
+  const int lane = ag.lane;
+  unsigned char* slot = ag.slot(s);
+  const Chunk kp = chunk_of<DT>(target_row<DT>(P, it.b, it.row), P.V, it.c, kDrawBytes);
+  fix_edges<DT>(kp, P.t_lo, P.t_hi, slot, lane);
+  const Chunk kq = draft_part<DT>(draft_row<DT>(P, it.b, it.row), kp);
+  fix_edges<DT>(kq, P.d_lo, P.d_hi, slot + kDraftOff, lane);
+  const float t = chunk_draw<DT>(slot, kp, kq, true, it.prm, lane);
+  const int e = it.n;   // the request's entry in the list
+  int old = 0;
+  if (lane == 0) {
+    st_word(P.dmass + static_cast<size_t>(e) * P.NCd + it.c, ready_bits(t));
+    old = atomicAdd(&P.req[it.b].cnt, 1);
+  }
+  old = __shfl_sync(0xffffffffu, old, 0);
+  if (old != P.NCd - 1) return;
+  if (lane == 0) P.req[it.b].cnt = 0;   // every piece is in: ready for the next call
+  __syncwarp();
+  residual_search<DT>(P, ag, s, e, it.b, it.row, it.prm);
+}
+
+// Whole warp: residual item i (entry i / NCd, piece i mod NCd).
+__device__ __forceinline__ Item residual_item(const Params& P, int i) {
+  Item it;
+  const int e = i / P.NCd;
+  it.kind = kItemR;
+  it.c = i - e * P.NCd;
+  it.n = e;
+  it.b = __ldcg(P.rlist + e);
+  it.row = __ldcg(&P.req[it.b].j);
+  it.prm = __ldcg(&P.req[it.b].prm);
+  it.sT = 0.0f;
+  it.x = -1;
+  it.pad = 0;
+  return it;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 1) residual_kernel(const Params P) {
+  __shared__ AgentSmem A[kAgents];
+  extern __shared__ __align__(128) unsigned char dyn[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid < kAgents * kSlots) {
+    mbar_init(&A[tid / kSlots].bar[tid % kSlots], 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+  wait_previous();
+  Agent ag;
+  ag.A = &A[warp];
+  ag.ring = dyn + static_cast<size_t>(warp) * kSlots * kSlotBytes;
+  ag.ph = 0;
+  ag.lane = lane;
+  const int count = __ldcg(P.header + kHResid);
+  const int total = count * P.NCd;
+  const int G = static_cast<int>(gridDim.x) * kAgents;
+  int next = static_cast<int>(blockIdx.x) * kAgents + warp;
+  int issued = 0, consumed = 0;
+  bool ok = true;
+  for (;;) {
+    while (issued - consumed < kSlots && next < total) {
+      const Item it = residual_item(P, next);
+      next += G;
+      __syncwarp();
+      if (lane == 0) issue<DT>(P, ag, issued % kSlots, it);
+      ++issued;
+    }
+    if (issued == consumed) break;
+    const int s = consumed % kSlots;
+    if (!wait_slot(P, ag, s)) {
+      ok = false;
+      break;
+    }
+    consume_residual<DT>(P, ag, s, A[warp].item[s]);
+    ++consumed;
+  }
+  (void)ok;
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    const int prev = atomicAdd(P.header + kHExit3, 1);
+    if (prev == static_cast<int>(gridDim.x) - 1) {
+      P.header[kHExit3] = 0;
+      P.header[kHResid] = 0;   // the list is used up: empty for the next call
     }
   }
 }
 
 // ---------------------------------------------------------------- host side
 
+
 int elt_bytes(specv_dtype dt) { return dt == SPECV_BF16 ? 2 : 4; }
 
 struct Layout {
-  size_t header, req, part, dpart, zx, total;
+  size_t header, req, part, zx, rlist, dmass, total;
 };
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
@@ -1641,21 +1656,30 @@ int chunks_per_row(int V, specv_dtype dt, int CB) {
   return static_cast<int>((15 + static_cast<long long>(V) * elt_bytes(dt) + CB - 1) / CB);
 }
 
+// Requests per launch sequence: larger batches run as consecutive
+// sequences that share the workspace.
+int launch_batch(int B) { return B < kPlanMax ? B : kPlanMax; }
+
 Layout ws_layout(int B, int K, int V, specv_dtype dt) {
+  const size_t Bl = static_cast<size_t>(launch_batch(B));
   const size_t R = 2 * static_cast<size_t>(K) + 1;
   const size_t NC = chunks_per_row(V, dt, kChunkBytes);
   const size_t NCd = chunks_per_row(V, dt, kDrawBytes);
   Layout L;
   L.header = 0;
   L.req = kHeaderBytes;
-  L.part = align256(L.req + sizeof(Req) * static_cast<size_t>(B));
-  L.dpart = align256(L.part + sizeof(uint2) * B * R * NC);
-  L.zx = align256(L.dpart + sizeof(uint2) * static_cast<size_t>(B) * NCd);
-  L.total = align256(L.zx + sizeof(uint2) * static_cast<size_t>(B) * R);
+  L.part = align256(L.req + sizeof(Req) * Bl);
+  L.zx = align256(L.part + sizeof(uint2) * Bl * R * NC);
+  L.rlist = align256(L.zx + sizeof(float) * Bl * R);
+  L.dmass = align256(L.rlist + sizeof(int32_t) * Bl);
+  L.total = align256(L.dmass + sizeof(uint32_t) * Bl * NCd);
   return L;
 }
 
-// Resident CTAs of the kernel on the current device, cached per device.
+constexpr int kDecideSmem = kDecideWarps * kSlotBytes;
+
+// Resident CTAs of the stats kernel on the current device (one per SM),
+// with every kernel's shared-memory limit raised once per device.
 template <int DT>
 cudaError_t resident_ctas(int* out) {
   static std::mutex mu;
@@ -1666,11 +1690,17 @@ cudaError_t resident_ctas(int* out) {
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(mu);
   if (!cache[dev]) {
-    e = cudaFuncSetAttribute(verify_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(stats_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kRingBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(residual_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kRingBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(decide_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kDecideSmem);
     if (e != cudaSuccess) return e;
     int per_sm = 0, sms = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, verify_kernel<DT>, kThreads,
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stats_kernel<DT>, kThreads,
                                                       kRingBytes);
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -1685,14 +1715,43 @@ cudaError_t resident_ctas_for(specv_dtype dtype, int* out) {
   return dtype == SPECV_BF16 ? resident_ctas<SPECV_BF16>(out) : resident_ctas<SPECV_F32>(out);
 }
 
-// CTAs for a call: enough agents for the stats items of every row, at most
-// the resident count.
+// CTAs of the stats kernel: enough agents for two chunks each, at most the
+// resident count.
 int grid_for(int B, int K, int V, specv_dtype dtype, int ctas) {
-  const long long items =
-      static_cast<long long>(B) * (2 * K + 1) * chunks_per_row(V, dtype, kChunkBytes);
-  long long want = (items + kAgents - 1) / kAgents;
+  const long long items = static_cast<long long>(launch_batch(B)) * (2 * K + 1) *
+                          chunks_per_row(V, dtype, kChunkBytes);
+  long long want = (items + 2 * kAgents - 1) / (2 * kAgents);
   if (want < 1) want = 1;
   return static_cast<int>(want < ctas ? want : ctas);
+}
+
+// Launches kernel<<<grid, block, smem, stream>>>(P) as a programmatic
+// dependent of the previous kernel on the stream.
+template <class Kern>
+cudaError_t launch_dependent(Kern kernel, int grid, int block, int smem, cudaStream_t stream,
+                             const Params& P) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(static_cast<unsigned>(block));
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, P);
+}
+
+template <int DT>
+cudaError_t launch_sequence(const Params& P, int grid, cudaStream_t stream) {
+  stats_kernel<DT><<<grid, kThreads, kRingBytes, stream>>>(P);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int dgrid = (P.B + kDecideWarps - 1) / kDecideWarps;
+  e = launch_dependent(decide_kernel<DT>, dgrid, kDecideWarps * 32, kDecideSmem, stream, P);
+  if (e != cudaSuccess) return e;
+  return launch_dependent(residual_kernel<DT>, grid, kThreads, kRingBytes, stream, P);
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -1727,41 +1786,46 @@ specv_status launch(const void* target, const void* draft, specv_dtype dtype,
 
   const Layout L = ws_layout(B, K, V, dtype);
   unsigned char* ws = static_cast<unsigned char*>(workspace);
-  Params P;
-  P.target = static_cast<const unsigned char*>(target);
-  P.draft = static_cast<const unsigned char*>(draft);
-  P.draft_tokens = draft_tokens;
-  P.draft_len = draft_len;
-  P.temperature = temperature;
-  P.uniforms = uniforms;
-  P.uniforms_resample = uniforms_resample;
-  P.B = B;
-  P.K = K;
-  P.V = V;
-  P.R = 2 * K + 1;
-  P.NC = chunks_per_row(V, dtype, kChunkBytes);
-  P.NCd = chunks_per_row(V, dtype, kDrawBytes);
-  P.inv_NC = 1.0f / static_cast<float>(P.NC);
-  const uintptr_t t0 = reinterpret_cast<uintptr_t>(target);
-  const uintptr_t d0 = reinterpret_cast<uintptr_t>(draft);
-  P.t_lo = up16(t0);
-  P.t_hi = down16(t0 + static_cast<size_t>(B) * (K + 1) * V * eb);
-  P.d_lo = draft ? up16(d0) : 0;
-  P.d_hi = draft ? down16(d0 + static_cast<size_t>(B) * K * V * eb) : 0;
-  P.accepted_len = accepted_len;
-  P.out_tokens = out_tokens;
-  P.header = reinterpret_cast<int32_t*>(ws + L.header);
-  P.req = reinterpret_cast<Req*>(ws + L.req);
-  P.part = reinterpret_cast<uint2*>(ws + L.part);
-  P.dpart = reinterpret_cast<uint2*>(ws + L.dpart);
-  P.zx = reinterpret_cast<uint2*>(ws + L.zx);
-  P.row_stats = row_stats;
-
-  if (dtype == SPECV_BF16)
-    verify_kernel<SPECV_BF16><<<grid, kThreads, kRingBytes, stream>>>(P);
-  else
-    verify_kernel<SPECV_F32><<<grid, kThreads, kRingBytes, stream>>>(P);
-  return cudaGetLastError() == cudaSuccess ? SPECV_OK : SPECV_ERR_CUDA;
+  // Batches beyond one launch sequence run as consecutive sequences on
+  // `stream`; each leaves the workspace ready for the next.
+  for (int b0 = 0; b0 < B; b0 += kPlanMax) {
+    const int Bl = B - b0 < kPlanMax ? B - b0 : kPlanMax;
+    Params P;
+    P.target = static_cast<const unsigned char*>(target) + static_cast<size_t>(b0) * (K + 1) * V * eb;
+    P.draft = draft ? static_cast<const unsigned char*>(draft) + static_cast<size_t>(b0) * K * V * eb
+                    : nullptr;
+    P.draft_tokens = draft_tokens + static_cast<size_t>(b0) * K;
+    P.draft_len = draft_len ? draft_len + b0 : nullptr;
+    P.temperature = temperature + b0;
+    P.uniforms = uniforms + static_cast<size_t>(b0) * (K + 1);
+    P.uniforms_resample = uniforms_resample + b0;
+    P.B = Bl;
+    P.K = K;
+    P.V = V;
+    P.R = 2 * K + 1;
+    P.NC = chunks_per_row(V, dtype, kChunkBytes);
+    P.NCd = chunks_per_row(V, dtype, kDrawBytes);
+    P.inv_NC = 1.0f / static_cast<float>(P.NC);
+    const uintptr_t t0 = reinterpret_cast<uintptr_t>(P.target);
+    const uintptr_t d0 = reinterpret_cast<uintptr_t>(P.draft);
+    P.t_lo = up16(t0);
+    P.t_hi = down16(t0 + static_cast<size_t>(Bl) * (K + 1) * V * eb);
+    P.d_lo = draft ? up16(d0) : 0;
+    P.d_hi = draft ? down16(d0 + static_cast<size_t>(Bl) * K * V * eb) : 0;
+    P.accepted_len = accepted_len + b0;
+    P.out_tokens = out_tokens + static_cast<size_t>(b0) * (K + 1);
+    P.header = reinterpret_cast<int32_t*>(ws + L.header);
+    P.req = reinterpret_cast<Req*>(ws + L.req);
+    P.part = reinterpret_cast<uint2*>(ws + L.part);
+    P.zx = reinterpret_cast<float*>(ws + L.zx);
+    P.rlist = reinterpret_cast<int32_t*>(ws + L.rlist);
+    P.dmass = reinterpret_cast<uint32_t*>(ws + L.dmass);
+    P.row_stats = row_stats ? row_stats + static_cast<size_t>(b0) * (K + 1) * 8 : nullptr;
+    const cudaError_t e = dtype == SPECV_BF16 ? launch_sequence<SPECV_BF16>(P, grid, stream)
+                                              : launch_sequence<SPECV_F32>(P, grid, stream);
+    if (e != cudaSuccess) return SPECV_ERR_CUDA;
+  }
+  return SPECV_OK;
 }
 
 size_t pad256(size_t x) { return align256(x); }
@@ -1802,7 +1866,7 @@ cudaError_t noalloc_scratch(void** out) {
 
 extern "C" {
 
-int specv_version(void) { return 400; }
+int specv_version(void) { return 500; }
 
 int specv_max_vocab(specv_dtype dtype) {
   if (dtype != SPECV_F32 && dtype != SPECV_BF16) return 0;

@@ -100,7 +100,7 @@ def test_binding_refuses_cpu_tensors():
 
 def test_noalloc_rejects_shapes_beyond_its_array(L):
     # the size check runs on the host before any pointer is used
-    B, K, V = 2048, 16, 50000
+    B, K, V = 1024, 16, 500000
     assert L.specv_workspace_bytes(B, K, V, 1) > _native.NOALLOC_SCRATCH_BYTES
     rc = L.spec_verify_sample_noalloc(FAKE, FAKE, 1, FAKE, FAKE, FAKE, FAKE, FAKE, B, K, V, FAKE,
                                       FAKE, None)
