@@ -14,11 +14,10 @@
 //
 //  1. stats_kernel streams every row a request needs (target rows t <= n,
 //     draft rows t < n when sampled) once from HBM with TMA bulk copies,
-//     in 12 KB chunks.  Each warp is an agent with a private ring of two
-//     shared-memory slots; a CTA's warps take chunks in order from a
-//     shared-memory queue that one warp at a time refills by claiming a
-//     block of tickets from a global counter and decoding it, one ticket
-//     per lane.  A chunk is reduced to a record: its maximum and sum of
+//     in 6 KB chunks.  Each warp is an agent with a private ring of two
+//     shared-memory slots; warp g of the grid's G takes chunks g, g + G,
+//     g + 2 G, ... (decoded 32 at a time, one per lane).  A chunk is
+//     reduced to a record: its maximum and sum of
 //     exp((z - max)/T), or at T = 0 its maximum and lowest argmax.  The
 //     chunk holding a drafted token also records that token's logit.
 //  2. decide_kernel, one warp per request, combines the records, runs the
@@ -27,7 +26,7 @@
 //     records, the token from one re-read chunk.  A rejected sampled
 //     request is appended to a list for the residual draw.
 //  3. residual_kernel reads the rejected rows again (target and draft, in
-//     6 KB pieces), sums (p - q)+ per piece, and the warp that completes a
+//     3 KB pieces), sums (p - q)+ per piece, and the warp that completes a
 //     request's pieces draws its token: the piece from the sums, the token
 //     from one re-read piece pair.
 //
@@ -47,18 +46,17 @@
 
 namespace {
 
-constexpr int kAgents = 8;                              // agent warps per CTA
+constexpr int kAgents = 16;                             // agent warps per CTA
 constexpr int kThreads = kAgents * 32;
 constexpr int kSlots = 2;                               // ring slots per agent
-constexpr int kChunkBytes = 12288;                      // deciding / bonus item: one chunk of one row
-constexpr int kDrawBytes = 6144;                        // residual item: this much of each row
+constexpr int kChunkBytes = 6144;                       // deciding / bonus item: one chunk of one row
+constexpr int kDrawBytes = 3072;                        // residual piece: this much of each row
 constexpr int kDrawSweeps = kDrawBytes / 512;           // 32 lanes x 16 bytes per sweep
 constexpr int kDraftOff = kDrawBytes;                   // draft part of a residual slot
 constexpr int kSlotBytes = kChunkBytes + 32;
 constexpr int kRingBytes = kAgents * kSlots * kSlotBytes;
 constexpr int kPlanMax = 1024;                          // requests per launch (the host splits)
 constexpr int kDecideWarps = 8;                         // decide_kernel: one warp per request
-constexpr int kBlockMax = 32;                           // tickets a warp claims at once, at most
 constexpr int kMaxRowBytes = 1 << 21;                   // 2 MB per row of logits
 constexpr int kMaxChunks = (kMaxRowBytes + 15 + kChunkBytes - 1) / kChunkBytes;
 constexpr int kMaxDrawChunks = (kMaxRowBytes + 15 + kDrawBytes - 1) / kDrawBytes;
@@ -68,13 +66,12 @@ constexpr uint32_t kSuspendHintNs = 20000;
 static_assert(kSlotBytes >= kDraftOff + kDrawBytes + 16, "residual slot too small");
 static_assert(kSlotBytes % 16 == 0, "slots must keep 16-byte alignment");
 static_assert(kMaxChunks * 8 <= kSlotBytes, "the records of one row fit a slot");
-static_assert(kMaxChunks <= 6 * 32, "the chunk masses of a row fit six per lane");
 static_assert(kMaxDrawChunks * 4 <= kSlotBytes, "the residual masses of one row fit a slot");
-static_assert(kMaxDrawChunks < 512 && kMaxChunks < 512, "a chunk index fits 9 bits");
+static_assert(kMaxChunks < 512, "a stats chunk index fits 9 bits");
 static_assert(kPlanMax <= 1024 && 2 * SPECV_MAX_DRAFT + 1 < 64, "a request fits 10 bits, a row 6");
 
 // workspace header words (int32 index), one 128-byte line each
-constexpr int kHStatus = 0, kHExit = 32, kHTicket = 64, kHResid = 96, kHExit3 = 128;
+constexpr int kHStatus = 0, kHResid = 96, kHExit3 = 128;
 constexpr int kHeaderBytes = 1024;
 static_assert((kHExit3 + 1) * 4 <= kHeaderBytes, "header words fit the header");
 
@@ -122,6 +119,8 @@ struct Params {
   float* zx;        // [B][R] the drafted token's logit in rows t < n
   int32_t* rlist;   // [B] requests waiting for a residual draw (count: header[kHResid])
   uint32_t* dmass;  // [B][NCd] residual mass records: mass | ready
+  uint32_t* dsw;    // [B][NCd][kDrawSweeps] residual sweep-sum records: sum | ready
+  float* bsw;       // [B][NC][kChunkBytes / 512] sweep sums of each sampled request's row n
   float* row_stats; // [B][K+1][8] or null
 };
 
@@ -142,7 +141,7 @@ struct __align__(16) Item {
   int n;        // the request's draft length
   float sT;     // log2(e)/T (0: greedy)
   int x;        // drafted token of the row (rows t < n of sampled requests), else -1
-  int pad;
+  int bonus;    // the row is target row n of a sampled request (its sweep sums are kept)
   float4 prm;   // residual: the decision's Mp, Mq, log2(e)/T, S_p/S_q
 };
 
@@ -151,23 +150,8 @@ struct AgentSmem {
   Item item[kSlots];   // the items in the slots
 };
 
-// The CTA's queue of decoded items, in ticket order.  A warp that finds it
-// short takes the lock, claims the next block of tickets from the global
-// counter and decodes it, one ticket per lane.
-constexpr int kFifo = 64;
-constexpr int kFifoLow = 16;   // refill when fewer items than this are ready
-struct Fifo {
-  uint4 e[kFifo];
-  int head;     // entries reserved by warps
-  int tail;     // entries published
-  int lock;     // a warp is refilling
-  int closed;   // the last ticket is claimed
-  int last;     // first ticket of this CTA's last claim
-};
-
 struct Smem {
   Plan plan;
-  Fifo fifo;
   AgentSmem ag[kAgents];
   int red[kAgents * 2];
 };
@@ -609,23 +593,26 @@ __device__ __forceinline__ int count_le(const int* a, int n, int x) {
   return lo;
 }
 
-// A decoded item in 16 bytes: kind << 28 | b << 15 | row << 9 | chunk, the
+// A decoded item in 16 bytes: bonus row << 30 | kind << 28 | b << 15 |
+// row << 9 | chunk, the
 // drafted token of the row (or -1), log2(e)/T (0: greedy), draft length.
-__device__ __forceinline__ uint4 pack_item(int kind, int b, int row, int c, int x, float sT, int n) {
-  return make_uint4((static_cast<uint32_t>(kind) << 28) | (static_cast<uint32_t>(b) << 15) |
+__device__ __forceinline__ uint4 pack_item(int kind, int b, int row, int c, int x, float sT, int n,
+                                           bool bonus) {
+  return make_uint4((bonus ? 0x40000000u : 0u) | (static_cast<uint32_t>(kind) << 28) |
+                        (static_cast<uint32_t>(b) << 15) |
                         (static_cast<uint32_t>(row) << 9) | static_cast<uint32_t>(c),
                     static_cast<uint32_t>(x), __float_as_uint(sT), static_cast<uint32_t>(n));
 }
 __device__ __forceinline__ Item unpack_item(uint4 e) {
   Item it;
-  it.kind = static_cast<int>(e.x >> 28);
+  it.kind = static_cast<int>((e.x >> 28) & 3u);
   it.b = static_cast<int>((e.x >> 15) & 0x3FFu);
   it.row = static_cast<int>((e.x >> 9) & 0x3Fu);
   it.c = static_cast<int>(e.x & 0x1FFu);
   it.x = static_cast<int>(e.y);
   it.sT = __uint_as_float(e.z);
   it.n = static_cast<int>(e.w);
-  it.pad = 0;
+  it.bonus = (e.x >> 30) & 1u;
   it.prm = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
   return it;
 }
@@ -644,7 +631,7 @@ __device__ uint4 decode_ticket(const Params& P, const Plan& pl, int t) {
   const int row = slot_row(slot, sampled, n, P.K);
   int x = -1;
   if (sampled && slot < 2 * n) x = __ldg(P.draft_tokens + static_cast<size_t>(b) * P.K + (slot >> 1));
-  return pack_item(kItemA, b, row, c, x, sT, n);
+  return pack_item(kItemA, b, row, c, x, sT, n, sampled && slot == 2 * n);
 }
 // ---------------------------------------------------------------- chunk reductions
 
@@ -890,6 +877,177 @@ __device__ int draw_in_slot(const unsigned char* slot, const Chunk& kp, const Ch
     }
     if (pick < 0) pick = lastq;
     tok = vs.e_base + j * CH + pick;
+  }
+  return __shfl_sync(0xffffffffu, tok, l);
+}
+
+// ---------------------------------------------------------------- sweep sums
+
+constexpr int kChunkSweeps = kChunkBytes / 512;   // 512-byte sweeps of a stats chunk
+
+// Values of slot vector j of a chunk, -inf outside [e_lo, e_hi).
+template <int DT>
+__device__ __forceinline__ void slot_vec(const unsigned char* slot, const Vecs& vs, const Chunk& k,
+                                         int j, float* v) {
+  using E = Elt<DT>;
+  constexpr int CH = E::kPerVec;
+  const int e0 = vs.e_base + j * CH;
+  if (e0 >= k.e_lo && e0 + CH <= k.e_hi) {
+    E::unpack(reinterpret_cast<const uint4*>(slot)[j], v);
+  } else if (e0 + CH > k.e_lo && e0 < k.e_hi) {
+    masked_vec<DT>(slot, vs, k, j, v);
+  } else {
+#pragma unroll
+    for (int q = 0; q < CH; ++q) v[q] = -INFINITY;
+  }
+}
+
+// Whole warp: (max, sum of exp((z - max)/T)) of a stats chunk, and the sum
+// of each 512-byte sweep (slot vectors [32 s, 32 s + 32)), which lane s
+// stores to sw[s].  The chunk sum is the sweep sums added in order.
+template <int DT>
+__device__ float2 chunk_softmax_sweeps(const unsigned char* slot, const Chunk& k, float sT,
+                                       int lane, float* sw) {
+  constexpr int CH = Elt<DT>::kPerVec;
+  const Vecs vs = vecs_of<DT>(k);
+  float m = -INFINITY;
+#pragma unroll 4
+  for (int s = 0; s < kChunkSweeps; ++s) {
+    float v[CH];
+    slot_vec<DT>(slot, vs, k, s * 32 + lane, v);
+#pragma unroll
+    for (int q = 0; q < CH; ++q) m = fmaxf(m, v[q]);
+  }
+  const float M = warp_max(m);
+  if (!(M > -INFINITY)) {
+    if (lane < kChunkSweeps) sw[lane] = 0.0f;
+    return make_float2(M, 0.0f);
+  }
+  const float c = __fmul_rn(M, sT);
+  const float corr = ex2(-__fmaf_rn(M, sT, -c));
+  float S = 0.0f, mine = 0.0f;
+#pragma unroll 4
+  for (int s = 0; s < kChunkSweeps; ++s) {
+    float v[CH];
+    slot_vec<DT>(slot, vs, k, s * 32 + lane, v);
+    float t = 0.0f;
+#pragma unroll
+    for (int q = 0; q < CH; ++q) t = __fadd_rn(t, ex2(__fmaf_rn(v[q], sT, -c)));
+    const float ssum = __fmul_rn(warp_sum(t), corr);
+    if (lane == s) mine = ssum;
+    S = __fadd_rn(S, ssum);
+  }
+  if (lane < kChunkSweeps) sw[lane] = mine;
+  return make_float2(M, S);
+}
+
+// Whole warp: the residual mass of a piece pair in a slot, sweep by sweep
+// (as chunk_draw forms the weights); lane s < kDrawSweeps gets sweep s's
+// sum, every lane the piece's total (the sweep sums added in order).
+template <int DT>
+__device__ float piece_sweeps(const unsigned char* slot, const Chunk& kp, const Chunk& kq,
+                              const float4& prm, int lane, float& mine) {
+  constexpr int CH = Elt<DT>::kPerVec;
+  const Vecs vs = vecs_of<DT>(kp);
+  const bool same = kq.off0 == kp.off0;
+  float total = 0.0f;
+  mine = 0.0f;
+#pragma unroll 4
+  for (int s = 0; s < kDrawSweeps; ++s) {
+    float w[CH];
+    vector_weights<DT>(slot, vs, kp, kq, true, same, prm, s * 32 + lane, w);
+    float t = 0.0f;
+#pragma unroll
+    for (int q = 0; q < CH; ++q) t = __fadd_rn(t, w[q]);
+    const float ssum = warp_sum(t);
+    if (lane == s) mine = ssum;
+    total = __fadd_rn(total, ssum);
+  }
+  return total;
+}
+
+// Values of slot vector j of chunk k read from global memory (the slot's
+// byte 0 is k.g0), -inf outside [e_lo, e_hi); a whole vector is read at
+// once when it lies inside the tensor's aligned range [lo, hi).
+template <int DT>
+__device__ __forceinline__ void global_vec(const Chunk& k, uintptr_t lo, uintptr_t hi, int j,
+                                           float* v) {
+  using E = Elt<DT>;
+  constexpr int CH = E::kPerVec, eb = E::kBytes;
+  const int e0 = -k.off0 / eb + j * CH;
+  const uintptr_t a = k.g0 + static_cast<uintptr_t>(j) * 16;
+  if (e0 >= k.e_lo && e0 + CH <= k.e_hi && a >= lo && a + 16 <= hi) {
+    E::unpack(__ldg(reinterpret_cast<const uint4*>(a)), v);
+    return;
+  }
+#pragma unroll
+  for (int q = 0; q < CH; ++q) {
+    const int e = e0 + q;
+    v[q] = (e >= k.e_lo && e < k.e_hi) ? E::ldg(reinterpret_cast<const unsigned char*>(a + q * eb))
+                                        : -INFINITY;
+  }
+}
+
+// The same elements of another row (a draft row at `row`): element e at
+// row + e * elt.  Elements outside [e_lo, e_hi) read 0.
+template <int DT>
+__device__ __forceinline__ void global_vec_at(uintptr_t row, uintptr_t lo, uintptr_t hi, int e0,
+                                              int e_lo, int e_hi, float* v) {
+  using E = Elt<DT>;
+  constexpr int CH = E::kPerVec, eb = E::kBytes;
+  const uintptr_t a = row + static_cast<intptr_t>(e0) * eb;
+  if (e0 >= e_lo && e0 + CH <= e_hi && (a & 15) == 0 && a >= lo && a + 16 <= hi) {
+    E::unpack(__ldg(reinterpret_cast<const uint4*>(a)), v);
+    return;
+  }
+#pragma unroll
+  for (int q = 0; q < CH; ++q) {
+    const int e = e0 + q;
+    v[q] = (e >= e_lo && e < e_hi) ? E::ldg(reinterpret_cast<const unsigned char*>(a + q * eb))
+                                   : 0.0f;
+  }
+}
+
+// Whole warp: the first of n consecutive masses (lane i < n holds mass i)
+// whose running total exceeds tau; rounding that leaves tau beyond the
+// total falls on the last positive one.  rem gets tau less the masses
+// before it.  -1: nothing positive.
+__device__ __forceinline__ int pick_lane(float mine, int n, float tau, int lane, float& rem) {
+  const float x = lane < n ? mine : 0.0f;
+  const float incl = warp_incl_scan(x, lane);
+  const unsigned hit = __ballot_sync(0xffffffffu, x > 0.0f && incl > tau);
+  const unsigned pos = __ballot_sync(0xffffffffu, x > 0.0f);
+  const int l = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : -1);
+  if (l < 0) return -1;
+  rem = __fsub_rn(tau, __shfl_sync(0xffffffffu, __fsub_rn(incl, x), l));
+  return l;
+}
+
+// Whole warp: the element of one sweep whose running weight first exceeds
+// tau (lane l holds the weights w[] of vector 32 s + l, first element e0);
+// rounding that leaves tau beyond the sweep falls on its last positive
+// element.  -1: nothing positive.
+template <int CH>
+__device__ __forceinline__ int pick_in_sweep(const float* w, float tau, int e0, int lane) {
+  float sum = 0.0f;
+#pragma unroll
+  for (int q = 0; q < CH; ++q) sum = __fadd_rn(sum, w[q]);
+  float rem;
+  const int l = pick_lane(sum, 32, tau, lane, rem);
+  if (l < 0) return -1;
+  int tok = -1;
+  if (lane == l) {
+    float run = 0.0f;
+    int pick = -1, lastq = -1;
+#pragma unroll
+    for (int q = 0; q < CH; ++q) {
+      if (w[q] > 0.0f) {
+        run = __fadd_rn(run, w[q]);
+        if (pick < 0 && run > rem) pick = q;
+        lastq = q;
+      }
+    }
+    tok = e0 + (pick < 0 ? lastq : pick);
   }
   return __shfl_sync(0xffffffffu, tok, l);
 }
@@ -1149,7 +1307,8 @@ __device__ __forceinline__ void p_masses(const uint2* rec, int NC, float Mp, flo
 // its outputs.  Greedy: the argmax of target rows t <= n against the
 // drafts.  Sampled: the left-to-right test u_t q(x_t) < p(x_t) in log2 form;
 // every draft accepted draws the bonus token from p_n here (the chunk from
-// row n's records, the token from one re-read chunk); a rejection at j
+// row n's records, the sweep from its sweep sums, the token from one re-read
+// 512-byte sweep); a rejection at j
 // stores the residual draw's parameters and lists the request for the
 // residual kernel, which writes out_tokens[b, j].  Slot 0 of the warp's
 // ring is its scratch.
@@ -1251,18 +1410,34 @@ __device__ void decide_request(const Params& P, Agent& ag, int b) {
     write_outputs(P, b, j, -1, x_lane, lane);   // the residual kernel writes the token
     return;
   }
-  // every draft accepted: the bonus token from p_n with uniforms[b, n]
+  // every draft accepted: the bonus token from p_n with uniforms[b, n]: the
+  // chunk from row n's records, the 512-byte sweep from that chunk's sweep
+  // sums (kept by the stats kernel), the element from the sweep read again
+  constexpr int CH = Elt<DT>::kPerVec;
   const float u = __shfl_sync(0xffffffffu, u_lane, n);
+  const uint2* rec_n = P.part + (static_cast<size_t>(b) * R + n) * NC;
   float* mass = reinterpret_cast<float*>(ag.slot(0));
-  p_masses(P.part + (static_cast<size_t>(b) * R + n) * NC, NC, Mp, sT, mass, lane);
+  p_masses(rec_n, NC, Mp, sT, mass, lane);
   float W, rem;
   const int chunk = pick_chunk(mass, NC, u, lane, W, rem);
   int tok = -1;
   if (chunk >= 0) {
-    Chunk kp, kq;
-    if (fetch<DT>(P, ag, 0, target_row<DT>(P, b, n), 0, chunk, kChunkBytes, false, kp, kq))
-      tok = draw_in_slot<DT>(ag.slot(0), kp, kq, false, make_float4(Mp, 0.0f, sT, 0.0f), rem,
-                             kChunkBytes / 512, lane);
+    const float f = scaled_exp(__uint_as_float(__ldcg(rec_n + chunk).x), Mp, sT);
+    const float sw = lane < kChunkSweeps
+        ? __fmul_rn(__ldcg(P.bsw + (static_cast<size_t>(b) * NC + chunk) * kChunkSweeps + lane), f)
+        : 0.0f;
+    float rem2 = 0.0f;
+    const int sweep = pick_lane(sw, kChunkSweeps, rem, lane, rem2);
+    if (sweep >= 0) {
+      const Chunk kp = chunk_of<DT>(target_row<DT>(P, b, n), V, chunk, kChunkBytes);
+      const int jv = sweep * 32 + lane;
+      float v[CH], w[CH];
+      global_vec<DT>(kp, P.t_lo, P.t_hi, jv, v);
+      const float4 prm = make_float4(Mp, 0.0f, sT, 0.0f);
+#pragma unroll
+      for (int q = 0; q < CH; ++q) w[q] = weight(v[q], 0.0f, false, prm);
+      tok = pick_in_sweep<CH>(w, rem2, -kp.off0 / Elt<DT>::kBytes + jv * CH, lane);
+    }
   }
   if (rs && lane == 0) {
     rs[n * 8 + 6] = __fdiv_rn(W, Sp);
@@ -1277,8 +1452,9 @@ __device__ void decide_request(const Params& P, Agent& ag, int b) {
 }
 
 // Whole warp: the residual draw of listed request b (entry e, rejected at
-// row j) once all its pieces are summed: the piece from their sums, the
-// token from one re-read piece pair, with uniforms_resample[b].  A residual
+// row j) once all its pieces are summed, with uniforms_resample[b]: the
+// piece from their sums, the sweep from the piece's sweep sums, the token
+// from the sweep of both rows read again.  A residual
 // of exactly zero mass falls back to drawing from p_j with the same uniform
 // (its chunk masses from row j's records).  Slot s is the scratch.
 template <int DT>
@@ -1309,26 +1485,53 @@ __device__ void residual_search(const Params& P, Agent& ag, int s, int e, int b,
     }
   }
   __syncwarp();
+  constexpr int CH = Elt<DT>::kPerVec;
   const float ur = __ldg(P.uniforms_resample + b);
   float W = 0.0f, rem = 0.0f;
   int chunk = staged ? pick_chunk(mass, NCd, ur, lane, W, rem) : -1;
   const uintptr_t rp = target_row<DT>(P, b, j);
+  uint32_t* srec = P.dsw + static_cast<size_t>(e) * NCd * kDrawSweeps;
   int tok = -1;
-  Chunk kp, kq;
   if (!staged) {
     // a wait gave up: flagged below
   } else if (W > 0.0f) {
-    if (chunk >= 0 &&
-        fetch<DT>(P, ag, s, rp, draft_row<DT>(P, b, j), chunk, kDrawBytes, true, kp, kq))
-      tok = draw_in_slot<DT>(ag.slot(s), kp, kq, true, prm, rem, kDrawSweeps, lane);
+    if (chunk >= 0) {
+      // the piece's sweep sums (stored before its sum, behind a fence)
+      const uint32_t wsw = lane < kDrawSweeps ? ld_word(srec + chunk * kDrawSweeps + lane) : kReady;
+      if (!__all_sync(0xffffffffu, (wsw & kReady) != 0u)) {
+        staged = false;
+      } else {
+        float rem2 = 0.0f;
+        const int sweep = pick_lane(lane < kDrawSweeps ? ready_value(wsw) : 0.0f, kDrawSweeps,
+                                    rem, lane, rem2);
+        if (sweep >= 0) {
+          const Chunk kp = chunk_of<DT>(rp, V, chunk, kDrawBytes);
+          const int jv = sweep * 32 + lane;
+          const int e0 = -kp.off0 / Elt<DT>::kBytes + jv * CH;
+          float vp[CH], vq[CH], w[CH];
+          global_vec<DT>(kp, P.t_lo, P.t_hi, jv, vp);
+          global_vec_at<DT>(draft_row<DT>(P, b, j), P.d_lo, P.d_hi, e0, kp.e_lo, kp.e_hi, vq);
+#pragma unroll
+          for (int q = 0; q < CH; ++q) w[q] = weight(vp[q], vq[q], true, prm);
+          tok = pick_in_sweep<CH>(w, rem2, e0, lane);
+        }
+      }
+    }
   } else {
+    // a residual of exactly zero mass: draw from p_j, its chunk masses from
+    // row j's records, the token from one re-read chunk
     p_masses(P.part + (static_cast<size_t>(b) * P.R + j) * NC, NC, prm.x, prm.z, mass, lane);
     float Wp;
     chunk = pick_chunk(mass, NC, ur, lane, Wp, rem);
+    Chunk kp, kq;
     if (chunk >= 0 && fetch<DT>(P, ag, s, rp, 0, chunk, kChunkBytes, false, kp, kq))
       tok = draw_in_slot<DT>(ag.slot(s), kp, kq, false, make_float4(prm.x, 0.0f, prm.z, 0.0f),
                              rem, kChunkBytes / 512, lane);
   }
+  // every sum of this entry is visible (each sweep sum before its piece's
+  // sum, all of those seen): clear them for the next call
+  __syncwarp();
+  for (int i = lane; i < NCd * kDrawSweeps; i += 32) srec[i] = 0u;
   if (P.row_stats && lane == 0) {
     float* rs = P.row_stats + (static_cast<size_t>(b) * (K + 1) + j) * 8;
     rs[6] = __fdiv_rn(W, __ldcg(&P.req[b].Sp_j));
@@ -1356,7 +1559,8 @@ __device__ __forceinline__ void wait_previous() { asm volatile("griddepcontrol.w
 // ---------------------------------------------------------------- stats kernel
 
 // Whole warp: reduces the chunk in slot s to its record; the chunk holding
-// the row's drafted token also records that token's logit.
+// the row's drafted token also records that token's logit, and a sampled
+// request's row n also keeps its sweep sums.
 template <int DT>
 __device__ void consume_stats(const Params& P, Agent& ag, int s, const Item& it) {
   const int lane = ag.lane;
@@ -1365,8 +1569,13 @@ __device__ void consume_stats(const Params& P, Agent& ag, int s, const Item& it)
   const Chunk k = chunk_of<DT>(record_row_addr<DT>(P, it.b, it.row), P.V, it.c, kChunkBytes);
   fix_edges<DT>(k, is_draft ? P.d_lo : P.t_lo, is_draft ? P.d_hi : P.t_hi, slot, lane);
   float2 r;
-  if (it.sT > 0.0f) r = chunk_softmax<DT>(slot, k, it.sT, lane);
-  else r = chunk_argmax<DT>(slot, k, lane);
+  if (it.bonus)
+    r = chunk_softmax_sweeps<DT>(slot, k, it.sT, lane,
+                                 P.bsw + (static_cast<size_t>(it.b) * P.NC + it.c) * kChunkSweeps);
+  else if (it.sT > 0.0f)
+    r = chunk_softmax<DT>(slot, k, it.sT, lane);
+  else
+    r = chunk_argmax<DT>(slot, k, lane);
   if (lane == 0) {
     P.part[(static_cast<size_t>(it.b) * P.R + it.row) * P.NC + it.c] =
         make_uint2(__float_as_uint(r.x), __float_as_uint(r.y));
@@ -1376,113 +1585,55 @@ __device__ void consume_stats(const Params& P, Agent& ag, int s, const Item& it)
   }
 }
 
-// Whole warp, holding the queue's lock: claims the next block of tickets
-// (about half of what is left per CTA, at most kBlockMax, at least one) and
-// publishes their decoded items.  With `force` false it does nothing while
-// enough items are ready.
-__device__ void refill(const Params& P, const Plan& pl, Fifo& f, int lane, bool force) {
-  int base = 0, k = 0, tail = 0, go = 0;
-  if (lane == 0) {
-    tail = *reinterpret_cast<volatile int*>(&f.tail);
-    const int head = *reinterpret_cast<volatile int*>(&f.head);
-    go = !*reinterpret_cast<volatile int*>(&f.closed) && (force || tail - head < kFifoLow);
-    if (go) {
-      const int rem = pl.total - f.last;
-      k = min(kBlockMax, max(1, rem / (2 * static_cast<int>(gridDim.x))));
-      base = static_cast<int>(atomicAdd(reinterpret_cast<unsigned int*>(P.header + kHTicket),
-                                        static_cast<unsigned int>(k)));
-      f.last = base;
-    }
+// A warp's tickets, decoded 32 at a time (one per lane): the warp's i-th
+// ticket is first + i * stride.
+struct TicketRun {
+  int first, stride, total;
+  int base;     // index of the ticket lane 0 holds
+  uint4 mine;   // this lane's decoded ticket (base + lane)
+};
+
+// Whole warp: the i-th ticket's item (i increasing); false past the last.
+__device__ __forceinline__ bool run_item(const Params& P, const Plan& pl, TicketRun& tr, int i,
+                                         int lane, Item& it) {
+  if (tr.first + i * tr.stride >= tr.total) return false;
+  if (i >= tr.base + 32) {
+    tr.base = i;
+    const int t = tr.first + (i + lane) * tr.stride;
+    if (t < tr.total) tr.mine = decode_ticket(P, pl, t);
   }
-  if (!__shfl_sync(0xffffffffu, go, 0)) return;
-  base = __shfl_sync(0xffffffffu, base, 0);
-  k = __shfl_sync(0xffffffffu, k, 0);
-  tail = __shfl_sync(0xffffffffu, tail, 0);
-  const int n = base >= pl.total ? 0 : min(k, pl.total - base);
-  if (lane < n) f.e[(tail + lane) % kFifo] = decode_ticket(P, pl, base + lane);
-  __syncwarp();
-  if (lane == 0) {
-    __threadfence_block();
-    *reinterpret_cast<volatile int*>(&f.tail) = tail + n;
-    if (base + k >= pl.total) {
-      __threadfence_block();
-      *reinterpret_cast<volatile int*>(&f.closed) = 1;
-    }
-  }
-  __syncwarp();
+  const int l = i - tr.base;
+  uint4 e;
+  e.x = __shfl_sync(0xffffffffu, tr.mine.x, l);
+  e.y = __shfl_sync(0xffffffffu, tr.mine.y, l);
+  e.z = __shfl_sync(0xffffffffu, tr.mine.z, l);
+  e.w = __shfl_sync(0xffffffffu, tr.mine.w, l);
+  it = unpack_item(e);
+  return true;
 }
 
-// Whole warp: tries the queue's lock and refills.
-__device__ __forceinline__ bool try_refill(const Params& P, const Plan& pl, Fifo& f, int lane,
-                                           bool force) {
-  int got = 0;
-  if (lane == 0) got = atomicCAS(&f.lock, 0, 1) == 0;
-  got = __shfl_sync(0xffffffffu, got, 0);
-  if (got) {
-    refill(P, pl, f, lane, force);
-    if (lane == 0) {
-      __threadfence_block();
-      atomicExch(&f.lock, 0);
-    }
-  }
-  return got != 0;
-}
-
-// Whole warp: the next item of the CTA, in ticket order; false when no
-// ticket is left.
-__device__ bool pop_item(const Params& P, const Plan& pl, Fifo& f, int lane, Item& it) {
-  int idx = 0;
-  if (lane == 0) idx = atomicAdd(&f.head, 1);
-  idx = __shfl_sync(0xffffffffu, idx, 0);
-  const long long t0 = clock64();
-  for (;;) {
-    int closed = 0, tail = 0;
-    if (lane == 0) {
-      closed = *reinterpret_cast<volatile int*>(&f.closed);
-      __threadfence_block();
-      tail = *reinterpret_cast<volatile int*>(&f.tail);
-    }
-    closed = __shfl_sync(0xffffffffu, closed, 0);
-    tail = __shfl_sync(0xffffffffu, tail, 0);
-    if (idx < tail) {
-      it = unpack_item(f.e[idx % kFifo]);
-      if (!closed && tail - idx <= kFifoLow) try_refill(P, pl, f, lane, false);
-      return true;
-    }
-    if (closed) return false;
-    if (!try_refill(P, pl, f, lane, true)) __nanosleep(32);
-    if (clock64() - t0 > kWaitLimitCycles) {
-      if (lane == 0) atomicOr(P.header + kHStatus, SPECV_DEV_TIMEOUT);
-      return false;
-    }
-  }
-}
-
-// Whole warp: one agent of the stats kernel.  It keeps one item ahead of
-// its ring and issues it as soon as a slot frees.
+// Whole warp: one agent of the stats kernel.  Warp g of the grid's G
+// streams tickets g, g + G, g + 2 G, ... through its ring, refilling a slot
+// as soon as its chunk is reduced.
 template <int DT>
-__device__ void stats_agent(const Params& P, const Plan& pl, Agent& ag, Fifo& fifo) {
+__device__ void stats_agent(const Params& P, const Plan& pl, Agent& ag, int g, int G) {
   const int lane = ag.lane;
+  TicketRun tr;
+  tr.first = g;
+  tr.stride = G;
+  tr.total = pl.total;
+  tr.base = -64;
+  tr.mine = make_uint4(0u, 0u, 0u, 0u);
   int issued = 0, consumed = 0;
-  bool more = true, have = false;
-  Item pend;
   for (;;) {
     while (issued - consumed < kSlots) {
-      if (!have) {
-        if (!more || !pop_item(P, pl, fifo, lane, pend)) {
-          more = false;
-          break;
-        }
-        have = true;
-      }
+      Item it;
+      if (!run_item(P, pl, tr, issued, lane, it)) break;
       __syncwarp();
-      if (lane == 0) issue<DT>(P, ag, issued % kSlots, pend);
+      if (lane == 0) issue<DT>(P, ag, issued % kSlots, it);
       ++issued;
-      have = false;
     }
     if (issued == consumed) break;   // no tickets left and nothing in flight
-    if (more && !have) have = pop_item(P, pl, fifo, lane, pend);   // decode ahead
-    if (!have) more = false;
     const int s = consumed % kSlots;
     if (!wait_slot(P, ag, s)) return;
     consume_stats<DT>(P, ag, s, ag.A->item[s]);
@@ -1501,7 +1652,6 @@ __global__ void __launch_bounds__(kThreads, 1) stats_kernel(const Params P) {
     mbar_init(&S.ag[tid / kSlots].bar[tid % kSlots], 1);
     mbar_init_fence();
   }
-  if (tid == 0) S.fifo.head = S.fifo.tail = S.fifo.lock = S.fifo.closed = S.fifo.last = 0;
   build_plan(P, S.plan, S.red);   // ends with a CTA barrier
   allow_dependents();
 
@@ -1510,18 +1660,9 @@ __global__ void __launch_bounds__(kThreads, 1) stats_kernel(const Params P) {
   ag.ring = dyn + static_cast<size_t>(warp) * kSlots * kSlotBytes;
   ag.ph = 0;
   ag.lane = tid & 31;
-  stats_agent<DT>(P, S.plan, ag, S.fifo);
+  stats_agent<DT>(P, S.plan, ag, static_cast<int>(blockIdx.x) * kAgents + warp,
+                  static_cast<int>(gridDim.x) * kAgents);
 
-  __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    const int prev = atomicAdd(P.header + kHExit, 1);
-    if (prev == static_cast<int>(gridDim.x) - 1) {
-      // last CTA: every ticket is taken; reset for the next call
-      P.header[kHExit] = 0;
-      P.header[kHTicket] = 0;
-    }
-  }
 }
 
 // ---------------------------------------------------------------- decide kernel
@@ -1559,10 +1700,17 @@ __device__ void consume_residual(const Params& P, Agent& ag, int s, const Item& 
   fix_edges<DT>(kp, P.t_lo, P.t_hi, slot, lane);
   const Chunk kq = draft_part<DT>(draft_row<DT>(P, it.b, it.row), kp);
   fix_edges<DT>(kq, P.d_lo, P.d_hi, slot + kDraftOff, lane);
-  const float t = chunk_draw<DT>(slot, kp, kq, true, it.prm, lane);
+  float mine;
+  const float t = piece_sweeps<DT>(slot, kp, kq, it.prm, lane, mine);
   const int e = it.n;   // the request's entry in the list
+  // sweep sums first, then (after a fence) the piece's sum and its count:
+  // whoever sees the sum sees the sweep sums
+  if (lane < kDrawSweeps)
+    st_word(P.dsw + (static_cast<size_t>(e) * P.NCd + it.c) * kDrawSweeps + lane, ready_bits(mine));
+  __syncwarp();
   int old = 0;
   if (lane == 0) {
+    __threadfence();
     st_word(P.dmass + static_cast<size_t>(e) * P.NCd + it.c, ready_bits(t));
     old = atomicAdd(&P.req[it.b].cnt, 1);
   }
@@ -1573,7 +1721,7 @@ __device__ void consume_residual(const Params& P, Agent& ag, int s, const Item& 
   residual_search<DT>(P, ag, s, e, it.b, it.row, it.prm);
 }
 
-// Whole warp: residual item i (entry i / NCd, piece i mod NCd).
+// One lane: residual item i (entry i / NCd, piece i mod NCd).
 __device__ __forceinline__ Item residual_item(const Params& P, int i) {
   Item it;
   const int e = i / P.NCd;
@@ -1585,7 +1733,34 @@ __device__ __forceinline__ Item residual_item(const Params& P, int i) {
   it.prm = __ldcg(&P.req[it.b].prm);
   it.sT = 0.0f;
   it.x = -1;
-  it.pad = 0;
+  it.bonus = 0;
+  return it;
+}
+
+__device__ __forceinline__ Item residual_pick_init() {
+  Item it;
+  it.kind = kItemR;
+  it.b = it.row = it.c = it.n = it.x = it.bonus = 0;
+  it.sT = 0.0f;
+  it.prm = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  return it;
+}
+
+// Whole warp: the warp's k-th residual item (lane k mod 32 decoded it).
+__device__ __forceinline__ Item residual_pick(const Item& mine, int l) {
+  Item it;
+  it.kind = kItemR;
+  it.c = __shfl_sync(0xffffffffu, mine.c, l);
+  it.n = __shfl_sync(0xffffffffu, mine.n, l);
+  it.b = __shfl_sync(0xffffffffu, mine.b, l);
+  it.row = __shfl_sync(0xffffffffu, mine.row, l);
+  it.prm.x = __shfl_sync(0xffffffffu, mine.prm.x, l);
+  it.prm.y = __shfl_sync(0xffffffffu, mine.prm.y, l);
+  it.prm.z = __shfl_sync(0xffffffffu, mine.prm.z, l);
+  it.prm.w = __shfl_sync(0xffffffffu, mine.prm.w, l);
+  it.sT = 0.0f;
+  it.x = -1;
+  it.bonus = 0;
   return it;
 }
 
@@ -1608,13 +1783,20 @@ __global__ void __launch_bounds__(kThreads, 1) residual_kernel(const Params P) {
   const int count = __ldcg(P.header + kHResid);
   const int total = count * P.NCd;
   const int G = static_cast<int>(gridDim.x) * kAgents;
-  int next = static_cast<int>(blockIdx.x) * kAgents + warp;
+  const int first = static_cast<int>(blockIdx.x) * kAgents + warp;
+  const int mine_n = first < total ? (total - first + G - 1) / G : 0;   // this warp's items
+  Item mine = residual_pick_init();
+  int base = -64;
   int issued = 0, consumed = 0;
   bool ok = true;
   for (;;) {
-    while (issued - consumed < kSlots && next < total) {
-      const Item it = residual_item(P, next);
-      next += G;
+    while (issued - consumed < kSlots && issued < mine_n) {
+      if (issued >= base + 32) {   // decode the next 32 of this warp's items, one per lane
+        base = issued;
+        const int i = first + (base + lane) * G;
+        if (i < total) mine = residual_item(P, i);
+      }
+      const Item it = residual_pick(mine, issued - base);
       __syncwarp();
       if (lane == 0) issue<DT>(P, ag, issued % kSlots, it);
       ++issued;
@@ -1646,7 +1828,7 @@ __global__ void __launch_bounds__(kThreads, 1) residual_kernel(const Params P) {
 int elt_bytes(specv_dtype dt) { return dt == SPECV_BF16 ? 2 : 4; }
 
 struct Layout {
-  size_t header, req, part, zx, rlist, dmass, total;
+  size_t header, req, part, zx, rlist, dmass, dsw, bsw, total;
 };
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
@@ -1672,7 +1854,9 @@ Layout ws_layout(int B, int K, int V, specv_dtype dt) {
   L.zx = align256(L.part + sizeof(uint2) * Bl * R * NC);
   L.rlist = align256(L.zx + sizeof(float) * Bl * R);
   L.dmass = align256(L.rlist + sizeof(int32_t) * Bl);
-  L.total = align256(L.dmass + sizeof(uint32_t) * Bl * NCd);
+  L.dsw = align256(L.dmass + sizeof(uint32_t) * Bl * NCd);
+  L.bsw = align256(L.dsw + sizeof(uint32_t) * Bl * NCd * kDrawSweeps);
+  L.total = align256(L.bsw + sizeof(float) * Bl * NC * kChunkSweeps);
   return L;
 }
 
@@ -1820,6 +2004,8 @@ specv_status launch(const void* target, const void* draft, specv_dtype dtype,
     P.zx = reinterpret_cast<float*>(ws + L.zx);
     P.rlist = reinterpret_cast<int32_t*>(ws + L.rlist);
     P.dmass = reinterpret_cast<uint32_t*>(ws + L.dmass);
+    P.dsw = reinterpret_cast<uint32_t*>(ws + L.dsw);
+    P.bsw = reinterpret_cast<float*>(ws + L.bsw);
     P.row_stats = row_stats ? row_stats + static_cast<size_t>(b0) * (K + 1) * 8 : nullptr;
     const cudaError_t e = dtype == SPECV_BF16 ? launch_sequence<SPECV_BF16>(P, grid, stream)
                                               : launch_sequence<SPECV_F32>(P, grid, stream);
