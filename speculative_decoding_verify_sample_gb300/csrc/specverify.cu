@@ -71,14 +71,13 @@ static_assert(kMaxChunks < 512, "a stats chunk index fits 9 bits");
 static_assert(kPlanMax <= 1024 && 2 * SPECV_MAX_DRAFT + 1 < 64, "a request fits 10 bits, a row 6");
 
 // workspace header words (int32 index), one 128-byte line each
-constexpr int kHStatus = 0, kHResid = 96, kHExit3 = 128;
+constexpr int kHStatus = 0, kHEpoch = 64, kHResid = 96, kHExit3 = 128;
 constexpr int kHeaderBytes = 1024;
 static_assert((kHExit3 + 1) * 4 <= kHeaderBytes, "header words fit the header");
 
-// Residual mass records are written with one store each, and bit 31 is set
-// in every written record, so a zero record is "not written yet".  The
-// warp that reads them returns them to zero.
-constexpr uint32_t kReady = 0x80000000u;
+// Residual sum records are (value, call tag) pairs written with one 8-byte
+// store, so a record whose tag is not this call's is "not written yet"; no
+// record needs clearing between calls.
 
 constexpr int kItemA = 1, kItemR = 3;
 
@@ -118,8 +117,8 @@ struct Params {
   uint2* part;      // [B][R][NC] chunk records: (max, sum) or (max, index)
   float* zx;        // [B][R] the drafted token's logit in rows t < n
   int32_t* rlist;   // [B] requests waiting for a residual draw (count: header[kHResid])
-  uint32_t* dmass;  // [B][NCd] residual mass records: mass | ready
-  uint32_t* dsw;    // [B][NCd][kDrawSweeps] residual sweep-sum records: sum | ready
+  uint2* dmass;     // [B][NCd] residual sums of the pieces: (sum, tag)
+  uint2* dsw;       // [B][NCd][kDrawSweeps] residual sums of their sweeps: (sum, tag)
   float* bsw;       // [B][NC][kChunkBytes / 512] sweep sums of each sampled request's row n
   float* row_stats; // [B][K+1][8] or null
 };
@@ -1192,100 +1191,15 @@ __device__ bool fetch(const Params& P, Agent& ag, int s, uintptr_t rp, uintptr_t
 
 // ---------------------------------------------------------------- records
 
-__device__ __forceinline__ void st_word(uint32_t* p, uint32_t v) {
-  asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+__device__ __forceinline__ void st_tagged(uint2* p, float v, uint32_t tag) {
+  const unsigned long long w = (static_cast<unsigned long long>(tag) << 32) | __float_as_uint(v);
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
 }
 
-__device__ __forceinline__ uint32_t ld_word(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-// A nonnegative (or NaN) float with the ready bit, and back.
-__device__ __forceinline__ uint32_t ready_bits(float x) {
-  return (x != x ? 0x7FC00000u : __float_as_uint(x)) | kReady;
-}
-__device__ __forceinline__ float ready_value(uint32_t u) { return __uint_as_float(u & ~kReady); }
-
-// Whole warp: stages n records (written by an earlier kernel) into shared
-// memory, eight loads in flight per lane.
-__device__ __forceinline__ void stage_records(uint2* dst, const uint2* src, int n, int lane) {
-  for (int base = 0; base < n; base += 8 * 32) {
-    uint2 v[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int i = base + k * 32 + lane;
-      if (i < n) v[k] = __ldcg(src + i);
-    }
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int i = base + k * 32 + lane;
-      if (i < n) dst[i] = v[k];
-    }
-  }
-}
-
-// (max, sum) of one row from its NC staged records: the maximum first, then
-// the chunk sums rescaled to it, in chunk order.
-__device__ __forceinline__ void combine_row(const uint2* p, int NC, float sT, float& M, float& S) {
-  M = -INFINITY;
-  for (int c = 0; c < NC; ++c) M = fmaxf(M, __uint_as_float(p[c].x));
-  S = 0.0f;
-  if (M == -INFINITY) return;
-  for (int c = 0; c < NC; ++c) {
-    const float m = __uint_as_float(p[c].x);
-    if (m > -INFINITY) S = __fadd_rn(S, __fmul_rn(__uint_as_float(p[c].y), scaled_exp(m, M, sT)));
-  }
-}
-
-// Argmax of one row from its staged records: chunks are in index order, so
-// the first chunk holding the maximum has the lowest index.
-__device__ __forceinline__ void argmax_row(const uint2* p, int NC, float& v, int& i) {
-  v = __uint_as_float(p[0].x);
-  i = static_cast<int>(p[0].y);
-  for (int c = 1; c < NC; ++c) {
-    const float m = __uint_as_float(p[c].x);
-    if (m > v) {
-      v = m;
-      i = static_cast<int>(p[c].y);
-    }
-  }
-}
-
-// Whole warp: combines request b's records of target rows [0, nt) and
-// draft rows [0, nd), staged pass by pass through scratch (kSlotBytes):
-// lane t gets target row t (Mp, Sp, or the argmax) and draft row t (Mq, Sq).
-__device__ void combine_request(const Params& P, unsigned char* scratch, int b, int nt, int nd,
-                                bool greedy, float sT, int lane, float& Mp, float& Sp, float& Mq,
-                                float& Sq, int& arg) {
-  const int NC = P.NC, K = P.K;
-  uint2* buf = reinterpret_cast<uint2*>(scratch);
-  const int cap = max(1, kSlotBytes / (8 * NC));   // rows per pass
-  const uint2* rec = P.part + static_cast<size_t>(b) * P.R * NC;
-  Mp = Mq = -INFINITY;
-  Sp = Sq = 0.0f;
-  arg = INT_MAX;
-  for (int v0 = 0; v0 < nt + nd; v0 += cap) {
-    const int v1 = min(nt + nd, v0 + cap);
-    // virtual rows [v0, v1): target rows first, then draft rows
-    const int ta = v0, tb = min(v1, nt);
-    const int da = max(v0, nt) - nt, db = v1 - nt;
-    const int ntr = max(0, tb - ta);
-    __syncwarp();
-    if (ntr > 0) stage_records(buf, rec + static_cast<size_t>(ta) * NC, ntr * NC, lane);
-    if (db > da)
-      stage_records(buf + ntr * NC, rec + static_cast<size_t>(K + 1 + da) * NC, (db - da) * NC,
-                    lane);
-    __syncwarp();
-    if (lane >= ta && lane < tb) {
-      const uint2* p = buf + (lane - ta) * NC;
-      if (greedy) argmax_row(p, NC, Mp, arg);
-      else combine_row(p, NC, sT, Mp, Sp);
-    }
-    if (lane >= da && lane < db) combine_row(buf + (ntr + lane - da) * NC, NC, sT, Mq, Sq);
-  }
-  __syncwarp();
+__device__ __forceinline__ uint2 ld_tagged(const uint2* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return make_uint2(static_cast<uint32_t>(v), static_cast<uint32_t>(v >> 32));
 }
 
 // Whole warp: chunk masses of a draw from p (one row's records rescaled to
@@ -1303,42 +1217,113 @@ __device__ __forceinline__ void p_masses(const uint2* rec, int NC, float Mp, flo
 
 // ---------------------------------------------------------------- decisions
 
-// Whole warp: decides request b from the stats kernel's records and writes
-// its outputs.  Greedy: the argmax of target rows t <= n against the
-// drafts.  Sampled: the left-to-right test u_t q(x_t) < p(x_t) in log2 form;
-// every draft accepted draws the bonus token from p_n here (the chunk from
-// row n's records, the sweep from its sweep sums, the token from one re-read
-// 512-byte sweep); a rejection at j
-// stores the residual draw's parameters and lists the request for the
-// residual kernel, which writes out_tokens[b, j].  Slot 0 of the warp's
-// ring is its scratch.
+constexpr int kMaxRows = 2 * SPECV_MAX_DRAFT + 1;
+
+// The decision kernel's shared memory: one request's combined rows.
+struct DecideSmem {
+  float M[kMaxRows], S[kMaxRows];   // row r: maximum (raw logit) and sum, or the argmax value
+  int arg[kMaxRows];                // greedy: the argmax
+  float mass[kMaxChunks];           // chunk masses of a bonus draw
+};
+
+// Whole warp: combines one row from its NC records, a lane per chunk
+// (lane c takes chunks c, c + 32, ...): (max, sum of exp((z - max)/T)), or
+// at T = 0 (max, lowest index holding it).
+__device__ __forceinline__ void combine_row_warp(const uint2* rec, int NC, bool greedy, float sT,
+                                                 int lane, float& M, float& S, int& arg) {
+  float m = -INFINITY;
+  int idx = INT_MAX;
+  for (int c = lane; c < NC; c += 32) {
+    const uint2 r = __ldcg(rec + c);
+    const float v = __uint_as_float(r.x);
+    if (v > m) {   // chunks in increasing order: the first chunk holding a lane's maximum
+      m = v;
+      idx = static_cast<int>(r.y);
+    }
+  }
+  M = warp_max(m);
+  S = 0.0f;
+  arg = INT_MAX;
+  if (greedy) {
+    arg = warp_min_int(m == M ? idx : INT_MAX);
+    return;
+  }
+  float s = 0.0f;
+  if (M > -INFINITY) {
+    for (int c = lane; c < NC; c += 32) {
+      const uint2 r = __ldcg(rec + c);
+      const float v = __uint_as_float(r.x);
+      if (v > -INFINITY) s = __fadd_rn(s, __fmul_rn(__uint_as_float(r.y), scaled_exp(v, M, sT)));
+    }
+  }
+  S = warp_sum(s);
+}
+
+// Whole CTA: decides request b from the stats kernel's records and writes
+// its outputs.  The CTA's warps combine the request's rows (target rows
+// t <= n, draft rows t < n when sampled); warp 0 then takes the decision.
+// Greedy: the argmax of target rows t <= n against the drafts.  Sampled:
+// the left-to-right test u_t q(x_t) < p(x_t) in log2 form; every draft
+// accepted draws the bonus token from p_n here (the chunk from row n's
+// records, the sweep from its sweep sums, the token from one re-read
+// 512-byte sweep); a rejection at j stores the residual draw's parameters
+// and lists the request for the residual kernel, which writes
+// out_tokens[b, j].
 template <int DT>
-__device__ void decide_request(const Params& P, Agent& ag, int b) {
-  const int lane = ag.lane, K = P.K, V = P.V, R = P.R, NC = P.NC;
+__device__ void decide_request(const Params& P, DecideSmem& D, int b) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int K = P.K, V = P.V, R = P.R, NC = P.NC;
   const int n = request_len(P, b);
   const float T = __ldg(P.temperature + b);
   int bad = request_bad(P, n, T);
   if (bad) {
-    if (lane == 0) atomicOr(P.header + kHStatus, bad);
-    write_outputs(P, b, -1, -1, -1, lane);
+    if (warp == 0) {
+      if (lane == 0) atomicOr(P.header + kHStatus, bad);
+      write_outputs(P, b, -1, -1, -1, lane);
+    }
     return;
   }
   const bool greedy = !(T > 0.0f);
   const float sT = greedy ? 0.0f : temp_scale(T);
+  const int nt = n + 1, nd = greedy ? 0 : n;
+  // warp 0's inputs first, so their loads overlap the combining
   int x_lane = -1;
-  float u_lane = 0.0f;
-  if (lane < n) x_lane = __ldg(P.draft_tokens + static_cast<size_t>(b) * K + lane);
-  if (lane <= n) u_lane = __ldg(P.uniforms + static_cast<size_t>(b) * (K + 1) + lane);
-  const float ur = __ldg(P.uniforms_resample + b);
-  float zp = 0.0f, zq = 0.0f;
-  if (!greedy && lane < n) {
-    zp = __ldcg(P.zx + static_cast<size_t>(b) * R + lane);
-    zq = __ldcg(P.zx + static_cast<size_t>(b) * R + K + 1 + lane);
+  float u_lane = 0.0f, ur = 0.0f, zp = 0.0f, zq = 0.0f;
+  if (warp == 0) {
+    if (lane < n) x_lane = __ldg(P.draft_tokens + static_cast<size_t>(b) * K + lane);
+    if (lane <= n) u_lane = __ldg(P.uniforms + static_cast<size_t>(b) * (K + 1) + lane);
+    ur = __ldg(P.uniforms_resample + b);
+    if (!greedy && lane < n) {
+      zp = __ldcg(P.zx + static_cast<size_t>(b) * R + lane);
+      zq = __ldcg(P.zx + static_cast<size_t>(b) * R + K + 1 + lane);
+    }
   }
-  float Mp_l, Sp_l, Mq_l, Sq_l;
-  int g;
-  combine_request(P, ag.slot(0), b, n + 1, greedy ? 0 : n, greedy, sT, lane, Mp_l, Sp_l, Mq_l,
-                  Sq_l, g);
+  for (int r = warp; r < nt + nd; r += kDecideWarps) {
+    const int row = r < nt ? r : K + 1 + (r - nt);
+    float M, S;
+    int arg;
+    combine_row_warp(P.part + (static_cast<size_t>(b) * R + row) * NC, NC, greedy, sT, lane, M, S,
+                     arg);
+    if (lane == 0) {
+      D.M[r] = M;
+      D.S[r] = S;
+      D.arg[r] = arg;
+    }
+  }
+  __syncthreads();
+  if (warp != 0) return;
+
+  float Mp_l = -INFINITY, Sp_l = 0.0f, Mq_l = -INFINITY, Sq_l = 0.0f;
+  int g = INT_MAX;
+  if (lane < nt) {
+    Mp_l = D.M[lane];
+    Sp_l = D.S[lane];
+    g = D.arg[lane];
+  }
+  if (lane < nd) {
+    Mq_l = D.M[nt + lane];
+    Sq_l = D.S[nt + lane];
+  }
   if (__any_sync(0xffffffffu, lane < n && (x_lane < 0 || x_lane >= V))) bad |= SPECV_DEV_BAD_TOKEN;
   if (__any_sync(0xffffffffu, lane <= n && !(u_lane >= 0.0f && u_lane < 1.0f)) ||
       !(ur >= 0.0f && ur < 1.0f))
@@ -1410,16 +1395,13 @@ __device__ void decide_request(const Params& P, Agent& ag, int b) {
     write_outputs(P, b, j, -1, x_lane, lane);   // the residual kernel writes the token
     return;
   }
-  // every draft accepted: the bonus token from p_n with uniforms[b, n]: the
-  // chunk from row n's records, the 512-byte sweep from that chunk's sweep
-  // sums (kept by the stats kernel), the element from the sweep read again
+  // every draft accepted: the bonus token from p_n with uniforms[b, n]
   constexpr int CH = Elt<DT>::kPerVec;
   const float u = __shfl_sync(0xffffffffu, u_lane, n);
   const uint2* rec_n = P.part + (static_cast<size_t>(b) * R + n) * NC;
-  float* mass = reinterpret_cast<float*>(ag.slot(0));
-  p_masses(rec_n, NC, Mp, sT, mass, lane);
+  p_masses(rec_n, NC, Mp, sT, D.mass, lane);
   float W, rem;
-  const int chunk = pick_chunk(mass, NC, u, lane, W, rem);
+  const int chunk = pick_chunk(D.mass, NC, u, lane, W, rem);
   int tok = -1;
   if (chunk >= 0) {
     const float f = scaled_exp(__uint_as_float(__ldcg(rec_n + chunk).x), Mp, sT);
@@ -1451,59 +1433,55 @@ __device__ void decide_request(const Params& P, Agent& ag, int b) {
   }
 }
 
+// Whole warp: n tagged records into dst (floats), each read until it
+// carries this call's tag; false if a wait gave up.
+__device__ bool stage_tagged(float* dst, const uint2* src, int n, uint32_t tag, int lane) {
+  const long long t0 = clock64();
+  for (int c0 = 0; c0 < n; c0 += 32) {
+    const int c = c0 + lane;
+    uint2 w = c < n ? ld_tagged(src + c) : make_uint2(0u, tag);
+    while (!__all_sync(0xffffffffu, w.y == tag)) {
+      if (clock64() - t0 > kWaitLimitCycles) return false;
+      __nanosleep(64);
+      if (w.y != tag) w = ld_tagged(src + c);
+    }
+    if (c < n) dst[c] = __uint_as_float(w.x);
+  }
+  __syncwarp();
+  return true;
+}
+
 // Whole warp: the residual draw of listed request b (entry e, rejected at
 // row j) once all its pieces are summed, with uniforms_resample[b]: the
 // piece from their sums, the sweep from the piece's sweep sums, the token
-// from the sweep of both rows read again.  A residual
-// of exactly zero mass falls back to drawing from p_j with the same uniform
-// (its chunk masses from row j's records).  Slot s is the scratch.
+// from the sweep of both rows read again.  A residual of exactly zero mass
+// falls back to drawing from p_j with the same uniform (its chunk masses
+// from row j's records, the token from one re-read chunk).  Slot s is the
+// scratch.
 template <int DT>
 __device__ void residual_search(const Params& P, Agent& ag, int s, int e, int b, int j,
-                                const float4& prm) {
+                                const float4& prm, uint32_t tag) {
+  constexpr int CH = Elt<DT>::kPerVec;
   const int lane = ag.lane, K = P.K, V = P.V, NC = P.NC, NCd = P.NCd;
   float* mass = reinterpret_cast<float*>(ag.slot(s));
-  uint32_t* drec = P.dmass + static_cast<size_t>(e) * NCd;
-  // a count completes once every piece has stored its sum, but a store may
-  // become visible after the count: sums are read until written (bounded)
-  bool staged = true;
-  const long long t0 = clock64();
   __syncwarp();
-  for (int c0 = 0; c0 < NCd; c0 += 32) {
-    const int c = c0 + lane;
-    uint32_t w = c < NCd ? ld_word(drec + c) : kReady;
-    while (!__all_sync(0xffffffffu, (w & kReady) != 0u)) {
-      if (clock64() - t0 > kWaitLimitCycles) {
-        staged = false;
-        break;
-      }
-      __nanosleep(64);
-      if (!(w & kReady)) w = ld_word(drec + c);
-    }
-    if (c < NCd) {
-      mass[c] = ready_value(w);
-      drec[c] = 0u;   // ready for the next call
-    }
-  }
-  __syncwarp();
-  constexpr int CH = Elt<DT>::kPerVec;
+  bool staged = stage_tagged(mass, P.dmass + static_cast<size_t>(e) * NCd, NCd, tag, lane);
   const float ur = __ldg(P.uniforms_resample + b);
   float W = 0.0f, rem = 0.0f;
   int chunk = staged ? pick_chunk(mass, NCd, ur, lane, W, rem) : -1;
   const uintptr_t rp = target_row<DT>(P, b, j);
-  uint32_t* srec = P.dsw + static_cast<size_t>(e) * NCd * kDrawSweeps;
   int tok = -1;
   if (!staged) {
     // a wait gave up: flagged below
   } else if (W > 0.0f) {
     if (chunk >= 0) {
-      // the piece's sweep sums (stored before its sum, behind a fence)
-      const uint32_t wsw = lane < kDrawSweeps ? ld_word(srec + chunk * kDrawSweeps + lane) : kReady;
-      if (!__all_sync(0xffffffffu, (wsw & kReady) != 0u)) {
-        staged = false;
-      } else {
+      float* sws = mass + ((NCd + 3) & ~3);
+      staged = stage_tagged(sws, P.dsw + (static_cast<size_t>(e) * NCd + chunk) * kDrawSweeps,
+                            kDrawSweeps, tag, lane);
+      if (staged) {
         float rem2 = 0.0f;
-        const int sweep = pick_lane(lane < kDrawSweeps ? ready_value(wsw) : 0.0f, kDrawSweeps,
-                                    rem, lane, rem2);
+        const int sweep = pick_lane(lane < kDrawSweeps ? sws[lane] : 0.0f, kDrawSweeps, rem,
+                                    lane, rem2);
         if (sweep >= 0) {
           const Chunk kp = chunk_of<DT>(rp, V, chunk, kDrawBytes);
           const int jv = sweep * 32 + lane;
@@ -1518,8 +1496,6 @@ __device__ void residual_search(const Params& P, Agent& ag, int s, int e, int b,
       }
     }
   } else {
-    // a residual of exactly zero mass: draw from p_j, its chunk masses from
-    // row j's records, the token from one re-read chunk
     p_masses(P.part + (static_cast<size_t>(b) * P.R + j) * NC, NC, prm.x, prm.z, mass, lane);
     float Wp;
     chunk = pick_chunk(mass, NC, ur, lane, Wp, rem);
@@ -1528,10 +1504,6 @@ __device__ void residual_search(const Params& P, Agent& ag, int s, int e, int b,
       tok = draw_in_slot<DT>(ag.slot(s), kp, kq, false, make_float4(prm.x, 0.0f, prm.z, 0.0f),
                              rem, kChunkBytes / 512, lane);
   }
-  // every sum of this entry is visible (each sweep sum before its piece's
-  // sum, all of those seen): clear them for the next call
-  __syncwarp();
-  for (int i = lane; i < NCd * kDrawSweeps; i += 32) srec[i] = 0u;
   if (P.row_stats && lane == 0) {
     float* rs = P.row_stats + (static_cast<size_t>(b) * (K + 1) + j) * 8;
     rs[6] = __fdiv_rn(W, __ldcg(&P.req[b].Sp_j));
@@ -1669,31 +1641,31 @@ __global__ void __launch_bounds__(kThreads, 1) stats_kernel(const Params P) {
 
 template <int DT>
 __global__ void __launch_bounds__(kDecideWarps * 32) decide_kernel(const Params P) {
-  __shared__ AgentSmem A[kDecideWarps];
-  extern __shared__ __align__(128) unsigned char dyn[];
-  const int tid = threadIdx.x, warp = tid >> 5;
-  if ((tid & 31) == 0) {
-    mbar_init(&A[warp].bar[0], 1);
-    mbar_init_fence();
-  }
-  __syncwarp();
+  __shared__ DecideSmem D;
   wait_previous();
   allow_dependents();
-  Agent ag;
-  ag.A = &A[warp];
-  ag.ring = dyn + static_cast<size_t>(warp) * kSlotBytes;
-  ag.ph = 0;
-  ag.lane = tid & 31;
-  for (int b = blockIdx.x * kDecideWarps + warp; b < P.B; b += gridDim.x * kDecideWarps)
-    decide_request<DT>(P, ag, b);
+  for (int b = blockIdx.x; b < P.B; b += gridDim.x) {
+    decide_request<DT>(P, D, b);
+    __syncthreads();
+  }
 }
 
 // ---------------------------------------------------------------- residual kernel
 
-// Whole warp: sums the residual (p - q)+ of the piece pair in slot s and
-// counts it; the warp completing the request's pieces draws its token.
+// A consumed piece whose count is not looked at yet.
+struct Pending {
+  int b, e, j;
+  float4 prm;
+  int old;   // lane 0: the count before this piece's
+  bool valid;
+};
+
+// Whole warp: sums the residual (p - q)+ of the piece pair in slot s, sweep
+// by sweep, stores the sums (tagged with the call) and counts the piece
+// (the count is looked at later).
 template <int DT>
-__device__ void consume_residual(const Params& P, Agent& ag, int s, const Item& it) {
+__device__ void consume_residual(const Params& P, Agent& ag, int s, const Item& it, uint32_t tag,
+                                 Pending& pd) {
   const int lane = ag.lane;
   unsigned char* slot = ag.slot(s);
   const Chunk kp = chunk_of<DT>(target_row<DT>(P, it.b, it.row), P.V, it.c, kDrawBytes);
@@ -1703,22 +1675,29 @@ __device__ void consume_residual(const Params& P, Agent& ag, int s, const Item& 
   float mine;
   const float t = piece_sweeps<DT>(slot, kp, kq, it.prm, lane, mine);
   const int e = it.n;   // the request's entry in the list
-  // sweep sums first, then (after a fence) the piece's sum and its count:
-  // whoever sees the sum sees the sweep sums
   if (lane < kDrawSweeps)
-    st_word(P.dsw + (static_cast<size_t>(e) * P.NCd + it.c) * kDrawSweeps + lane, ready_bits(mine));
-  __syncwarp();
-  int old = 0;
+    st_tagged(P.dsw + (static_cast<size_t>(e) * P.NCd + it.c) * kDrawSweeps + lane, mine, tag);
   if (lane == 0) {
-    __threadfence();
-    st_word(P.dmass + static_cast<size_t>(e) * P.NCd + it.c, ready_bits(t));
-    old = atomicAdd(&P.req[it.b].cnt, 1);
+    st_tagged(P.dmass + static_cast<size_t>(e) * P.NCd + it.c, t, tag);
+    pd.old = atomicAdd(&P.req[it.b].cnt, 1);
   }
-  old = __shfl_sync(0xffffffffu, old, 0);
+  pd.b = it.b;
+  pd.e = e;
+  pd.j = it.row;
+  pd.prm = it.prm;
+  pd.valid = true;
+}
+
+// Whole warp: looks at a consumed piece's count; the warp whose piece
+// completed the request draws its token, with slot s as scratch.
+template <int DT>
+__device__ void settle_residual(const Params& P, Agent& ag, int s, Pending& pd, uint32_t tag) {
+  pd.valid = false;
+  const int old = __shfl_sync(0xffffffffu, pd.old, 0);
   if (old != P.NCd - 1) return;
-  if (lane == 0) P.req[it.b].cnt = 0;   // every piece is in: ready for the next call
+  if (ag.lane == 0) P.req[pd.b].cnt = 0;   // every piece is in: ready for the next call
   __syncwarp();
-  residual_search<DT>(P, ag, s, e, it.b, it.row, it.prm);
+  residual_search<DT>(P, ag, s, pd.e, pd.b, pd.j, pd.prm, tag);
 }
 
 // One lane: residual item i (entry i / NCd, piece i mod NCd).
@@ -1781,6 +1760,7 @@ __global__ void __launch_bounds__(kThreads, 1) residual_kernel(const Params P) {
   ag.ph = 0;
   ag.lane = lane;
   const int count = __ldcg(P.header + kHResid);
+  const uint32_t tag = static_cast<uint32_t>(__ldcg(P.header + kHEpoch)) + 1u;
   const int total = count * P.NCd;
   const int G = static_cast<int>(gridDim.x) * kAgents;
   const int first = static_cast<int>(blockIdx.x) * kAgents + warp;
@@ -1789,6 +1769,9 @@ __global__ void __launch_bounds__(kThreads, 1) residual_kernel(const Params P) {
   int base = -64;
   int issued = 0, consumed = 0;
   bool ok = true;
+  Pending pd;
+  pd.valid = false;
+  pd.old = 0;
   for (;;) {
     while (issued - consumed < kSlots && issued < mine_n) {
       if (issued >= base + 32) {   // decode the next 32 of this warp's items, one per lane
@@ -1801,14 +1784,21 @@ __global__ void __launch_bounds__(kThreads, 1) residual_kernel(const Params P) {
       if (lane == 0) issue<DT>(P, ag, issued % kSlots, it);
       ++issued;
     }
-    if (issued == consumed) break;
+    if (issued == consumed) {
+      if (pd.valid) settle_residual<DT>(P, ag, 0, pd, tag);   // ring empty: slot 0 is free
+      break;
+    }
     const int s = consumed % kSlots;
     if (!wait_slot(P, ag, s)) {
       ok = false;
       break;
     }
-    consume_residual<DT>(P, ag, s, A[warp].item[s]);
+    Pending cur;
+    cur.old = 0;
+    consume_residual<DT>(P, ag, s, A[warp].item[s], tag, cur);
     ++consumed;
+    if (pd.valid) settle_residual<DT>(P, ag, s, pd, tag);   // slot s is consumed, not refilled
+    pd = cur;
   }
   (void)ok;
   __syncthreads();
@@ -1818,6 +1808,7 @@ __global__ void __launch_bounds__(kThreads, 1) residual_kernel(const Params P) {
     if (prev == static_cast<int>(gridDim.x) - 1) {
       P.header[kHExit3] = 0;
       P.header[kHResid] = 0;   // the list is used up: empty for the next call
+      P.header[kHEpoch] = static_cast<int32_t>(tag);   // the next call's records get a new tag
     }
   }
 }
@@ -1854,13 +1845,11 @@ Layout ws_layout(int B, int K, int V, specv_dtype dt) {
   L.zx = align256(L.part + sizeof(uint2) * Bl * R * NC);
   L.rlist = align256(L.zx + sizeof(float) * Bl * R);
   L.dmass = align256(L.rlist + sizeof(int32_t) * Bl);
-  L.dsw = align256(L.dmass + sizeof(uint32_t) * Bl * NCd);
-  L.bsw = align256(L.dsw + sizeof(uint32_t) * Bl * NCd * kDrawSweeps);
+  L.dsw = align256(L.dmass + sizeof(uint2) * Bl * NCd);
+  L.bsw = align256(L.dsw + sizeof(uint2) * Bl * NCd * kDrawSweeps);
   L.total = align256(L.bsw + sizeof(float) * Bl * NC * kChunkSweeps);
   return L;
 }
-
-constexpr int kDecideSmem = kDecideWarps * kSlotBytes;
 
 // Resident CTAs of the stats kernel on the current device (one per SM),
 // with every kernel's shared-memory limit raised once per device.
@@ -1879,9 +1868,6 @@ cudaError_t resident_ctas(int* out) {
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(residual_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                kRingBytes);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(decide_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kDecideSmem);
     if (e != cudaSuccess) return e;
     int per_sm = 0, sms = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stats_kernel<DT>, kThreads,
@@ -1932,8 +1918,7 @@ cudaError_t launch_sequence(const Params& P, int grid, cudaStream_t stream) {
   stats_kernel<DT><<<grid, kThreads, kRingBytes, stream>>>(P);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int dgrid = (P.B + kDecideWarps - 1) / kDecideWarps;
-  e = launch_dependent(decide_kernel<DT>, dgrid, kDecideWarps * 32, kDecideSmem, stream, P);
+  e = launch_dependent(decide_kernel<DT>, P.B, kDecideWarps * 32, 0, stream, P);
   if (e != cudaSuccess) return e;
   return launch_dependent(residual_kernel<DT>, grid, kThreads, kRingBytes, stream, P);
 }
@@ -2003,8 +1988,8 @@ specv_status launch(const void* target, const void* draft, specv_dtype dtype,
     P.part = reinterpret_cast<uint2*>(ws + L.part);
     P.zx = reinterpret_cast<float*>(ws + L.zx);
     P.rlist = reinterpret_cast<int32_t*>(ws + L.rlist);
-    P.dmass = reinterpret_cast<uint32_t*>(ws + L.dmass);
-    P.dsw = reinterpret_cast<uint32_t*>(ws + L.dsw);
+    P.dmass = reinterpret_cast<uint2*>(ws + L.dmass);
+    P.dsw = reinterpret_cast<uint2*>(ws + L.dsw);
     P.bsw = reinterpret_cast<float*>(ws + L.bsw);
     P.row_stats = row_stats ? row_stats + static_cast<size_t>(b0) * (K + 1) * 8 : nullptr;
     const cudaError_t e = dtype == SPECV_BF16 ? launch_sequence<SPECV_BF16>(P, grid, stream)
