@@ -46,6 +46,10 @@ import numpy as np  # noqa: E402
 METRIC = "verify rows/s (B×(K+1) rows of V logits) and achieved HBM GB/s vs GB300 peak"
 KERNEL_SRC = os.path.join(ROOT, "speculative_decoding_verify_sample_gb300", "csrc", "specverify.cu")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "verify_kernel_traffic.json")
+# A call launches three kernels (row statistics, decisions, residual draws)
+# per sequence of at most 1024 requests.
+KERNELS_PER_SEQUENCE = 3
+REQUESTS_PER_SEQUENCE = 1024
 FALLBACK_HBM_GBS = 6800.0
 
 WORKLOAD_TEXT = {
@@ -379,12 +383,14 @@ def run_ours(args, torch, world, rank, local):
             "kernel_plan": sv.launch_plan(B, K, V, inp["dtype"], inp.get("draft") is not None),
             "parallelism": f"{world} independent replica(s), requests sharded per rank"},
         "roofline": {
-            "kernel": "verify_kernel", "bound": "hbm", "achieved": round(achieved, 1),
+            "kernel": "spec_verify_sample (stats_kernel + decide_kernel + residual_kernel, "
+                      "one call)",
+            "bound": "hbm", "achieved": round(achieved, 1),
             "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
             "traffic": recorded_traffic(args.workload),
             "peak_source": f"{peak_src} HBM copy bandwidth",
             "algorithmic_bytes_per_launch": req_bytes},
-        "gpu_launches": K_steps,
+        "gpu_launches": K_steps * KERNELS_PER_SEQUENCE * math.ceil(B / REQUESTS_PER_SEQUENCE),
     }
     if clocks:
         line["clocks"] = clocks.summary()

@@ -8,8 +8,8 @@
 // draft is accepted draw a bonus token from p at the next position; at
 // temperature 0 compare argmax(p) with the draft instead.
 //
-// Design: three kernels on the caller's stream, the second and third
-// launched as programmatic dependents so their launch overlaps the previous
+// Design: four kernels on the caller's stream, each after the first
+// launched as a programmatic dependent so its launch overlaps the previous
 // kernel's tail.
 //
 //  1. stats_kernel streams every row a request needs (target rows t <= n,
@@ -26,9 +26,10 @@
 //     records, the token from one re-read chunk.  A rejected sampled
 //     request is appended to a list for the residual draw.
 //  3. residual_kernel reads the rejected rows again (target and draft, in
-//     3 KB pieces), sums (p - q)+ per piece, and the warp that completes a
-//     request's pieces draws its token: the piece from the sums, the token
-//     from one re-read piece pair.
+//     3 KB pieces) and sums (p - q)+ per piece and per 512-byte sweep.
+//  4. search_kernel, one warp per listed request, draws its token: the
+//     piece from the piece sums, the sweep from that piece's sweep sums,
+//     the token from the sweep of both rows read again.
 //
 // Every wait (a bulk copy, the queue, a record another warp writes) is
 // bounded in time and sets a status bit when it gives up.
@@ -71,13 +72,11 @@ static_assert(kMaxChunks < 512, "a stats chunk index fits 9 bits");
 static_assert(kPlanMax <= 1024 && 2 * SPECV_MAX_DRAFT + 1 < 64, "a request fits 10 bits, a row 6");
 
 // workspace header words (int32 index), one 128-byte line each
-constexpr int kHStatus = 0, kHEpoch = 64, kHResid = 96, kHExit3 = 128;
+constexpr int kHStatus = 0, kHResid = 96, kHExit4 = 128;
 constexpr int kHeaderBytes = 1024;
-static_assert((kHExit3 + 1) * 4 <= kHeaderBytes, "header words fit the header");
+static_assert((kHExit4 + 1) * 4 <= kHeaderBytes, "header words fit the header");
 
-// Residual sum records are (value, call tag) pairs written with one 8-byte
-// store, so a record whose tag is not this call's is "not written yet"; no
-// record needs clearing between calls.
+
 
 constexpr int kItemA = 1, kItemR = 3;
 
@@ -88,9 +87,8 @@ constexpr float kLn2 = 0.6931471805599453f;
 // parameters, written by the decision.
 struct __align__(16) Req {
   int j;          // the rejected row
-  int cnt;        // residual pieces summed (returns to zero)
   float Sp_j;     // S_p of the rejected row
-  int pad;
+  int pad[2];
   float4 prm;     // Mp, Mq, log2(e)/T, S_p/S_q of the rejected row
 };
 static_assert(sizeof(Req) == 32, "Req is one 32-byte record");
@@ -117,8 +115,8 @@ struct Params {
   uint2* part;      // [B][R][NC] chunk records: (max, sum) or (max, index)
   float* zx;        // [B][R] the drafted token's logit in rows t < n
   int32_t* rlist;   // [B] requests waiting for a residual draw (count: header[kHResid])
-  uint2* dmass;     // [B][NCd] residual sums of the pieces: (sum, tag)
-  uint2* dsw;       // [B][NCd][kDrawSweeps] residual sums of their sweeps: (sum, tag)
+  float* dmass;     // [B][NCd] residual sums of the pieces (by list entry)
+  float* dsw;       // [B][NCd][kDrawSweeps] residual sums of their sweeps
   float* bsw;       // [B][NC][kChunkBytes / 512] sweep sums of each sampled request's row n
   float* row_stats; // [B][K+1][8] or null
 };
@@ -726,22 +724,35 @@ __device__ __forceinline__ float2 chunk_softmax(const unsigned char* slot, const
   const float M = warp_max(m);
   if (!(M > -INFINITY)) return make_float2(M, 0.0f);
   const float c = __fmul_rn(M, sT);
-  float s0 = 0.0f, s1 = 0.0f;
-#pragma unroll 2
-  for (int j = vs.vf0 + lane; j < vs.vf1; j += 32) {
-    float v[CH];
-    E::unpack(vec[j], v);
+  // eight independent sums, two vectors per step, so the exponentials and
+  // the adds of different elements overlap
+  float s[8];
 #pragma unroll
-    for (int q = 0; q < CH; q += 2) {
-      s0 = __fadd_rn(s0, ex2(__fmaf_rn(v[q], sT, -c)));
-      s1 = __fadd_rn(s1, ex2(__fmaf_rn(v[q + 1], sT, -c)));
+  for (int q = 0; q < 8; ++q) s[q] = 0.0f;
+  int j = vs.vf0 + lane;
+#pragma unroll 2
+  for (; j + 32 < vs.vf1; j += 64) {
+    float a[CH], b[CH];
+    E::unpack(vec[j], a);
+    E::unpack(vec[j + 32], b);
+#pragma unroll
+    for (int q = 0; q < CH; ++q) {
+      s[q & 7] = __fadd_rn(s[q & 7], ex2(__fmaf_rn(a[q], sT, -c)));
+      s[(q + CH) & 7] = __fadd_rn(s[(q + CH) & 7], ex2(__fmaf_rn(b[q], sT, -c)));
     }
+  }
+  if (j < vs.vf1) {
+    float a[CH];
+    E::unpack(vec[j], a);
+#pragma unroll
+    for (int q = 0; q < CH; ++q) s[q & 7] = __fadd_rn(s[q & 7], ex2(__fmaf_rn(a[q], sT, -c)));
   }
   if (my_edge >= 0) {
 #pragma unroll
-    for (int q = 0; q < CH; ++q) s0 = __fadd_rn(s0, ex2(__fmaf_rn(ev[q], sT, -c)));
+    for (int q = 0; q < CH; ++q) s[q & 7] = __fadd_rn(s[q & 7], ex2(__fmaf_rn(ev[q], sT, -c)));
   }
-  const float S = warp_sum(__fadd_rn(s0, s1));
+  const float S = warp_sum(__fadd_rn(__fadd_rn(__fadd_rn(s[0], s[1]), __fadd_rn(s[2], s[3])),
+                                     __fadd_rn(__fadd_rn(s[4], s[5]), __fadd_rn(s[6], s[7]))));
   return make_float2(M, __fmul_rn(S, ex2(-__fmaf_rn(M, sT, -c))));
 }
 
@@ -1191,17 +1202,6 @@ __device__ bool fetch(const Params& P, Agent& ag, int s, uintptr_t rp, uintptr_t
 
 // ---------------------------------------------------------------- records
 
-__device__ __forceinline__ void st_tagged(uint2* p, float v, uint32_t tag) {
-  const unsigned long long w = (static_cast<unsigned long long>(tag) << 32) | __float_as_uint(v);
-  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
-}
-
-__device__ __forceinline__ uint2 ld_tagged(const uint2* p) {
-  unsigned long long v;
-  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return make_uint2(static_cast<uint32_t>(v), static_cast<uint32_t>(v >> 32));
-}
-
 // Whole warp: chunk masses of a draw from p (one row's records rescaled to
 // the row maximum Mp) into scratch.
 __device__ __forceinline__ void p_masses(const uint2* rec, int NC, float Mp, float sT, float* mass,
@@ -1433,66 +1433,46 @@ __device__ void decide_request(const Params& P, DecideSmem& D, int b) {
   }
 }
 
-// Whole warp: n tagged records into dst (floats), each read until it
-// carries this call's tag; false if a wait gave up.
-__device__ bool stage_tagged(float* dst, const uint2* src, int n, uint32_t tag, int lane) {
-  const long long t0 = clock64();
-  for (int c0 = 0; c0 < n; c0 += 32) {
-    const int c = c0 + lane;
-    uint2 w = c < n ? ld_tagged(src + c) : make_uint2(0u, tag);
-    while (!__all_sync(0xffffffffu, w.y == tag)) {
-      if (clock64() - t0 > kWaitLimitCycles) return false;
-      __nanosleep(64);
-      if (w.y != tag) w = ld_tagged(src + c);
-    }
-    if (c < n) dst[c] = __uint_as_float(w.x);
-  }
-  __syncwarp();
-  return true;
-}
-
 // Whole warp: the residual draw of listed request b (entry e, rejected at
-// row j) once all its pieces are summed, with uniforms_resample[b]: the
-// piece from their sums, the sweep from the piece's sweep sums, the token
-// from the sweep of both rows read again.  A residual of exactly zero mass
-// falls back to drawing from p_j with the same uniform (its chunk masses
-// from row j's records, the token from one re-read chunk).  Slot s is the
-// scratch.
+// row j), with uniforms_resample[b]: the piece from the piece sums, the
+// sweep from that piece's sweep sums, the token from the sweep of both rows
+// read again.  A residual of exactly zero mass falls back to drawing from
+// p_j with the same uniform (its chunk masses from row j's records, the
+// token from one re-read chunk).  Slot 0 of the warp's ring is its scratch.
 template <int DT>
-__device__ void residual_search(const Params& P, Agent& ag, int s, int e, int b, int j,
-                                const float4& prm, uint32_t tag) {
+__device__ void residual_search(const Params& P, Agent& ag, int e) {
   constexpr int CH = Elt<DT>::kPerVec;
   const int lane = ag.lane, K = P.K, V = P.V, NC = P.NC, NCd = P.NCd;
-  float* mass = reinterpret_cast<float*>(ag.slot(s));
+  const int b = __ldcg(P.rlist + e);
+  const int j = __ldcg(&P.req[b].j);
+  const float4 prm = __ldcg(&P.req[b].prm);
+  float* mass = reinterpret_cast<float*>(ag.slot(0));
+  const float* dm = P.dmass + static_cast<size_t>(e) * NCd;
   __syncwarp();
-  bool staged = stage_tagged(mass, P.dmass + static_cast<size_t>(e) * NCd, NCd, tag, lane);
+  for (int c = lane; c < NCd; c += 32) mass[c] = __ldcg(dm + c);
+  __syncwarp();
   const float ur = __ldg(P.uniforms_resample + b);
   float W = 0.0f, rem = 0.0f;
-  int chunk = staged ? pick_chunk(mass, NCd, ur, lane, W, rem) : -1;
+  int chunk = pick_chunk(mass, NCd, ur, lane, W, rem);
   const uintptr_t rp = target_row<DT>(P, b, j);
   int tok = -1;
-  if (!staged) {
-    // a wait gave up: flagged below
-  } else if (W > 0.0f) {
+  if (W > 0.0f) {
     if (chunk >= 0) {
-      float* sws = mass + ((NCd + 3) & ~3);
-      staged = stage_tagged(sws, P.dsw + (static_cast<size_t>(e) * NCd + chunk) * kDrawSweeps,
-                            kDrawSweeps, tag, lane);
-      if (staged) {
-        float rem2 = 0.0f;
-        const int sweep = pick_lane(lane < kDrawSweeps ? sws[lane] : 0.0f, kDrawSweeps, rem,
-                                    lane, rem2);
-        if (sweep >= 0) {
-          const Chunk kp = chunk_of<DT>(rp, V, chunk, kDrawBytes);
-          const int jv = sweep * 32 + lane;
-          const int e0 = -kp.off0 / Elt<DT>::kBytes + jv * CH;
-          float vp[CH], vq[CH], w[CH];
-          global_vec<DT>(kp, P.t_lo, P.t_hi, jv, vp);
-          global_vec_at<DT>(draft_row<DT>(P, b, j), P.d_lo, P.d_hi, e0, kp.e_lo, kp.e_hi, vq);
+      const float sw = lane < kDrawSweeps
+          ? __ldcg(P.dsw + (static_cast<size_t>(e) * NCd + chunk) * kDrawSweeps + lane)
+          : 0.0f;
+      float rem2 = 0.0f;
+      const int sweep = pick_lane(sw, kDrawSweeps, rem, lane, rem2);
+      if (sweep >= 0) {
+        const Chunk kp = chunk_of<DT>(rp, V, chunk, kDrawBytes);
+        const int jv = sweep * 32 + lane;
+        const int e0 = -kp.off0 / Elt<DT>::kBytes + jv * CH;
+        float vp[CH], vq[CH], w[CH];
+        global_vec<DT>(kp, P.t_lo, P.t_hi, jv, vp);
+        global_vec_at<DT>(draft_row<DT>(P, b, j), P.d_lo, P.d_hi, e0, kp.e_lo, kp.e_hi, vq);
 #pragma unroll
-          for (int q = 0; q < CH; ++q) w[q] = weight(vp[q], vq[q], true, prm);
-          tok = pick_in_sweep<CH>(w, rem2, e0, lane);
-        }
+        for (int q = 0; q < CH; ++q) w[q] = weight(vp[q], vq[q], true, prm);
+        tok = pick_in_sweep<CH>(w, rem2, e0, lane);
       }
     }
   } else {
@@ -1500,8 +1480,8 @@ __device__ void residual_search(const Params& P, Agent& ag, int s, int e, int b,
     float Wp;
     chunk = pick_chunk(mass, NC, ur, lane, Wp, rem);
     Chunk kp, kq;
-    if (chunk >= 0 && fetch<DT>(P, ag, s, rp, 0, chunk, kChunkBytes, false, kp, kq))
-      tok = draw_in_slot<DT>(ag.slot(s), kp, kq, false, make_float4(prm.x, 0.0f, prm.z, 0.0f),
+    if (chunk >= 0 && fetch<DT>(P, ag, 0, rp, 0, chunk, kChunkBytes, false, kp, kq))
+      tok = draw_in_slot<DT>(ag.slot(0), kp, kq, false, make_float4(prm.x, 0.0f, prm.z, 0.0f),
                              rem, kChunkBytes / 512, lane);
   }
   if (P.row_stats && lane == 0) {
@@ -1510,11 +1490,12 @@ __device__ void residual_search(const Params& P, Agent& ag, int s, int e, int b,
     rs[7] = static_cast<float>(tok);
   }
   if (tok < 0 || tok >= V) {
-    if (lane == 0) atomicOr(P.header + kHStatus, staged ? SPECV_DEV_BAD_ROW : SPECV_DEV_TIMEOUT);
+    if (lane == 0) atomicOr(P.header + kHStatus, SPECV_DEV_BAD_ROW);
     write_outputs(P, b, -1, -1, -1, lane);
   } else if (lane == 0) {
     P.out_tokens[static_cast<size_t>(b) * (K + 1) + j] = tok;
   }
+  __syncwarp();
 }
 
 // ---------------------------------------------------------------- programmatic launch
@@ -1652,20 +1633,10 @@ __global__ void __launch_bounds__(kDecideWarps * 32) decide_kernel(const Params 
 
 // ---------------------------------------------------------------- residual kernel
 
-// A consumed piece whose count is not looked at yet.
-struct Pending {
-  int b, e, j;
-  float4 prm;
-  int old;   // lane 0: the count before this piece's
-  bool valid;
-};
-
-// Whole warp: sums the residual (p - q)+ of the piece pair in slot s, sweep
-// by sweep, stores the sums (tagged with the call) and counts the piece
-// (the count is looked at later).
+// Whole warp: sums the residual (p - q)+ of the piece pair in slot s,
+// sweep by sweep, and stores the piece's sum and its sweep sums.
 template <int DT>
-__device__ void consume_residual(const Params& P, Agent& ag, int s, const Item& it, uint32_t tag,
-                                 Pending& pd) {
+__device__ void consume_residual(const Params& P, Agent& ag, int s, const Item& it) {
   const int lane = ag.lane;
   unsigned char* slot = ag.slot(s);
   const Chunk kp = chunk_of<DT>(target_row<DT>(P, it.b, it.row), P.V, it.c, kDrawBytes);
@@ -1675,29 +1646,8 @@ __device__ void consume_residual(const Params& P, Agent& ag, int s, const Item& 
   float mine;
   const float t = piece_sweeps<DT>(slot, kp, kq, it.prm, lane, mine);
   const int e = it.n;   // the request's entry in the list
-  if (lane < kDrawSweeps)
-    st_tagged(P.dsw + (static_cast<size_t>(e) * P.NCd + it.c) * kDrawSweeps + lane, mine, tag);
-  if (lane == 0) {
-    st_tagged(P.dmass + static_cast<size_t>(e) * P.NCd + it.c, t, tag);
-    pd.old = atomicAdd(&P.req[it.b].cnt, 1);
-  }
-  pd.b = it.b;
-  pd.e = e;
-  pd.j = it.row;
-  pd.prm = it.prm;
-  pd.valid = true;
-}
-
-// Whole warp: looks at a consumed piece's count; the warp whose piece
-// completed the request draws its token, with slot s as scratch.
-template <int DT>
-__device__ void settle_residual(const Params& P, Agent& ag, int s, Pending& pd, uint32_t tag) {
-  pd.valid = false;
-  const int old = __shfl_sync(0xffffffffu, pd.old, 0);
-  if (old != P.NCd - 1) return;
-  if (ag.lane == 0) P.req[pd.b].cnt = 0;   // every piece is in: ready for the next call
-  __syncwarp();
-  residual_search<DT>(P, ag, s, pd.e, pd.b, pd.j, pd.prm, tag);
+  if (lane < kDrawSweeps) P.dsw[(static_cast<size_t>(e) * P.NCd + it.c) * kDrawSweeps + lane] = mine;
+  if (lane == 0) P.dmass[static_cast<size_t>(e) * P.NCd + it.c] = t;
 }
 
 // One lane: residual item i (entry i / NCd, piece i mod NCd).
@@ -1759,8 +1709,8 @@ __global__ void __launch_bounds__(kThreads, 1) residual_kernel(const Params P) {
   ag.ring = dyn + static_cast<size_t>(warp) * kSlots * kSlotBytes;
   ag.ph = 0;
   ag.lane = lane;
+  allow_dependents();
   const int count = __ldcg(P.header + kHResid);
-  const uint32_t tag = static_cast<uint32_t>(__ldcg(P.header + kHEpoch)) + 1u;
   const int total = count * P.NCd;
   const int G = static_cast<int>(gridDim.x) * kAgents;
   const int first = static_cast<int>(blockIdx.x) * kAgents + warp;
@@ -1768,10 +1718,6 @@ __global__ void __launch_bounds__(kThreads, 1) residual_kernel(const Params P) {
   Item mine = residual_pick_init();
   int base = -64;
   int issued = 0, consumed = 0;
-  bool ok = true;
-  Pending pd;
-  pd.valid = false;
-  pd.old = 0;
   for (;;) {
     while (issued - consumed < kSlots && issued < mine_n) {
       if (issued >= base + 32) {   // decode the next 32 of this warp's items, one per lane
@@ -1784,31 +1730,42 @@ __global__ void __launch_bounds__(kThreads, 1) residual_kernel(const Params P) {
       if (lane == 0) issue<DT>(P, ag, issued % kSlots, it);
       ++issued;
     }
-    if (issued == consumed) {
-      if (pd.valid) settle_residual<DT>(P, ag, 0, pd, tag);   // ring empty: slot 0 is free
-      break;
-    }
+    if (issued == consumed) break;
     const int s = consumed % kSlots;
-    if (!wait_slot(P, ag, s)) {
-      ok = false;
-      break;
-    }
-    Pending cur;
-    cur.old = 0;
-    consume_residual<DT>(P, ag, s, A[warp].item[s], tag, cur);
+    if (!wait_slot(P, ag, s)) break;
+    consume_residual<DT>(P, ag, s, A[warp].item[s]);
     ++consumed;
-    if (pd.valid) settle_residual<DT>(P, ag, s, pd, tag);   // slot s is consumed, not refilled
-    pd = cur;
   }
-  (void)ok;
+}
+
+// ---------------------------------------------------------------- search kernel
+
+template <int DT>
+__global__ void __launch_bounds__(kDecideWarps * 32) search_kernel(const Params P) {
+  __shared__ AgentSmem A[kDecideWarps];
+  extern __shared__ __align__(128) unsigned char dyn[];
+  const int tid = threadIdx.x, warp = tid >> 5;
+  if ((tid & 31) == 0) {
+    mbar_init(&A[warp].bar[0], 1);
+    mbar_init_fence();
+  }
+  __syncwarp();
+  wait_previous();
+  Agent ag;
+  ag.A = &A[warp];
+  ag.ring = dyn + static_cast<size_t>(warp) * kSlotBytes;
+  ag.ph = 0;
+  ag.lane = tid & 31;
+  const int count = __ldcg(P.header + kHResid);
+  for (int e = blockIdx.x * kDecideWarps + warp; e < count; e += gridDim.x * kDecideWarps)
+    residual_search<DT>(P, ag, e);
   __syncthreads();
   if (tid == 0) {
     __threadfence();
-    const int prev = atomicAdd(P.header + kHExit3, 1);
+    const int prev = atomicAdd(P.header + kHExit4, 1);
     if (prev == static_cast<int>(gridDim.x) - 1) {
-      P.header[kHExit3] = 0;
+      P.header[kHExit4] = 0;
       P.header[kHResid] = 0;   // the list is used up: empty for the next call
-      P.header[kHEpoch] = static_cast<int32_t>(tag);   // the next call's records get a new tag
     }
   }
 }
@@ -1845,8 +1802,8 @@ Layout ws_layout(int B, int K, int V, specv_dtype dt) {
   L.zx = align256(L.part + sizeof(uint2) * Bl * R * NC);
   L.rlist = align256(L.zx + sizeof(float) * Bl * R);
   L.dmass = align256(L.rlist + sizeof(int32_t) * Bl);
-  L.dsw = align256(L.dmass + sizeof(uint2) * Bl * NCd);
-  L.bsw = align256(L.dsw + sizeof(uint2) * Bl * NCd * kDrawSweeps);
+  L.dsw = align256(L.dmass + sizeof(float) * Bl * NCd);
+  L.bsw = align256(L.dsw + sizeof(float) * Bl * NCd * kDrawSweeps);
   L.total = align256(L.bsw + sizeof(float) * Bl * NC * kChunkSweeps);
   return L;
 }
@@ -1868,6 +1825,9 @@ cudaError_t resident_ctas(int* out) {
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(residual_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                kRingBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(search_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kDecideWarps * kSlotBytes);
     if (e != cudaSuccess) return e;
     int per_sm = 0, sms = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stats_kernel<DT>, kThreads,
@@ -1920,7 +1880,10 @@ cudaError_t launch_sequence(const Params& P, int grid, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   e = launch_dependent(decide_kernel<DT>, P.B, kDecideWarps * 32, 0, stream, P);
   if (e != cudaSuccess) return e;
-  return launch_dependent(residual_kernel<DT>, grid, kThreads, kRingBytes, stream, P);
+  e = launch_dependent(residual_kernel<DT>, grid, kThreads, kRingBytes, stream, P);
+  if (e != cudaSuccess) return e;
+  return launch_dependent(search_kernel<DT>, (P.B + kDecideWarps - 1) / kDecideWarps,
+                          kDecideWarps * 32, kDecideWarps * kSlotBytes, stream, P);
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -1988,8 +1951,8 @@ specv_status launch(const void* target, const void* draft, specv_dtype dtype,
     P.part = reinterpret_cast<uint2*>(ws + L.part);
     P.zx = reinterpret_cast<float*>(ws + L.zx);
     P.rlist = reinterpret_cast<int32_t*>(ws + L.rlist);
-    P.dmass = reinterpret_cast<uint2*>(ws + L.dmass);
-    P.dsw = reinterpret_cast<uint2*>(ws + L.dsw);
+    P.dmass = reinterpret_cast<float*>(ws + L.dmass);
+    P.dsw = reinterpret_cast<float*>(ws + L.dsw);
     P.bsw = reinterpret_cast<float*>(ws + L.bsw);
     P.row_stats = row_stats ? row_stats + static_cast<size_t>(b0) * (K + 1) * 8 : nullptr;
     const cudaError_t e = dtype == SPECV_BF16 ? launch_sequence<SPECV_BF16>(P, grid, stream)
