@@ -912,13 +912,36 @@ __device__ __forceinline__ void slot_vec(const unsigned char* slot, const Vecs& 
   }
 }
 
+// Whole warp: N values per lane (N = 8 or 16) to their sums over the warp,
+// halving the values a lane holds at each exchange: lane l ends with the
+// sum of value l >> (5 - log2 N) (2 N - 1 shuffles instead of 5 N).
+template <int N>
+__device__ __forceinline__ float sweep_totals(float (&v)[N], int lane) {
+  static_assert(N == 8 || N == 16, "8 or 16 values");
+  int o = 16;
+#pragma unroll
+  for (int h = N / 2; h >= 1; h /= 2) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < h; ++i) {
+      const float send = up ? v[i] : v[i + h];
+      const float keep = up ? v[i + h] : v[i];
+      v[i] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, o));
+    }
+    o >>= 1;
+  }
+#pragma unroll
+  for (; o >= 1; o >>= 1) v[0] = __fadd_rn(v[0], __shfl_xor_sync(0xffffffffu, v[0], o));
+  return v[0];
+}
+
 // Whole warp: (max, sum of exp((z - max)/T)) of a stats chunk, and the sum
-// of each 512-byte sweep (slot vectors [32 s, 32 s + 32)), which lane s
-// stores to sw[s].  The chunk sum is the sweep sums added in order.
+// of each 512-byte sweep (slot vectors [32 s, 32 s + 32)), stored to sw[s].
 template <int DT>
 __device__ float2 chunk_softmax_sweeps(const unsigned char* slot, const Chunk& k, float sT,
                                        int lane, float* sw) {
   constexpr int CH = Elt<DT>::kPerVec;
+  static_assert(kChunkSweeps <= 16, "sweeps of a chunk fit the exchange");
   const Vecs vs = vecs_of<DT>(k);
   float m = -INFINITY;
 #pragma unroll 4
@@ -929,51 +952,65 @@ __device__ float2 chunk_softmax_sweeps(const unsigned char* slot, const Chunk& k
     for (int q = 0; q < CH; ++q) m = fmaxf(m, v[q]);
   }
   const float M = warp_max(m);
+  const bool store = (lane & 1) == 0 && (lane >> 1) < kChunkSweeps;
   if (!(M > -INFINITY)) {
-    if (lane < kChunkSweeps) sw[lane] = 0.0f;
+    if (store) sw[lane >> 1] = 0.0f;
     return make_float2(M, 0.0f);
   }
   const float c = __fmul_rn(M, sT);
   const float corr = ex2(-__fmaf_rn(M, sT, -c));
-  float S = 0.0f, mine = 0.0f;
-#pragma unroll 4
+  float t[16];
+#pragma unroll
+  for (int s = 0; s < 16; ++s) t[s] = 0.0f;
+  float all = 0.0f;
+#pragma unroll
   for (int s = 0; s < kChunkSweeps; ++s) {
     float v[CH];
     slot_vec<DT>(slot, vs, k, s * 32 + lane, v);
-    float t = 0.0f;
+    float a = 0.0f, b = 0.0f;
 #pragma unroll
-    for (int q = 0; q < CH; ++q) t = __fadd_rn(t, ex2(__fmaf_rn(v[q], sT, -c)));
-    const float ssum = __fmul_rn(warp_sum(t), corr);
-    if (lane == s) mine = ssum;
-    S = __fadd_rn(S, ssum);
+    for (int q = 0; q < CH; q += 2) {
+      a = __fadd_rn(a, ex2(__fmaf_rn(v[q], sT, -c)));
+      b = __fadd_rn(b, ex2(__fmaf_rn(v[q + 1], sT, -c)));
+    }
+    t[s] = __fadd_rn(a, b);
+    all = __fadd_rn(all, t[s]);
   }
-  if (lane < kChunkSweeps) sw[lane] = mine;
-  return make_float2(M, S);
+  const float S = warp_sum(all);
+  const float mine = sweep_totals<16>(t, lane);
+  if (store) sw[lane >> 1] = __fmul_rn(mine, corr);
+  return make_float2(M, __fmul_rn(S, corr));
 }
 
 // Whole warp: the residual mass of a piece pair in a slot, sweep by sweep
-// (as chunk_draw forms the weights); lane s < kDrawSweeps gets sweep s's
-// sum, every lane the piece's total (the sweep sums added in order).
+// (as chunk_draw forms the weights).  Returns the piece's total; `mine`
+// gets the sum of sweep lane >> 2 (lanes 4 s hold sweep s).
 template <int DT>
 __device__ float piece_sweeps(const unsigned char* slot, const Chunk& kp, const Chunk& kq,
                               const float4& prm, int lane, float& mine) {
   constexpr int CH = Elt<DT>::kPerVec;
+  static_assert(kDrawSweeps <= 8, "sweeps of a piece fit the exchange");
   const Vecs vs = vecs_of<DT>(kp);
   const bool same = kq.off0 == kp.off0;
-  float total = 0.0f;
-  mine = 0.0f;
-#pragma unroll 4
+  float t[8];
+#pragma unroll
+  for (int s = 0; s < 8; ++s) t[s] = 0.0f;
+  float all = 0.0f;
+#pragma unroll
   for (int s = 0; s < kDrawSweeps; ++s) {
     float w[CH];
     vector_weights<DT>(slot, vs, kp, kq, true, same, prm, s * 32 + lane, w);
-    float t = 0.0f;
+    float a = 0.0f, b = 0.0f;
 #pragma unroll
-    for (int q = 0; q < CH; ++q) t = __fadd_rn(t, w[q]);
-    const float ssum = warp_sum(t);
-    if (lane == s) mine = ssum;
-    total = __fadd_rn(total, ssum);
+    for (int q = 0; q < CH; q += 2) {
+      a = __fadd_rn(a, w[q]);
+      b = __fadd_rn(b, w[q + 1]);
+    }
+    t[s] = __fadd_rn(a, b);
+    all = __fadd_rn(all, t[s]);
   }
-  return total;
+  mine = sweep_totals<8>(t, lane);
+  return warp_sum(all);
 }
 
 // Values of slot vector j of chunk k read from global memory (the slot's
@@ -1646,7 +1683,8 @@ __device__ void consume_residual(const Params& P, Agent& ag, int s, const Item& 
   float mine;
   const float t = piece_sweeps<DT>(slot, kp, kq, it.prm, lane, mine);
   const int e = it.n;   // the request's entry in the list
-  if (lane < kDrawSweeps) P.dsw[(static_cast<size_t>(e) * P.NCd + it.c) * kDrawSweeps + lane] = mine;
+  if ((lane & 3) == 0 && (lane >> 2) < kDrawSweeps)
+    P.dsw[(static_cast<size_t>(e) * P.NCd + it.c) * kDrawSweeps + (lane >> 2)] = mine;
   if (lane == 0) P.dmass[static_cast<size_t>(e) * P.NCd + it.c] = t;
 }
 
