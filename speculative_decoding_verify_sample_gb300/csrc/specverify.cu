@@ -8,9 +8,9 @@
 // draft is accepted draw a bonus token from p at the next position; at
 // temperature 0 compare argmax(p) with the draft instead.
 //
-// Design: four kernels on the caller's stream, each after the first
-// launched as a programmatic dependent so its launch overlaps the previous
-// kernel's tail.
+// Design: four kernels on the caller's stream, each launched as a
+// programmatic dependent so its launch and prologue overlap the previous
+// kernel's tail; each waits for the previous kernel before it writes.
 //
 //  1. stats_kernel streams every row a request needs (target rows t <= n,
 //     draft rows t < n when sampled) once from HBM with TMA bulk copies,
@@ -1260,10 +1260,31 @@ constexpr int kMaxRows = 2 * SPECV_MAX_DRAFT + 1;
 struct DecideSmem {
   float M[kMaxRows], S[kMaxRows];   // row r: maximum (raw logit) and sum, or the argmax value
   int arg[kMaxRows];                // greedy: the argmax
-  float mass[kMaxChunks];           // chunk masses of a bonus draw
+  float mass[kMaxChunks];           // a sampled request's row n: chunk masses of the bonus draw
+  float sw[kMaxChunks * kChunkSweeps];   // and the kept sweep sums of its chunks
+  uint2 rec[kDecideWarps][kMaxChunks];   // each warp's row records, staged
 };
 
-// Whole warp: combines one row from its NC records, a lane per chunk
+// Whole warp: n 8-byte records into shared memory, four loads in flight per
+// lane before any is stored.
+__device__ __forceinline__ void stage_rec(uint2* dst, const uint2* src, int n, int lane) {
+  for (int base = 0; base < n; base += 128) {
+    uint2 v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int i = base + 32 * k + lane;
+      if (i < n) v[k] = __ldcg(src + i);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int i = base + 32 * k + lane;
+      if (i < n) dst[i] = v[k];
+    }
+  }
+  __syncwarp();
+}
+
+// Whole warp: combines one row from its NC staged records, a lane per chunk
 // (lane c takes chunks c, c + 32, ...): (max, sum of exp((z - max)/T)), or
 // at T = 0 (max, lowest index holding it).
 __device__ __forceinline__ void combine_row_warp(const uint2* rec, int NC, bool greedy, float sT,
@@ -1271,7 +1292,7 @@ __device__ __forceinline__ void combine_row_warp(const uint2* rec, int NC, bool 
   float m = -INFINITY;
   int idx = INT_MAX;
   for (int c = lane; c < NC; c += 32) {
-    const uint2 r = __ldcg(rec + c);
+    const uint2 r = rec[c];
     const float v = __uint_as_float(r.x);
     if (v > m) {   // chunks in increasing order: the first chunk holding a lane's maximum
       m = v;
@@ -1288,7 +1309,7 @@ __device__ __forceinline__ void combine_row_warp(const uint2* rec, int NC, bool 
   float s = 0.0f;
   if (M > -INFINITY) {
     for (int c = lane; c < NC; c += 32) {
-      const uint2 r = __ldcg(rec + c);
+      const uint2 r = rec[c];
       const float v = __uint_as_float(r.x);
       if (v > -INFINITY) s = __fadd_rn(s, __fmul_rn(__uint_as_float(r.y), scaled_exp(v, M, sT)));
     }
@@ -1339,12 +1360,25 @@ __device__ void decide_request(const Params& P, DecideSmem& D, int b) {
     const int row = r < nt ? r : K + 1 + (r - nt);
     float M, S;
     int arg;
-    combine_row_warp(P.part + (static_cast<size_t>(b) * R + row) * NC, NC, greedy, sT, lane, M, S,
-                     arg);
+    uint2* rec = D.rec[warp];
+    __syncwarp();
+    stage_rec(rec, P.part + (static_cast<size_t>(b) * R + row) * NC, NC, lane);
+    const bool bonus_row = !greedy && r == n;
+    if (bonus_row) {   // row n: the kept sweep sums too, loaded while the row combines
+      const float* bs = P.bsw + static_cast<size_t>(b) * NC * kChunkSweeps;
+      for (int i = lane; i < NC * kChunkSweeps; i += 32) D.sw[i] = __ldcg(bs + i);
+    }
+    combine_row_warp(rec, NC, greedy, sT, lane, M, S, arg);
     if (lane == 0) {
       D.M[r] = M;
       D.S[r] = S;
       D.arg[r] = arg;
+    }
+    if (bonus_row) {   // the bonus draw's chunk masses, ready before the decision
+      for (int c = lane; c < NC; c += 32) {
+        const float m = __uint_as_float(rec[c].x);
+        D.mass[c] = m > -INFINITY ? __fmul_rn(__uint_as_float(rec[c].y), scaled_exp(m, M, sT)) : 0.0f;
+      }
     }
   }
   __syncthreads();
@@ -1436,15 +1470,12 @@ __device__ void decide_request(const Params& P, DecideSmem& D, int b) {
   constexpr int CH = Elt<DT>::kPerVec;
   const float u = __shfl_sync(0xffffffffu, u_lane, n);
   const uint2* rec_n = P.part + (static_cast<size_t>(b) * R + n) * NC;
-  p_masses(rec_n, NC, Mp, sT, D.mass, lane);
   float W, rem;
   const int chunk = pick_chunk(D.mass, NC, u, lane, W, rem);
   int tok = -1;
   if (chunk >= 0) {
     const float f = scaled_exp(__uint_as_float(__ldcg(rec_n + chunk).x), Mp, sT);
-    const float sw = lane < kChunkSweeps
-        ? __fmul_rn(__ldcg(P.bsw + (static_cast<size_t>(b) * NC + chunk) * kChunkSweeps + lane), f)
-        : 0.0f;
+    const float sw = lane < kChunkSweeps ? __fmul_rn(D.sw[chunk * kChunkSweeps + lane], f) : 0.0f;
     float rem2 = 0.0f;
     const int sweep = pick_lane(sw, kChunkSweeps, rem, lane, rem2);
     if (sweep >= 0) {
@@ -1642,7 +1673,10 @@ __global__ void __launch_bounds__(kThreads, 1) stats_kernel(const Params P) {
     mbar_init(&S.ag[tid / kSlots].bar[tid % kSlots], 1);
     mbar_init_fence();
   }
-  build_plan(P, S.plan, S.red);   // ends with a CTA barrier
+  build_plan(P, S.plan, S.red);   // ends with a CTA barrier; reads the inputs only
+  // The previous kernel on the stream (the last one of an earlier call, when
+  // calls follow each other) may still run: write nothing before it ends.
+  wait_previous();
   allow_dependents();
 
   Agent ag;
@@ -1789,6 +1823,7 @@ __global__ void __launch_bounds__(kDecideWarps * 32) search_kernel(const Params 
   }
   __syncwarp();
   wait_previous();
+  allow_dependents();
   Agent ag;
   ag.A = &A[warp];
   ag.ring = dyn + static_cast<size_t>(warp) * kSlotBytes;
@@ -1913,8 +1948,7 @@ cudaError_t launch_dependent(Kern kernel, int grid, int block, int smem, cudaStr
 
 template <int DT>
 cudaError_t launch_sequence(const Params& P, int grid, cudaStream_t stream) {
-  stats_kernel<DT><<<grid, kThreads, kRingBytes, stream>>>(P);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_dependent(stats_kernel<DT>, grid, kThreads, kRingBytes, stream, P);
   if (e != cudaSuccess) return e;
   e = launch_dependent(decide_kernel<DT>, P.B, kDecideWarps * 32, 0, stream, P);
   if (e != cudaSuccess) return e;
