@@ -46,9 +46,9 @@ import numpy as np  # noqa: E402
 METRIC = "verify rows/s (B×(K+1) rows of V logits) and achieved HBM GB/s vs GB300 peak"
 KERNEL_SRC = os.path.join(ROOT, "speculative_decoding_verify_sample_gb300", "csrc", "specverify.cu")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "verify_kernel_traffic.json")
-# A call launches three kernels (row statistics, decisions, residual draws)
-# per sequence of at most 1024 requests.
-KERNELS_PER_SEQUENCE = 3
+# A call launches four kernels (row statistics, decisions, residual piece
+# sums, residual searches) per sequence of at most 1024 requests.
+KERNELS_PER_SEQUENCE = 4
 REQUESTS_PER_SEQUENCE = 1024
 FALLBACK_HBM_GBS = 6800.0
 
@@ -383,8 +383,8 @@ def run_ours(args, torch, world, rank, local):
             "kernel_plan": sv.launch_plan(B, K, V, inp["dtype"], inp.get("draft") is not None),
             "parallelism": f"{world} independent replica(s), requests sharded per rank"},
         "roofline": {
-            "kernel": "spec_verify_sample (stats_kernel + decide_kernel + residual_kernel, "
-                      "one call)",
+            "kernel": "spec_verify_sample (stats_kernel + decide_kernel + residual_kernel + "
+                      "search_kernel, one call)",
             "bound": "hbm", "achieved": round(achieved, 1),
             "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
             "traffic": recorded_traffic(args.workload),

@@ -138,9 +138,9 @@ specv_status specv_workspace_init(void* workspace, size_t workspace_bytes, specv
  *   workspace         specv_workspace_bytes(B, K, V, dtype) bytes, 256-byte aligned,
  *                     zeroed once with specv_workspace_init.  Calls that may
  *                     run concurrently need separate workspaces.
- * Enqueues three kernels on `stream` per 1024 requests (row statistics,
- * decisions, residual draws; the second and third as programmatic dependent
- * launches); no host synchronisation.
+ * Enqueues four kernels on `stream` per 1024 requests (row statistics,
+ * decisions, residual piece sums, residual searches; the last three as
+ * programmatic dependent launches); no host synchronisation.
  */
 specv_status spec_verify_sample(const void* target_logits, const void* draft_logits,
                                 specv_dtype dtype, const int32_t* draft_tokens,

@@ -57,7 +57,7 @@ constexpr int kDraftOff = kDrawBytes;                   // draft part of a resid
 constexpr int kSlotBytes = kChunkBytes + 32;
 constexpr int kRingBytes = kAgents * kSlots * kSlotBytes;
 constexpr int kPlanMax = 1024;                          // requests per launch (the host splits)
-constexpr int kDecideWarps = 8;                         // decide_kernel: one warp per request
+constexpr int kDecideWarps = 4;                         // warps of a decide / search CTA
 constexpr int kMaxRowBytes = 1 << 21;                   // 2 MB per row of logits
 constexpr int kMaxChunks = (kMaxRowBytes + 15 + kChunkBytes - 1) / kChunkBytes;
 constexpr int kMaxDrawChunks = (kMaxRowBytes + 15 + kDrawBytes - 1) / kDrawBytes;
@@ -117,7 +117,6 @@ struct Params {
   int32_t* rlist;   // [B] requests waiting for a residual draw (count: header[kHResid])
   float* dmass;     // [B][NCd] residual sums of the pieces (by list entry)
   float* dsw;       // [B][NCd][kDrawSweeps] residual sums of their sweeps
-  float* bsw;       // [B][NC][kChunkBytes / 512] sweep sums of each sampled request's row n
   float* row_stats; // [B][K+1][8] or null
 };
 
@@ -138,7 +137,7 @@ struct __align__(16) Item {
   int n;        // the request's draft length
   float sT;     // log2(e)/T (0: greedy)
   int x;        // drafted token of the row (rows t < n of sampled requests), else -1
-  int bonus;    // the row is target row n of a sampled request (its sweep sums are kept)
+  int bonus;    // unused (0)
   float4 prm;   // residual: the decision's Mp, Mq, log2(e)/T, S_p/S_q
 };
 
@@ -628,7 +627,7 @@ __device__ uint4 decode_ticket(const Params& P, const Plan& pl, int t) {
   const int row = slot_row(slot, sampled, n, P.K);
   int x = -1;
   if (sampled && slot < 2 * n) x = __ldg(P.draft_tokens + static_cast<size_t>(b) * P.K + (slot >> 1));
-  return pack_item(kItemA, b, row, c, x, sT, n, sampled && slot == 2 * n);
+  return pack_item(kItemA, b, row, c, x, sT, n, false);
 }
 // ---------------------------------------------------------------- chunk reductions
 
@@ -895,23 +894,6 @@ __device__ int draw_in_slot(const unsigned char* slot, const Chunk& kp, const Ch
 
 constexpr int kChunkSweeps = kChunkBytes / 512;   // 512-byte sweeps of a stats chunk
 
-// Values of slot vector j of a chunk, -inf outside [e_lo, e_hi).
-template <int DT>
-__device__ __forceinline__ void slot_vec(const unsigned char* slot, const Vecs& vs, const Chunk& k,
-                                         int j, float* v) {
-  using E = Elt<DT>;
-  constexpr int CH = E::kPerVec;
-  const int e0 = vs.e_base + j * CH;
-  if (e0 >= k.e_lo && e0 + CH <= k.e_hi) {
-    E::unpack(reinterpret_cast<const uint4*>(slot)[j], v);
-  } else if (e0 + CH > k.e_lo && e0 < k.e_hi) {
-    masked_vec<DT>(slot, vs, k, j, v);
-  } else {
-#pragma unroll
-    for (int q = 0; q < CH; ++q) v[q] = -INFINITY;
-  }
-}
-
 // Whole warp: N values per lane (N = 8 or 16) to their sums over the warp,
 // halving the values a lane holds at each exchange: lane l ends with the
 // sum of value l >> (5 - log2 N) (2 N - 1 shuffles instead of 5 N).
@@ -933,53 +915,6 @@ __device__ __forceinline__ float sweep_totals(float (&v)[N], int lane) {
 #pragma unroll
   for (; o >= 1; o >>= 1) v[0] = __fadd_rn(v[0], __shfl_xor_sync(0xffffffffu, v[0], o));
   return v[0];
-}
-
-// Whole warp: (max, sum of exp((z - max)/T)) of a stats chunk, and the sum
-// of each 512-byte sweep (slot vectors [32 s, 32 s + 32)), stored to sw[s].
-template <int DT>
-__device__ float2 chunk_softmax_sweeps(const unsigned char* slot, const Chunk& k, float sT,
-                                       int lane, float* sw) {
-  constexpr int CH = Elt<DT>::kPerVec;
-  static_assert(kChunkSweeps <= 16, "sweeps of a chunk fit the exchange");
-  const Vecs vs = vecs_of<DT>(k);
-  float m = -INFINITY;
-#pragma unroll 4
-  for (int s = 0; s < kChunkSweeps; ++s) {
-    float v[CH];
-    slot_vec<DT>(slot, vs, k, s * 32 + lane, v);
-#pragma unroll
-    for (int q = 0; q < CH; ++q) m = fmaxf(m, v[q]);
-  }
-  const float M = warp_max(m);
-  const bool store = (lane & 1) == 0 && (lane >> 1) < kChunkSweeps;
-  if (!(M > -INFINITY)) {
-    if (store) sw[lane >> 1] = 0.0f;
-    return make_float2(M, 0.0f);
-  }
-  const float c = __fmul_rn(M, sT);
-  const float corr = ex2(-__fmaf_rn(M, sT, -c));
-  float t[16];
-#pragma unroll
-  for (int s = 0; s < 16; ++s) t[s] = 0.0f;
-  float all = 0.0f;
-#pragma unroll
-  for (int s = 0; s < kChunkSweeps; ++s) {
-    float v[CH];
-    slot_vec<DT>(slot, vs, k, s * 32 + lane, v);
-    float a = 0.0f, b = 0.0f;
-#pragma unroll
-    for (int q = 0; q < CH; q += 2) {
-      a = __fadd_rn(a, ex2(__fmaf_rn(v[q], sT, -c)));
-      b = __fadd_rn(b, ex2(__fmaf_rn(v[q + 1], sT, -c)));
-    }
-    t[s] = __fadd_rn(a, b);
-    all = __fadd_rn(all, t[s]);
-  }
-  const float S = warp_sum(all);
-  const float mine = sweep_totals<16>(t, lane);
-  if (store) sw[lane >> 1] = __fmul_rn(mine, corr);
-  return make_float2(M, __fmul_rn(S, corr));
 }
 
 // Whole warp: the residual mass of a piece pair in a slot, sweep by sweep
@@ -1255,15 +1190,32 @@ __device__ __forceinline__ void p_masses(const uint2* rec, int NC, float Mp, flo
 // ---------------------------------------------------------------- decisions
 
 constexpr int kMaxRows = 2 * SPECV_MAX_DRAFT + 1;
+constexpr int kDecideRecs = 1024;   // records a decide CTA stages at once
+constexpr int kDecideBuf = kDecideRecs > kDecideWarps * kMaxChunks ? kDecideRecs
+                                                                    : kDecideWarps * kMaxChunks;
 
 // The decision kernel's shared memory: one request's combined rows.
 struct DecideSmem {
   float M[kMaxRows], S[kMaxRows];   // row r: maximum (raw logit) and sum, or the argmax value
   int arg[kMaxRows];                // greedy: the argmax
   float mass[kMaxChunks];           // a sampled request's row n: chunk masses of the bonus draw
-  float sw[kMaxChunks * kChunkSweeps];   // and the kept sweep sums of its chunks
-  uint2 rec[kDecideWarps][kMaxChunks];   // each warp's row records, staged
+  int x[SPECV_MAX_DRAFT];           // the request's drafted tokens
+  float u[SPECV_MAX_DRAFT + 1];     // its uniforms
+  float zp[SPECV_MAX_DRAFT], zq[SPECV_MAX_DRAFT];   // the drafted tokens' logits
+  float ur;                         // its resample uniform
+  alignas(16) uint2 rec[kDecideBuf];   // the request's row records (else each warp's row), staged
 };
+
+// One lane: an asynchronous 16-byte copy global -> shared (through L2), and
+// the wait for every such copy this lane issued.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)),
+               "l"(__cvta_generic_to_global(src))
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
 
 // Whole warp: n 8-byte records into shared memory, four loads in flight per
 // lane before any is stored.
@@ -1317,14 +1269,51 @@ __device__ __forceinline__ void combine_row_warp(const uint2* rec, int NC, bool 
   S = warp_sum(s);
 }
 
+// One group of 8 lanes (sub = lane & 7; every lane of the warp calls it):
+// combines a row from its NC staged records, chunks c = sub, sub + 8, ...;
+// a group with valid false takes no records.
+__device__ __forceinline__ void combine_row_group(const uint2* rec, int NC, bool valid, bool greedy,
+                                                  float sT, int sub, float& M, float& S,
+                                                  int& arg) {
+  const int nc = valid ? NC : 0;
+  float m = -INFINITY;
+  int idx = INT_MAX;
+  for (int c = sub; c < nc; c += 8) {
+    const uint2 r = rec[c];
+    const float v = __uint_as_float(r.x);
+    if (v > m) {   // chunks in increasing order: the first chunk holding a lane's maximum
+      m = v;
+      idx = static_cast<int>(r.y);
+    }
+  }
+  M = m;
+#pragma unroll
+  for (int o = 4; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  int a = m == M ? idx : INT_MAX;
+#pragma unroll
+  for (int o = 4; o > 0; o >>= 1) a = min(a, __shfl_xor_sync(0xffffffffu, a, o));
+  arg = a;
+  float s = 0.0f;
+  if (!greedy && M > -INFINITY) {
+    for (int c = sub; c < nc; c += 8) {
+      const uint2 r = rec[c];
+      const float v = __uint_as_float(r.x);
+      if (v > -INFINITY) s = __fadd_rn(s, __fmul_rn(__uint_as_float(r.y), scaled_exp(v, M, sT)));
+    }
+  }
+#pragma unroll
+  for (int o = 4; o > 0; o >>= 1) s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, o));
+  S = s;
+}
+
 // Whole CTA: decides request b from the stats kernel's records and writes
 // its outputs.  The CTA's warps combine the request's rows (target rows
 // t <= n, draft rows t < n when sampled); warp 0 then takes the decision.
 // Greedy: the argmax of target rows t <= n against the drafts.  Sampled:
 // the left-to-right test u_t q(x_t) < p(x_t) in log2 form; every draft
 // accepted draws the bonus token from p_n here (the chunk from row n's
-// records, the sweep from its sweep sums, the token from one re-read
-// 512-byte sweep); a rejection at j stores the residual draw's parameters
+// records, then that chunk read once more for its sweep sums, the sweep
+// and the element); a rejection at j stores the residual draw's parameters
 // and lists the request for the residual kernel, which writes
 // out_tokens[b, j].
 template <int DT>
@@ -1344,45 +1333,106 @@ __device__ void decide_request(const Params& P, DecideSmem& D, int b) {
   const bool greedy = !(T > 0.0f);
   const float sT = greedy ? 0.0f : temp_scale(T);
   const int nt = n + 1, nd = greedy ? 0 : n;
-  // warp 0's inputs first, so their loads overlap the combining
-  int x_lane = -1;
-  float u_lane = 0.0f, ur = 0.0f, zp = 0.0f, zq = 0.0f;
-  if (warp == 0) {
-    if (lane < n) x_lane = __ldg(P.draft_tokens + static_cast<size_t>(b) * K + lane);
-    if (lane <= n) u_lane = __ldg(P.uniforms + static_cast<size_t>(b) * (K + 1) + lane);
-    ur = __ldg(P.uniforms_resample + b);
-    if (!greedy && lane < n) {
-      zp = __ldcg(P.zx + static_cast<size_t>(b) * R + lane);
-      zq = __ldcg(P.zx + static_cast<size_t>(b) * R + K + 1 + lane);
+  // The request's records and warp 0's inputs (drafted tokens, uniforms,
+  // the drafted tokens' logits) in one batch of loads, every load issued
+  // before any is stored; records that do not fit are staged a row at a
+  // time per warp below.
+  const int nrows = nt + nd;
+  const bool all_at_once = nrows * NC <= kDecideRecs;
+  {
+    int xi = -1;
+    float uf = 0.0f, zpf = 0.0f, zqf = 0.0f, urf = 0.0f;
+    if (tid < 32) {
+      if (tid < n) xi = __ldg(P.draft_tokens + static_cast<size_t>(b) * K + tid);
+      if (tid <= n) uf = __ldg(P.uniforms + static_cast<size_t>(b) * (K + 1) + tid);
+      if (!greedy && tid < n) {
+        zpf = __ldcg(P.zx + static_cast<size_t>(b) * R + tid);
+        zqf = __ldcg(P.zx + static_cast<size_t>(b) * R + K + 1 + tid);
+      }
+      if (tid == 0) urf = __ldg(P.uniforms_resample + b);
+    }
+    constexpr int kPer = kDecideRecs / (kDecideWarps * 32);
+    uint2 v[kPer];
+    if (all_at_once) {
+      const uint2* base = P.part + static_cast<size_t>(b) * R * NC;
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int i = k * kDecideWarps * 32 + tid;
+        if (i < nrows * NC) {
+          const int r = i / NC;
+          const int row = r < nt ? r : K + 1 + (r - nt);
+          v[k] = __ldcg(base + static_cast<size_t>(row) * NC + (i - r * NC));
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int i = k * kDecideWarps * 32 + tid;
+        if (i < nrows * NC) D.rec[i] = v[k];
+      }
+    }
+    if (tid < 32) {
+      if (tid < SPECV_MAX_DRAFT) {
+        D.x[tid] = xi;
+        D.zp[tid] = zpf;
+        D.zq[tid] = zqf;
+      }
+      if (tid <= SPECV_MAX_DRAFT) D.u[tid] = uf;
+      if (tid == 0) D.ur = urf;
     }
   }
-  for (int r = warp; r < nt + nd; r += kDecideWarps) {
-    const int row = r < nt ? r : K + 1 + (r - nt);
-    float M, S;
-    int arg;
-    uint2* rec = D.rec[warp];
-    __syncwarp();
-    stage_rec(rec, P.part + (static_cast<size_t>(b) * R + row) * NC, NC, lane);
-    const bool bonus_row = !greedy && r == n;
-    if (bonus_row) {   // row n: the kept sweep sums too, loaded while the row combines
-      const float* bs = P.bsw + static_cast<size_t>(b) * NC * kChunkSweeps;
-      for (int i = lane; i < NC * kChunkSweeps; i += 32) D.sw[i] = __ldcg(bs + i);
+  __syncthreads();
+  if (all_at_once) {
+    // a group of 8 lanes per row, 16 rows at a time
+    const int sub = lane & 7;
+    for (int base = warp * 4; base < nrows; base += kDecideWarps * 4) {
+      const int r = base + (lane >> 3);
+      float M, S;
+      int arg;
+      combine_row_group(D.rec + r * NC, NC, r < nrows, greedy, sT, sub, M, S, arg);
+      if (r < nrows) {
+        if (sub == 0) {
+          D.M[r] = M;
+          D.S[r] = S;
+          D.arg[r] = arg;
+        }
+        if (!greedy && r == n) {   // the bonus draw's chunk masses, ready before the decision
+          const uint2* rec = D.rec + r * NC;
+          for (int c = sub; c < NC; c += 8) {
+            const float m = __uint_as_float(rec[c].x);
+            D.mass[c] = m > -INFINITY ? __fmul_rn(__uint_as_float(rec[c].y), scaled_exp(m, M, sT)) : 0.0f;
+          }
+        }
+      }
     }
-    combine_row_warp(rec, NC, greedy, sT, lane, M, S, arg);
-    if (lane == 0) {
-      D.M[r] = M;
-      D.S[r] = S;
-      D.arg[r] = arg;
-    }
-    if (bonus_row) {   // the bonus draw's chunk masses, ready before the decision
-      for (int c = lane; c < NC; c += 32) {
-        const float m = __uint_as_float(rec[c].x);
-        D.mass[c] = m > -INFINITY ? __fmul_rn(__uint_as_float(rec[c].y), scaled_exp(m, M, sT)) : 0.0f;
+  } else {
+    for (int r = warp; r < nrows; r += kDecideWarps) {
+      const int row = r < nt ? r : K + 1 + (r - nt);
+      float M, S;
+      int arg;
+      uint2* rec = D.rec + warp * kMaxChunks;
+      __syncwarp();
+      stage_rec(rec, P.part + (static_cast<size_t>(b) * R + row) * NC, NC, lane);
+      combine_row_warp(rec, NC, greedy, sT, lane, M, S, arg);
+      if (lane == 0) {
+        D.M[r] = M;
+        D.S[r] = S;
+        D.arg[r] = arg;
+      }
+      if (!greedy && r == n) {
+        for (int c = lane; c < NC; c += 32) {
+          const float m = __uint_as_float(rec[c].x);
+          D.mass[c] = m > -INFINITY ? __fmul_rn(__uint_as_float(rec[c].y), scaled_exp(m, M, sT)) : 0.0f;
+        }
       }
     }
   }
   __syncthreads();
   if (warp != 0) return;
+  const int x_lane = lane < n ? D.x[lane] : -1;
+  const float u_lane = lane <= n ? D.u[lane] : 0.0f;
+  const float ur = D.ur;
+  const float zp = lane < n ? D.zp[lane] : 0.0f;
+  const float zq = lane < n ? D.zq[lane] : 0.0f;
 
   float Mp_l = -INFINITY, Sp_l = 0.0f, Mq_l = -INFINITY, Sq_l = 0.0f;
   int g = INT_MAX;
@@ -1433,9 +1483,9 @@ __device__ void decide_request(const Params& P, DecideSmem& D, int b) {
   float lp = 0.0f, lq = 0.0f;
   bool accept = false;
   if (lane < n) {
-    lp = __fsub_rn(__fmul_rn(__fsub_rn(zp, Mp_l), sT), log2f(Sp_l));
-    lq = __fsub_rn(__fmul_rn(__fsub_rn(zq, Mq_l), sT), log2f(Sq_l));
-    accept = __fadd_rn(log2f(u_lane), lq) < lp;
+    lp = __fsub_rn(__fmul_rn(__fsub_rn(zp, Mp_l), sT), __log2f(Sp_l));
+    lq = __fsub_rn(__fmul_rn(__fsub_rn(zq, Mq_l), sT), __log2f(Sq_l));
+    accept = __fadd_rn(__log2f(u_lane), lq) < lp;
   }
   const unsigned rej = __ballot_sync(0xffffffffu, lane < n && !accept);
   const int j = rej ? __ffs(rej) - 1 : n;
@@ -1466,28 +1516,72 @@ __device__ void decide_request(const Params& P, DecideSmem& D, int b) {
     write_outputs(P, b, j, -1, x_lane, lane);   // the residual kernel writes the token
     return;
   }
-  // every draft accepted: the bonus token from p_n with uniforms[b, n]
+  // every draft accepted: the bonus token from p_n with uniforms[b, n]: the
+  // chunk from row n's chunk masses, then the chunk read once more: its
+  // sweep sums, the sweep, the element
   constexpr int CH = Elt<DT>::kPerVec;
   const float u = __shfl_sync(0xffffffffu, u_lane, n);
-  const uint2* rec_n = P.part + (static_cast<size_t>(b) * R + n) * NC;
   float W, rem;
   const int chunk = pick_chunk(D.mass, NC, u, lane, W, rem);
   int tok = -1;
   if (chunk >= 0) {
-    const float f = scaled_exp(__uint_as_float(__ldcg(rec_n + chunk).x), Mp, sT);
-    const float sw = lane < kChunkSweeps ? __fmul_rn(D.sw[chunk * kChunkSweeps + lane], f) : 0.0f;
-    float rem2 = 0.0f;
-    const int sweep = pick_lane(sw, kChunkSweeps, rem, lane, rem2);
-    if (sweep >= 0) {
-      const Chunk kp = chunk_of<DT>(target_row<DT>(P, b, n), V, chunk, kChunkBytes);
-      const int jv = sweep * 32 + lane;
-      float v[CH], w[CH];
-      global_vec<DT>(kp, P.t_lo, P.t_hi, jv, v);
-      const float4 prm = make_float4(Mp, 0.0f, sT, 0.0f);
+    const Chunk kp = chunk_of<DT>(target_row<DT>(P, b, n), V, chunk, kChunkBytes);
+    const float4 prm = make_float4(Mp, 0.0f, sT, 0.0f);
+    // every 16-byte vector of the chunk copied at once into the staging
+    // area (free after the combine) with cp.async; the few partly outside
+    // the chunk (row edges) are read element by element
+    uint4* stage = reinterpret_cast<uint4*>(D.rec);
+    unsigned whole = 0u;
+#pragma unroll
+    for (int s = 0; s < kChunkSweeps; ++s) {
+      const int jv = s * 32 + lane;
+      const int e0 = -kp.off0 / Elt<DT>::kBytes + jv * CH;
+      const uintptr_t a = kp.g0 + static_cast<uintptr_t>(jv) * 16;
+      const bool w = e0 >= kp.e_lo && e0 + CH <= kp.e_hi && a >= P.t_lo && a + 16 <= P.t_hi;
+      if (w) cp_async16(stage + jv, reinterpret_cast<const void*>(a));
+      whole |= static_cast<unsigned>(w) << s;
+    }
+    cp_async_wait_all();
+    __syncwarp();
+    // sweeps in order (one compact loop: this code runs once per call, cold),
+    // until the running mass passes the target; rounding that leaves it past
+    // the chunk's sweeps falls on the last positive one
+    float acc = 0.0f, rem2 = 0.0f;
+    int found = -1, last = -1;
+    float w[CH];
+#pragma unroll 1
+    for (int s = 0; s < kChunkSweeps; ++s) {
+      float v[CH];
+      if ((whole >> s) & 1u) Elt<DT>::unpack(stage[s * 32 + lane], v);
+      else global_vec<DT>(kp, P.t_lo, P.t_hi, s * 32 + lane, v);
+      float a = 0.0f;
+#pragma unroll
+      for (int q = 0; q < CH; ++q) {
+        w[q] = weight(v[q], 0.0f, false, prm);
+        a = __fadd_rn(a, w[q]);
+      }
+      const float ssum = warp_sum(a);
+      if (ssum > 0.0f) {
+        if (__fadd_rn(acc, ssum) > rem) {
+          found = s;
+          rem2 = __fsub_rn(rem, acc);
+          break;
+        }
+        last = s;
+      }
+      acc = __fadd_rn(acc, ssum);
+    }
+    if (found < 0 && last >= 0) {   // the last positive sweep, its last positive element
+      found = last;
+      rem2 = INFINITY;
+      float v[CH];
+      if ((whole >> last) & 1u) Elt<DT>::unpack(stage[last * 32 + lane], v);
+      else global_vec<DT>(kp, P.t_lo, P.t_hi, last * 32 + lane, v);
 #pragma unroll
       for (int q = 0; q < CH; ++q) w[q] = weight(v[q], 0.0f, false, prm);
-      tok = pick_in_sweep<CH>(w, rem2, -kp.off0 / Elt<DT>::kBytes + jv * CH, lane);
     }
+    if (found >= 0)
+      tok = pick_in_sweep<CH>(w, rem2, -kp.off0 / Elt<DT>::kBytes + (found * 32 + lane) * CH, lane);
   }
   if (rs && lane == 0) {
     rs[n * 8 + 6] = __fdiv_rn(W, Sp);
@@ -1580,8 +1674,7 @@ __device__ __forceinline__ void wait_previous() { asm volatile("griddepcontrol.w
 // ---------------------------------------------------------------- stats kernel
 
 // Whole warp: reduces the chunk in slot s to its record; the chunk holding
-// the row's drafted token also records that token's logit, and a sampled
-// request's row n also keeps its sweep sums.
+// the row's drafted token also records that token's logit.
 template <int DT>
 __device__ void consume_stats(const Params& P, Agent& ag, int s, const Item& it) {
   const int lane = ag.lane;
@@ -1590,10 +1683,7 @@ __device__ void consume_stats(const Params& P, Agent& ag, int s, const Item& it)
   const Chunk k = chunk_of<DT>(record_row_addr<DT>(P, it.b, it.row), P.V, it.c, kChunkBytes);
   fix_edges<DT>(k, is_draft ? P.d_lo : P.t_lo, is_draft ? P.d_hi : P.t_hi, slot, lane);
   float2 r;
-  if (it.bonus)
-    r = chunk_softmax_sweeps<DT>(slot, k, it.sT, lane,
-                                 P.bsw + (static_cast<size_t>(it.b) * P.NC + it.c) * kChunkSweeps);
-  else if (it.sT > 0.0f)
+  if (it.sT > 0.0f)
     r = chunk_softmax<DT>(slot, k, it.sT, lane);
   else
     r = chunk_argmax<DT>(slot, k, lane);
@@ -1692,7 +1782,7 @@ __global__ void __launch_bounds__(kThreads, 1) stats_kernel(const Params P) {
 // ---------------------------------------------------------------- decide kernel
 
 template <int DT>
-__global__ void __launch_bounds__(kDecideWarps * 32) decide_kernel(const Params P) {
+__global__ void __launch_bounds__(kDecideWarps * 32, 4) decide_kernel(const Params P) {
   __shared__ DecideSmem D;
   wait_previous();
   allow_dependents();
@@ -1849,7 +1939,7 @@ __global__ void __launch_bounds__(kDecideWarps * 32) search_kernel(const Params 
 int elt_bytes(specv_dtype dt) { return dt == SPECV_BF16 ? 2 : 4; }
 
 struct Layout {
-  size_t header, req, part, zx, rlist, dmass, dsw, bsw, total;
+  size_t header, req, part, zx, rlist, dmass, dsw, total;
 };
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
@@ -1876,8 +1966,7 @@ Layout ws_layout(int B, int K, int V, specv_dtype dt) {
   L.rlist = align256(L.zx + sizeof(float) * Bl * R);
   L.dmass = align256(L.rlist + sizeof(int32_t) * Bl);
   L.dsw = align256(L.dmass + sizeof(float) * Bl * NCd);
-  L.bsw = align256(L.dsw + sizeof(float) * Bl * NCd * kDrawSweeps);
-  L.total = align256(L.bsw + sizeof(float) * Bl * NC * kChunkSweeps);
+  L.total = align256(L.dsw + sizeof(float) * Bl * NCd * kDrawSweeps);
   return L;
 }
 
@@ -2025,7 +2114,6 @@ specv_status launch(const void* target, const void* draft, specv_dtype dtype,
     P.rlist = reinterpret_cast<int32_t*>(ws + L.rlist);
     P.dmass = reinterpret_cast<float*>(ws + L.dmass);
     P.dsw = reinterpret_cast<float*>(ws + L.dsw);
-    P.bsw = reinterpret_cast<float*>(ws + L.bsw);
     P.row_stats = row_stats ? row_stats + static_cast<size_t>(b0) * (K + 1) * 8 : nullptr;
     const cudaError_t e = dtype == SPECV_BF16 ? launch_sequence<SPECV_BF16>(P, grid, stream)
                                               : launch_sequence<SPECV_F32>(P, grid, stream);
