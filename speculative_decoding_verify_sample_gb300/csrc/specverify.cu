@@ -1,5 +1,5 @@
 // libspecverify: the speculative-decoding verification sampler for GB300
-// (sm_103a).  One persistent kernel does the whole step.
+// (sm_103a), as four kernels on the caller's stream.
 //
 // The rule ("Decodificación Especulativa y EAGLE", Phase 10 - Lesson 25,
 // sections "El Concepto", "La Regla de Exactitud", "Caso codicioso"): for
@@ -20,13 +20,15 @@
 //     reduced to a record: its maximum and sum of
 //     exp((z - max)/T), or at T = 0 its maximum and lowest argmax.  The
 //     chunk holding a drafted token also records that token's logit.
-//  2. decide_kernel, one warp per request, combines the records, runs the
+//  2. decide_kernel, one CTA per request, combines the records, runs the
 //     left-to-right accept test (or the greedy comparison) and writes the
-//     outputs.  A bonus draw is taken here: the chunk from the row's
-//     records, the token from one re-read chunk.  A rejected sampled
-//     request is appended to a list for the residual draw.
+//     outputs.  A request whose drafts are all accepted gets its bonus
+//     draw's chunk here (from row n's records) and joins a bonus list; a
+//     rejected sampled request joins the residual list.
 //  3. residual_kernel reads the rejected rows again (target and draft, in
 //     3 KB pieces) and sums (p - q)+ per piece and per 512-byte sweep.
+//     Warps of its own take the bonus draws meanwhile: the listed chunk
+//     read once more, walked sweep by sweep to the token.
 //  4. search_kernel, one warp per listed request, draws its token: the
 //     piece from the piece sums, the sweep from that piece's sweep sums,
 //     the token from the sweep of both rows read again.
@@ -72,9 +74,9 @@ static_assert(kMaxChunks < 512, "a stats chunk index fits 9 bits");
 static_assert(kPlanMax <= 1024 && 2 * SPECV_MAX_DRAFT + 1 < 64, "a request fits 10 bits, a row 6");
 
 // workspace header words (int32 index), one 128-byte line each
-constexpr int kHStatus = 0, kHResid = 96, kHExit4 = 128;
+constexpr int kHStatus = 0, kHResid = 96, kHExit4 = 128, kHBonus = 160;
 constexpr int kHeaderBytes = 1024;
-static_assert((kHExit4 + 1) * 4 <= kHeaderBytes, "header words fit the header");
+static_assert((kHBonus + 1) * 4 <= kHeaderBytes, "header words fit the header");
 
 
 
@@ -86,10 +88,11 @@ constexpr float kLn2 = 0.6931471805599453f;
 // Per-request state in the workspace (32 bytes): the residual draw's
 // parameters, written by the decision.
 struct __align__(16) Req {
-  int j;          // the rejected row
+  int j;          // the rejected row (a bonus draw: n)
   float Sp_j;     // S_p of the rejected row
-  int pad[2];
-  float4 prm;     // Mp, Mq, log2(e)/T, S_p/S_q of the rejected row
+  int chunk;      // a bonus draw: its chunk of row n
+  float rem;      // a bonus draw: the target mass left at that chunk
+  float4 prm;     // Mp, Mq, log2(e)/T, S_p/S_q of the rejected row (a bonus draw: Mp, 0, log2(e)/T, 0)
 };
 static_assert(sizeof(Req) == 32, "Req is one 32-byte record");
 
@@ -1311,18 +1314,43 @@ __device__ __forceinline__ void combine_row_group(const uint2* rec, int NC, bool
 // t <= n, draft rows t < n when sampled); warp 0 then takes the decision.
 // Greedy: the argmax of target rows t <= n against the drafts.  Sampled:
 // the left-to-right test u_t q(x_t) < p(x_t) in log2 form; every draft
-// accepted draws the bonus token from p_n here (the chunk from row n's
-// records, then that chunk read once more for its sweep sums, the sweep
-// and the element); a rejection at j stores the residual draw's parameters
-// and lists the request for the residual kernel, which writes
-// out_tokens[b, j].
+// accepted picks the bonus draw's chunk from row n's records and lists the
+// request for a bonus walk; a rejection at j stores the residual draw's
+// parameters and lists the request for the residual draw.  Either list's
+// kernel writes out_tokens[b, n] / out_tokens[b, j].
+// A decide CTA's view of request b's own inputs (the caller's buffers):
+// length, temperature, their status bits, and for the threads of warp 0 a
+// drafted token (lane t < n), a uniform (lane t <= n), the resample uniform
+// (lane 0).  Read before waiting on the stats kernel.
+struct DecideIn {
+  int n, bad, x;
+  float T, u, ur;
+};
+
+__device__ __forceinline__ DecideIn decide_inputs(const Params& P, int b) {
+  const int tid = threadIdx.x, K = P.K;
+  DecideIn in;
+  in.n = request_len(P, b);
+  in.T = __ldg(P.temperature + b);
+  in.bad = request_bad(P, in.n, in.T);
+  in.x = -1;
+  in.u = 0.0f;
+  in.ur = 0.0f;
+  if (!in.bad && tid < 32) {
+    if (tid < in.n) in.x = __ldg(P.draft_tokens + static_cast<size_t>(b) * K + tid);
+    if (tid <= in.n) in.u = __ldg(P.uniforms + static_cast<size_t>(b) * (K + 1) + tid);
+    if (tid == 0) in.ur = __ldg(P.uniforms_resample + b);
+  }
+  return in;
+}
+
 template <int DT>
-__device__ void decide_request(const Params& P, DecideSmem& D, int b) {
+__device__ void decide_request(const Params& P, DecideSmem& D, int b, const DecideIn& in) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K = P.K, V = P.V, R = P.R, NC = P.NC;
-  const int n = request_len(P, b);
-  const float T = __ldg(P.temperature + b);
-  int bad = request_bad(P, n, T);
+  const int n = in.n;
+  const float T = in.T;
+  int bad = in.bad;
   if (bad) {
     if (warp == 0) {
       if (lane == 0) atomicOr(P.header + kHStatus, bad);
@@ -1340,16 +1368,10 @@ __device__ void decide_request(const Params& P, DecideSmem& D, int b) {
   const int nrows = nt + nd;
   const bool all_at_once = nrows * NC <= kDecideRecs;
   {
-    int xi = -1;
-    float uf = 0.0f, zpf = 0.0f, zqf = 0.0f, urf = 0.0f;
-    if (tid < 32) {
-      if (tid < n) xi = __ldg(P.draft_tokens + static_cast<size_t>(b) * K + tid);
-      if (tid <= n) uf = __ldg(P.uniforms + static_cast<size_t>(b) * (K + 1) + tid);
-      if (!greedy && tid < n) {
-        zpf = __ldcg(P.zx + static_cast<size_t>(b) * R + tid);
-        zqf = __ldcg(P.zx + static_cast<size_t>(b) * R + K + 1 + tid);
-      }
-      if (tid == 0) urf = __ldg(P.uniforms_resample + b);
+    float zpf = 0.0f, zqf = 0.0f;
+    if (!greedy && tid < n) {
+      zpf = __ldcg(P.zx + static_cast<size_t>(b) * R + tid);
+      zqf = __ldcg(P.zx + static_cast<size_t>(b) * R + K + 1 + tid);
     }
     constexpr int kPer = kDecideRecs / (kDecideWarps * 32);
     uint2 v[kPer];
@@ -1372,12 +1394,12 @@ __device__ void decide_request(const Params& P, DecideSmem& D, int b) {
     }
     if (tid < 32) {
       if (tid < SPECV_MAX_DRAFT) {
-        D.x[tid] = xi;
+        D.x[tid] = in.x;
         D.zp[tid] = zpf;
         D.zq[tid] = zqf;
       }
-      if (tid <= SPECV_MAX_DRAFT) D.u[tid] = uf;
-      if (tid == 0) D.ur = urf;
+      if (tid <= SPECV_MAX_DRAFT) D.u[tid] = in.u;
+      if (tid == 0) D.ur = in.ur;
     }
   }
   __syncthreads();
@@ -1516,83 +1538,108 @@ __device__ void decide_request(const Params& P, DecideSmem& D, int b) {
     write_outputs(P, b, j, -1, x_lane, lane);   // the residual kernel writes the token
     return;
   }
-  // every draft accepted: the bonus token from p_n with uniforms[b, n]: the
-  // chunk from row n's chunk masses, then the chunk read once more: its
-  // sweep sums, the sweep, the element
-  constexpr int CH = Elt<DT>::kPerVec;
+  // every draft accepted: the bonus token from p_n with uniforms[b, n].  The
+  // chunk is picked here from row n's chunk masses; the residual kernel
+  // walks that chunk to the token and writes out_tokens[b, n].
   const float u = __shfl_sync(0xffffffffu, u_lane, n);
   float W, rem;
   const int chunk = pick_chunk(D.mass, NC, u, lane, W, rem);
-  int tok = -1;
-  if (chunk >= 0) {
-    const Chunk kp = chunk_of<DT>(target_row<DT>(P, b, n), V, chunk, kChunkBytes);
-    const float4 prm = make_float4(Mp, 0.0f, sT, 0.0f);
-    // every 16-byte vector of the chunk copied at once into the staging
-    // area (free after the combine) with cp.async; the few partly outside
-    // the chunk (row edges) are read element by element
-    uint4* stage = reinterpret_cast<uint4*>(D.rec);
-    unsigned whole = 0u;
-#pragma unroll
-    for (int s = 0; s < kChunkSweeps; ++s) {
-      const int jv = s * 32 + lane;
-      const int e0 = -kp.off0 / Elt<DT>::kBytes + jv * CH;
-      const uintptr_t a = kp.g0 + static_cast<uintptr_t>(jv) * 16;
-      const bool w = e0 >= kp.e_lo && e0 + CH <= kp.e_hi && a >= P.t_lo && a + 16 <= P.t_hi;
-      if (w) cp_async16(stage + jv, reinterpret_cast<const void*>(a));
-      whole |= static_cast<unsigned>(w) << s;
-    }
-    cp_async_wait_all();
-    __syncwarp();
-    // sweeps in order (one compact loop: this code runs once per call, cold),
-    // until the running mass passes the target; rounding that leaves it past
-    // the chunk's sweeps falls on the last positive one
-    float acc = 0.0f, rem2 = 0.0f;
-    int found = -1, last = -1;
-    float w[CH];
-#pragma unroll 1
-    for (int s = 0; s < kChunkSweeps; ++s) {
-      float v[CH];
-      if ((whole >> s) & 1u) Elt<DT>::unpack(stage[s * 32 + lane], v);
-      else global_vec<DT>(kp, P.t_lo, P.t_hi, s * 32 + lane, v);
-      float a = 0.0f;
-#pragma unroll
-      for (int q = 0; q < CH; ++q) {
-        w[q] = weight(v[q], 0.0f, false, prm);
-        a = __fadd_rn(a, w[q]);
-      }
-      const float ssum = warp_sum(a);
-      if (ssum > 0.0f) {
-        if (__fadd_rn(acc, ssum) > rem) {
-          found = s;
-          rem2 = __fsub_rn(rem, acc);
-          break;
-        }
-        last = s;
-      }
-      acc = __fadd_rn(acc, ssum);
-    }
-    if (found < 0 && last >= 0) {   // the last positive sweep, its last positive element
-      found = last;
-      rem2 = INFINITY;
-      float v[CH];
-      if ((whole >> last) & 1u) Elt<DT>::unpack(stage[last * 32 + lane], v);
-      else global_vec<DT>(kp, P.t_lo, P.t_hi, last * 32 + lane, v);
-#pragma unroll
-      for (int q = 0; q < CH; ++q) w[q] = weight(v[q], 0.0f, false, prm);
-    }
-    if (found >= 0)
-      tok = pick_in_sweep<CH>(w, rem2, -kp.off0 / Elt<DT>::kBytes + (found * 32 + lane) * CH, lane);
-  }
   if (rs && lane == 0) {
     rs[n * 8 + 6] = __fdiv_rn(W, Sp);
-    rs[n * 8 + 7] = static_cast<float>(tok);
+    if (chunk < 0) rs[n * 8 + 7] = -1.0f;
   }
-  if (tok < 0 || tok >= V) {
+  if (chunk < 0) {
     if (lane == 0) atomicOr(P.header + kHStatus, SPECV_DEV_BAD_ROW);
     write_outputs(P, b, -1, -1, x_lane, lane);
-  } else {
-    write_outputs(P, b, n, tok, x_lane, lane);
+    return;
   }
+  if (lane == 0) {
+    Req* q = P.req + b;
+    q->j = n;
+    q->chunk = chunk;
+    q->rem = rem;
+    q->prm = make_float4(Mp, 0.0f, sT, 0.0f);
+    P.rlist[P.B - 1 - atomicAdd(P.header + kHBonus, 1)] = b;   // the bonus list grows down
+  }
+  write_outputs(P, b, n, -1, x_lane, lane);
+}
+
+// Whole warp: the bonus token of listed request b (every draft accepted):
+// the decision's chunk of target row n copied into `stage` (16-byte
+// aligned, kChunkBytes), then its sweeps walked in order until the running
+// mass of p passes the target left at the chunk.  Rounding that leaves the
+// target past the chunk's sweeps falls on the last positive one.  Writes
+// out_tokens[b, n], or -1 throughout (status bit) when nothing is drawn.
+template <int DT>
+__device__ void bonus_draw(const Params& P, uint4* stage, int b, int lane) {
+  constexpr int CH = Elt<DT>::kPerVec;
+  const int K = P.K, V = P.V;
+  const Req* rq = P.req + b;
+  const int n = __ldcg(&rq->j), chunk = __ldcg(&rq->chunk);
+  const float rem = __ldcg(&rq->rem);
+  const float4 prm = __ldcg(&rq->prm);
+  const Chunk kp = chunk_of<DT>(target_row<DT>(P, b, n), V, chunk, kChunkBytes);
+  // every 16-byte vector of the chunk copied at once into the staging area
+  // with cp.async; the few partly outside the chunk (row edges) are read
+  // element by element
+  unsigned whole = 0u;
+#pragma unroll
+  for (int s = 0; s < kChunkSweeps; ++s) {
+    const int jv = s * 32 + lane;
+    const int e0 = -kp.off0 / Elt<DT>::kBytes + jv * CH;
+    const uintptr_t a = kp.g0 + static_cast<uintptr_t>(jv) * 16;
+    const bool in = e0 >= kp.e_lo && e0 + CH <= kp.e_hi && a >= P.t_lo && a + 16 <= P.t_hi;
+    if (in) cp_async16(stage + jv, reinterpret_cast<const void*>(a));
+    whole |= static_cast<unsigned>(in) << s;
+  }
+  cp_async_wait_all();
+  __syncwarp();
+  // sweeps in order (one compact loop: it runs once per request, cold)
+  float acc = 0.0f, rem2 = 0.0f;
+  int found = -1, last = -1;
+  float w[CH];
+#pragma unroll 1
+  for (int s = 0; s < kChunkSweeps; ++s) {
+    float v[CH];
+    if ((whole >> s) & 1u) Elt<DT>::unpack(stage[s * 32 + lane], v);
+    else global_vec<DT>(kp, P.t_lo, P.t_hi, s * 32 + lane, v);
+    float a = 0.0f;
+#pragma unroll
+    for (int q = 0; q < CH; ++q) {
+      w[q] = weight(v[q], 0.0f, false, prm);
+      a = __fadd_rn(a, w[q]);
+    }
+    const float ssum = warp_sum(a);
+    if (ssum > 0.0f) {
+      if (__fadd_rn(acc, ssum) > rem) {
+        found = s;
+        rem2 = __fsub_rn(rem, acc);
+        break;
+      }
+      last = s;
+    }
+    acc = __fadd_rn(acc, ssum);
+  }
+  if (found < 0 && last >= 0) {   // the last positive sweep, its last positive element
+    found = last;
+    rem2 = INFINITY;
+    float v[CH];
+    if ((whole >> last) & 1u) Elt<DT>::unpack(stage[last * 32 + lane], v);
+    else global_vec<DT>(kp, P.t_lo, P.t_hi, last * 32 + lane, v);
+#pragma unroll
+    for (int q = 0; q < CH; ++q) w[q] = weight(v[q], 0.0f, false, prm);
+  }
+  const int tok = found >= 0 ? pick_in_sweep<CH>(w, rem2, -kp.off0 / Elt<DT>::kBytes + (found * 32 + lane) * CH, lane)
+                             : -1;
+  if (P.row_stats && lane == 0)
+    P.row_stats[(static_cast<size_t>(b) * (K + 1) + n) * 8 + 7] = static_cast<float>(tok);
+  if (tok < 0 || tok >= V) {
+    if (lane == 0) atomicOr(P.header + kHStatus, SPECV_DEV_BAD_ROW);
+    write_outputs(P, b, -1, -1, -1, lane);
+  } else if (lane == 0) {
+    P.out_tokens[static_cast<size_t>(b) * (K + 1) + n] = tok;
+  }
+  __syncwarp();
 }
 
 // Whole warp: the residual draw of listed request b (entry e, rejected at
@@ -1784,10 +1831,14 @@ __global__ void __launch_bounds__(kThreads, 1) stats_kernel(const Params P) {
 template <int DT>
 __global__ void __launch_bounds__(kDecideWarps * 32, 4) decide_kernel(const Params P) {
   __shared__ DecideSmem D;
+  // the first request's own inputs are fetched while the stats kernel runs
+  int b = static_cast<int>(blockIdx.x);
+  DecideIn in = decide_inputs(P, min(b, P.B - 1));
   wait_previous();
   allow_dependents();
-  for (int b = blockIdx.x; b < P.B; b += gridDim.x) {
-    decide_request<DT>(P, D, b);
+  for (; b < P.B; b += gridDim.x) {
+    if (b != static_cast<int>(blockIdx.x)) in = decide_inputs(P, b);
+    decide_request<DT>(P, D, b, in);
     __syncthreads();
   }
 }
@@ -1873,10 +1924,19 @@ __global__ void __launch_bounds__(kThreads, 1) residual_kernel(const Params P) {
   ag.lane = lane;
   allow_dependents();
   const int count = __ldcg(P.header + kHResid);
+  const int nb = __ldcg(P.header + kHBonus);
   const int total = count * P.NCd;
   const int G = static_cast<int>(gridDim.x) * kAgents;
-  const int first = static_cast<int>(blockIdx.x) * kAgents + warp;
-  const int mine_n = first < total ? (total - first + G - 1) / G : 0;   // this warp's items
+  const int gw = static_cast<int>(blockIdx.x) * kAgents + warp;
+  // the bonus draws first, a warp each (slot 0 of its ring as staging); the
+  // residual items go to the other warps (to every warp when the bonus
+  // draws take them all)
+  for (int k = gw; k < nb; k += G)
+    bonus_draw<DT>(P, reinterpret_cast<uint4*>(ag.slot(0)), __ldcg(P.rlist + P.B - 1 - k), lane);
+  if (gw < nb) fence_proxy_async_smem();   // staging writes before bulk copies into the slot
+  const int Gr = nb < G ? G - nb : G;
+  const int first = nb < G ? gw - nb : gw;
+  const int mine_n = first >= 0 && first < total ? (total - first + Gr - 1) / Gr : 0;
   Item mine = residual_pick_init();
   int base = -64;
   int issued = 0, consumed = 0;
@@ -1884,7 +1944,7 @@ __global__ void __launch_bounds__(kThreads, 1) residual_kernel(const Params P) {
     while (issued - consumed < kSlots && issued < mine_n) {
       if (issued >= base + 32) {   // decode the next 32 of this warp's items, one per lane
         base = issued;
-        const int i = first + (base + lane) * G;
+        const int i = first + (base + lane) * Gr;
         if (i < total) mine = residual_item(P, i);
       }
       const Item it = residual_pick(mine, issued - base);
@@ -1928,7 +1988,8 @@ __global__ void __launch_bounds__(kDecideWarps * 32) search_kernel(const Params 
     const int prev = atomicAdd(P.header + kHExit4, 1);
     if (prev == static_cast<int>(gridDim.x) - 1) {
       P.header[kHExit4] = 0;
-      P.header[kHResid] = 0;   // the list is used up: empty for the next call
+      P.header[kHResid] = 0;   // the lists are used up: empty for the next call
+      P.header[kHBonus] = 0;
     }
   }
 }
