@@ -85,13 +85,14 @@ constexpr int kItemA = 1, kItemR = 3;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-// Per-request state in the workspace (32 bytes): the residual draw's
-// parameters, written by the decision.
+// A listed draw (32 bytes), written by the decision: entry e of the
+// residual list (e counted up from 0) or of the bonus list (counted down
+// from B - 1), so the draw's kernel reads everything it needs at once.
 struct __align__(16) Req {
+  int b;          // the request
   int j;          // the rejected row (a bonus draw: n)
-  float Sp_j;     // S_p of the rejected row
+  float aux;      // residual: S_p of the rejected row; bonus: the target mass left at its chunk
   int chunk;      // a bonus draw: its chunk of row n
-  float rem;      // a bonus draw: the target mass left at that chunk
   float4 prm;     // Mp, Mq, log2(e)/T, S_p/S_q of the rejected row (a bonus draw: Mp, 0, log2(e)/T, 0)
 };
 static_assert(sizeof(Req) == 32, "Req is one 32-byte record");
@@ -114,10 +115,9 @@ struct Params {
   int32_t* accepted_len;
   int32_t* out_tokens;
   int32_t* header;
-  Req* req;         // [B]
+  Req* req;         // [B] listed draws (counts: header[kHResid], header[kHBonus])
   uint2* part;      // [B][R][NC] chunk records: (max, sum) or (max, index)
   float* zx;        // [B][R] the drafted token's logit in rows t < n
-  int32_t* rlist;   // [B] requests waiting for a residual draw (count: header[kHResid])
   float* dmass;     // [B][NCd] residual sums of the pieces (by list entry)
   float* dsw;       // [B][NCd][kDrawSweeps] residual sums of their sweeps
   float* row_stats; // [B][K+1][8] or null
@@ -1197,6 +1197,22 @@ constexpr int kDecideRecs = 1024;   // records a decide CTA stages at once
 constexpr int kDecideBuf = kDecideRecs > kDecideWarps * kMaxChunks ? kDecideRecs
                                                                     : kDecideWarps * kMaxChunks;
 
+// One lane: a listed draw's record, written / read as two 16-byte words.
+__device__ __forceinline__ void store_req(Req* p, int b, int j, float aux, int chunk, float4 prm) {
+  *reinterpret_cast<int4*>(p) = make_int4(b, j, __float_as_int(aux), chunk);
+  p->prm = prm;
+}
+__device__ __forceinline__ Req load_req(const Req* p) {
+  const int4 a = __ldcg(reinterpret_cast<const int4*>(p));
+  Req r;
+  r.b = a.x;
+  r.j = a.y;
+  r.aux = __int_as_float(a.z);
+  r.chunk = a.w;
+  r.prm = __ldcg(&p->prm);
+  return r;
+}
+
 // The decision kernel's shared memory: one request's combined rows.
 struct DecideSmem {
   float M[kMaxRows], S[kMaxRows];   // row r: maximum (raw logit) and sum, or the argmax value
@@ -1529,11 +1545,8 @@ __device__ void decide_request(const Params& P, DecideSmem& D, int b, const Deci
     const float Mq = __shfl_sync(0xffffffffu, Mq_l, j);
     const float Sq = __shfl_sync(0xffffffffu, Sq_l, j);
     if (lane == 0) {
-      Req* q = P.req + b;
-      q->j = j;
-      q->Sp_j = Sp;
-      q->prm = make_float4(Mp, Mq, sT, __fdiv_rn(Sp, Sq));
-      P.rlist[atomicAdd(P.header + kHResid, 1)] = b;
+      store_req(P.req + atomicAdd(P.header + kHResid, 1), b, j, Sp, 0,
+                make_float4(Mp, Mq, sT, __fdiv_rn(Sp, Sq)));
     }
     write_outputs(P, b, j, -1, x_lane, lane);   // the residual kernel writes the token
     return;
@@ -1554,30 +1567,25 @@ __device__ void decide_request(const Params& P, DecideSmem& D, int b, const Deci
     return;
   }
   if (lane == 0) {
-    Req* q = P.req + b;
-    q->j = n;
-    q->chunk = chunk;
-    q->rem = rem;
-    q->prm = make_float4(Mp, 0.0f, sT, 0.0f);
-    P.rlist[P.B - 1 - atomicAdd(P.header + kHBonus, 1)] = b;   // the bonus list grows down
+    store_req(P.req + (P.B - 1 - atomicAdd(P.header + kHBonus, 1)), b, n, rem, chunk,
+              make_float4(Mp, 0.0f, sT, 0.0f));   // the bonus list grows down
   }
   write_outputs(P, b, n, -1, x_lane, lane);
 }
 
-// Whole warp: the bonus token of listed request b (every draft accepted):
+// Whole warp: the bonus token of listed draw r (every draft accepted):
 // the decision's chunk of target row n copied into `stage` (16-byte
 // aligned, kChunkBytes), then its sweeps walked in order until the running
 // mass of p passes the target left at the chunk.  Rounding that leaves the
 // target past the chunk's sweeps falls on the last positive one.  Writes
 // out_tokens[b, n], or -1 throughout (status bit) when nothing is drawn.
 template <int DT>
-__device__ void bonus_draw(const Params& P, uint4* stage, int b, int lane) {
+__device__ void bonus_draw(const Params& P, uint4* stage, const Req& r, int lane) {
   constexpr int CH = Elt<DT>::kPerVec;
   const int K = P.K, V = P.V;
-  const Req* rq = P.req + b;
-  const int n = __ldcg(&rq->j), chunk = __ldcg(&rq->chunk);
-  const float rem = __ldcg(&rq->rem);
-  const float4 prm = __ldcg(&rq->prm);
+  const int b = r.b, n = r.j, chunk = r.chunk;
+  const float rem = r.aux;
+  const float4 prm = r.prm;
   const Chunk kp = chunk_of<DT>(target_row<DT>(P, b, n), V, chunk, kChunkBytes);
   // every 16-byte vector of the chunk copied at once into the staging area
   // with cp.async; the few partly outside the chunk (row edges) are read
@@ -1652,9 +1660,9 @@ template <int DT>
 __device__ void residual_search(const Params& P, Agent& ag, int e) {
   constexpr int CH = Elt<DT>::kPerVec;
   const int lane = ag.lane, K = P.K, V = P.V, NC = P.NC, NCd = P.NCd;
-  const int b = __ldcg(P.rlist + e);
-  const int j = __ldcg(&P.req[b].j);
-  const float4 prm = __ldcg(&P.req[b].prm);
+  const Req r = load_req(P.req + e);
+  const int b = r.b, j = r.j;
+  const float4 prm = r.prm;
   float* mass = reinterpret_cast<float*>(ag.slot(0));
   const float* dm = P.dmass + static_cast<size_t>(e) * NCd;
   __syncwarp();
@@ -1695,7 +1703,7 @@ __device__ void residual_search(const Params& P, Agent& ag, int e) {
   }
   if (P.row_stats && lane == 0) {
     float* rs = P.row_stats + (static_cast<size_t>(b) * (K + 1) + j) * 8;
-    rs[6] = __fdiv_rn(W, __ldcg(&P.req[b].Sp_j));
+    rs[6] = __fdiv_rn(W, r.aux);
     rs[7] = static_cast<float>(tok);
   }
   if (tok < 0 || tok >= V) {
@@ -1870,9 +1878,10 @@ __device__ __forceinline__ Item residual_item(const Params& P, int i) {
   it.kind = kItemR;
   it.c = i - e * P.NCd;
   it.n = e;
-  it.b = __ldcg(P.rlist + e);
-  it.row = __ldcg(&P.req[it.b].j);
-  it.prm = __ldcg(&P.req[it.b].prm);
+  const Req r = load_req(P.req + e);
+  it.b = r.b;
+  it.row = r.j;
+  it.prm = r.prm;
   it.sT = 0.0f;
   it.x = -1;
   it.bonus = 0;
@@ -1932,7 +1941,7 @@ __global__ void __launch_bounds__(kThreads, 1) residual_kernel(const Params P) {
   // residual items go to the other warps (to every warp when the bonus
   // draws take them all)
   for (int k = gw; k < nb; k += G)
-    bonus_draw<DT>(P, reinterpret_cast<uint4*>(ag.slot(0)), __ldcg(P.rlist + P.B - 1 - k), lane);
+    bonus_draw<DT>(P, reinterpret_cast<uint4*>(ag.slot(0)), load_req(P.req + (P.B - 1 - k)), lane);
   if (gw < nb) fence_proxy_async_smem();   // staging writes before bulk copies into the slot
   const int Gr = nb < G ? G - nb : G;
   const int first = nb < G ? gw - nb : gw;
@@ -2000,7 +2009,7 @@ __global__ void __launch_bounds__(kDecideWarps * 32) search_kernel(const Params 
 int elt_bytes(specv_dtype dt) { return dt == SPECV_BF16 ? 2 : 4; }
 
 struct Layout {
-  size_t header, req, part, zx, rlist, dmass, dsw, total;
+  size_t header, req, part, zx, dmass, dsw, total;
 };
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
@@ -2024,8 +2033,7 @@ Layout ws_layout(int B, int K, int V, specv_dtype dt) {
   L.req = kHeaderBytes;
   L.part = align256(L.req + sizeof(Req) * Bl);
   L.zx = align256(L.part + sizeof(uint2) * Bl * R * NC);
-  L.rlist = align256(L.zx + sizeof(float) * Bl * R);
-  L.dmass = align256(L.rlist + sizeof(int32_t) * Bl);
+  L.dmass = align256(L.zx + sizeof(float) * Bl * R);
   L.dsw = align256(L.dmass + sizeof(float) * Bl * NCd);
   L.total = align256(L.dsw + sizeof(float) * Bl * NCd * kDrawSweeps);
   return L;
@@ -2172,7 +2180,6 @@ specv_status launch(const void* target, const void* draft, specv_dtype dtype,
     P.req = reinterpret_cast<Req*>(ws + L.req);
     P.part = reinterpret_cast<uint2*>(ws + L.part);
     P.zx = reinterpret_cast<float*>(ws + L.zx);
-    P.rlist = reinterpret_cast<int32_t*>(ws + L.rlist);
     P.dmass = reinterpret_cast<float*>(ws + L.dmass);
     P.dsw = reinterpret_cast<float*>(ws + L.dsw);
     P.row_stats = row_stats ? row_stats + static_cast<size_t>(b0) * (K + 1) * 8 : nullptr;
