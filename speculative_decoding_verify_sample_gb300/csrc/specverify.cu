@@ -309,6 +309,40 @@ __device__ __forceinline__ float scaled_exp(float z, float m, float sT) {
   return ex2(__fmul_rn(__fsub_rn(z, m), sT));
 }
 
+// Pairs of fp32 values in one 64-bit register pair, for the two-wide FP32
+// instructions of the sm_100 family (add / sub / mul / fma .rn.f32x2).
+// Each half is rounded exactly as the scalar instruction rounds it, so a
+// paired computation gives the scalar one's bits.
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 pk2(float lo, float hi) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void up2(f32x2 v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f32x2 sub2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
 __device__ __forceinline__ float temp_scale(float T) { return __fdiv_rn(kLog2e, T); }
 
 // ---------------------------------------------------------------- reductions
@@ -726,11 +760,20 @@ __device__ __forceinline__ float2 chunk_softmax(const unsigned char* slot, const
   const float M = warp_max(m);
   if (!(M > -INFINITY)) return make_float2(M, 0.0f);
   const float c = __fmul_rn(M, sT);
-  // eight independent sums, two vectors per step, so the exponentials and
-  // the adds of different elements overlap
-  float s[8];
+  // eight independent sums s_0 .. s_7 (element q of a vector into s_(q mod
+  // 8), the second vector of a step after the first), two vectors per step,
+  // so the exponentials and the adds of different elements overlap; the
+  // sums are kept in pairs (s_2i, s_2i+1) and formed with the two-wide
+  // instructions: 2^(z s - c) of two elements per fma, two sums per add
+  const f32x2 sT2 = pk2(sT, sT), nc2 = pk2(-c, -c);
+  f32x2 s2[4];
 #pragma unroll
-  for (int q = 0; q < 8; ++q) s[q] = 0.0f;
+  for (int q = 0; q < 4; ++q) s2[q] = pk2(0.0f, 0.0f);
+  auto add_pair = [&](f32x2& acc, float z0, float z1) {
+    float x0, x1;
+    up2(fma2(pk2(z0, z1), sT2, nc2), x0, x1);
+    acc = add2(acc, pk2(ex2(x0), ex2(x1)));
+  };
   int j = vs.vf0 + lane;
 #pragma unroll 2
   for (; j + 32 < vs.vf1; j += 64) {
@@ -738,21 +781,24 @@ __device__ __forceinline__ float2 chunk_softmax(const unsigned char* slot, const
     E::unpack(vec[j], a);
     E::unpack(vec[j + 32], b);
 #pragma unroll
-    for (int q = 0; q < CH; ++q) {
-      s[q & 7] = __fadd_rn(s[q & 7], ex2(__fmaf_rn(a[q], sT, -c)));
-      s[(q + CH) & 7] = __fadd_rn(s[(q + CH) & 7], ex2(__fmaf_rn(b[q], sT, -c)));
+    for (int q = 0; q < CH; q += 2) {
+      add_pair(s2[(q & 7) >> 1], a[q], a[q + 1]);
+      add_pair(s2[((q + CH) & 7) >> 1], b[q], b[q + 1]);
     }
   }
   if (j < vs.vf1) {
     float a[CH];
     E::unpack(vec[j], a);
 #pragma unroll
-    for (int q = 0; q < CH; ++q) s[q & 7] = __fadd_rn(s[q & 7], ex2(__fmaf_rn(a[q], sT, -c)));
+    for (int q = 0; q < CH; q += 2) add_pair(s2[(q & 7) >> 1], a[q], a[q + 1]);
   }
   if (my_edge >= 0) {
 #pragma unroll
-    for (int q = 0; q < CH; ++q) s[q & 7] = __fadd_rn(s[q & 7], ex2(__fmaf_rn(ev[q], sT, -c)));
+    for (int q = 0; q < CH; q += 2) add_pair(s2[(q & 7) >> 1], ev[q], ev[q + 1]);
   }
+  float s[8];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) up2(s2[q], s[2 * q], s[2 * q + 1]);
   const float S = warp_sum(__fadd_rn(__fadd_rn(__fadd_rn(s[0], s[1]), __fadd_rn(s[2], s[3])),
                                      __fadd_rn(__fadd_rn(s[4], s[5]), __fadd_rn(s[6], s[7]))));
   return make_float2(M, __fmul_rn(S, ex2(-__fmaf_rn(M, sT, -c))));
@@ -765,6 +811,20 @@ __device__ __forceinline__ float2 chunk_softmax(const unsigned char* slot, const
 __device__ __forceinline__ float weight(float zp, float zq, bool residual, const float4& prm) {
   const float ep = scaled_exp(zp, prm.x, prm.z);
   return fmaxf(residual ? __fmaf_rn(-prm.w, scaled_exp(zq, prm.y, prm.z), ep) : ep, 0.0f);
+}
+
+// weight() of two elements at once, residual form, with the two-wide
+// instructions: each half is rounded exactly as weight() rounds it.
+__device__ __forceinline__ void weight_pair(float zp0, float zp1, float zq0, float zq1,
+                                            const float4& prm, float& w0, float& w1) {
+  const f32x2 s2 = pk2(prm.z, prm.z);
+  float a0, a1, b0, b1;
+  up2(mul2(sub2(pk2(zp0, zp1), pk2(prm.x, prm.x)), s2), a0, a1);
+  up2(mul2(sub2(pk2(zq0, zq1), pk2(prm.y, prm.y)), s2), b0, b1);
+  float r0, r1;
+  up2(fma2(pk2(ex2(b0), ex2(b1)), pk2(-prm.w, -prm.w), pk2(ex2(a0), ex2(a1))), r0, r1);
+  w0 = fmaxf(r0, 0.0f);
+  w1 = fmaxf(r1, 0.0f);
 }
 
 // Final-draw weights of vector j of a chunk staged in a slot (target part
@@ -800,8 +860,13 @@ __device__ __forceinline__ void vector_weights(const unsigned char* slot, const 
 #pragma unroll
     for (int q = 0; q < CH; ++q) vq[q] = 0.0f;
   }
+  if (residual) {
 #pragma unroll
-  for (int q = 0; q < CH; ++q) w[q] = weight(vp[q], vq[q], residual, prm);
+    for (int q = 0; q < CH; q += 2) weight_pair(vp[q], vp[q + 1], vq[q], vq[q + 1], prm, w[q], w[q + 1]);
+  } else {
+#pragma unroll
+    for (int q = 0; q < CH; ++q) w[q] = weight(vp[q], 0.0f, false, prm);
+  }
 }
 
 // Whole warp: the final-draw mass of a draw chunk: per sweep of 32 vectors
@@ -938,12 +1003,11 @@ __device__ float piece_sweeps(const unsigned char* slot, const Chunk& kp, const 
   for (int s = 0; s < kDrawSweeps; ++s) {
     float w[CH];
     vector_weights<DT>(slot, vs, kp, kq, true, same, prm, s * 32 + lane, w);
-    float a = 0.0f, b = 0.0f;
+    f32x2 ab = pk2(0.0f, 0.0f);   // even and odd elements' sums
 #pragma unroll
-    for (int q = 0; q < CH; q += 2) {
-      a = __fadd_rn(a, w[q]);
-      b = __fadd_rn(b, w[q + 1]);
-    }
+    for (int q = 0; q < CH; q += 2) ab = add2(ab, pk2(w[q], w[q + 1]));
+    float a, b;
+    up2(ab, a, b);
     t[s] = __fadd_rn(a, b);
     all = __fadd_rn(all, t[s]);
   }
