@@ -56,6 +56,8 @@ constexpr int kChunkBytes = 6144;                       // deciding / bonus item
 constexpr int kDrawBytes = 3072;                        // residual piece: this much of each row
 constexpr int kDrawSweeps = kDrawBytes / 512;           // 32 lanes x 16 bytes per sweep
 constexpr int kDraftOff = kDrawBytes;                   // draft part of a residual slot
+constexpr int kPieceRec = 8;                            // floats per piece record: sweep sums, total, unused
+static_assert(kDrawSweeps + 1 <= kPieceRec && kPieceRec % 4 == 0, "a piece record is whole 16-byte words");
 constexpr int kSlotBytes = kChunkBytes + 32;
 constexpr int kRingBytes = kAgents * kSlots * kSlotBytes;
 constexpr int kPlanMax = 1024;                          // requests per launch (the host splits)
@@ -92,7 +94,7 @@ struct __align__(16) Req {
   int b;          // the request
   int j;          // the rejected row (a bonus draw: n)
   float aux;      // residual: S_p of the rejected row; bonus: the target mass left at its chunk
-  int chunk;      // a bonus draw: its chunk of row n
+  int chunk;      // bonus: its chunk of row n; residual: uniforms_resample[b] (float bits)
   float4 prm;     // Mp, Mq, log2(e)/T, S_p/S_q of the rejected row (a bonus draw: Mp, 0, log2(e)/T, 0)
 };
 static_assert(sizeof(Req) == 32, "Req is one 32-byte record");
@@ -118,8 +120,7 @@ struct Params {
   Req* req;         // [B] listed draws (counts: header[kHResid], header[kHBonus])
   uint2* part;      // [B][R][NC] chunk records: (max, sum) or (max, index)
   float* zx;        // [B][R] the drafted token's logit in rows t < n
-  float* dmass;     // [B][NCd] residual sums of the pieces (by list entry)
-  float* dsw;       // [B][NCd][kDrawSweeps] residual sums of their sweeps
+  float* dpc;       // [B][NCd][kPieceRec] residual sums of each piece: its sweeps, then its total (by list entry)
   float* row_stats; // [B][K+1][8] or null
 };
 
@@ -1105,16 +1106,18 @@ __device__ __forceinline__ int pick_in_sweep(const float* w, float tau, int e0, 
 // ---------------------------------------------------------------- draws
 
 // Whole warp: the chunk holding mass u * W of a draw, chunk masses
-// mass[0..n) in shared memory (lane l sums chunks [l m, l m + m) in order,
+// mass[c * stride], c in [0, n), in shared memory (lane l sums chunks
+// [l m, l m + m) in order,
 // then the lanes are scanned).  Returns the chunk and, in rem, the target
 // mass left inside it; rounding that leaves the target beyond the total
 // falls on the last chunk with positive mass.  Sets W to the total.  -1:
 // no mass at all.
-__device__ int pick_chunk(const float* mass, int n, float u, int lane, float& W, float& rem) {
+__device__ int pick_chunk(const float* mass, int n, float u, int lane, float& W, float& rem,
+                          int stride = 1) {
   const int m = (n + 31) / 32;
   const int c0 = min(n, lane * m), c1 = min(n, c0 + m);
   float lane_tot = 0.0f;
-  for (int c = c0; c < c1; ++c) lane_tot = __fadd_rn(lane_tot, mass[c]);
+  for (int c = c0; c < c1; ++c) lane_tot = __fadd_rn(lane_tot, mass[c * stride]);
   const float incl = warp_incl_scan(lane_tot, lane);
   W = __shfl_sync(0xffffffffu, incl, 31);
   const float excl = __fsub_rn(incl, lane_tot);
@@ -1129,7 +1132,7 @@ __device__ int pick_chunk(const float* mass, int n, float u, int lane, float& W,
     float acc = excl, last_acc = excl;
     int last_c = -1;
     for (int c = c0; c < c1 && chunk < 0; ++c) {
-      const float t = mass[c];
+      const float t = mass[c * stride];
       if (t > 0.0f) {
         if (__fadd_rn(acc, t) > tau) {
           chunk = c;
@@ -1257,7 +1260,7 @@ __device__ __forceinline__ void p_masses(const uint2* rec, int NC, float Mp, flo
 // ---------------------------------------------------------------- decisions
 
 constexpr int kMaxRows = 2 * SPECV_MAX_DRAFT + 1;
-constexpr int kDecideRecs = 1024;   // records a decide CTA stages at once
+constexpr int kDecideRecs = 2048;   // records a decide CTA stages at once (in batches of 1024)
 constexpr int kDecideBuf = kDecideRecs > kDecideWarps * kMaxChunks ? kDecideRecs
                                                                     : kDecideWarps * kMaxChunks;
 
@@ -1453,23 +1456,26 @@ __device__ void decide_request(const Params& P, DecideSmem& D, int b, const Deci
       zpf = __ldcg(P.zx + static_cast<size_t>(b) * R + tid);
       zqf = __ldcg(P.zx + static_cast<size_t>(b) * R + K + 1 + tid);
     }
-    constexpr int kPer = kDecideRecs / (kDecideWarps * 32);
-    uint2 v[kPer];
+    constexpr int kPer = 8;
+    constexpr int kBatch = kPer * kDecideWarps * 32;
     if (all_at_once) {
       const uint2* base = P.part + static_cast<size_t>(b) * R * NC;
+      for (int i0 = 0; i0 < nrows * NC; i0 += kBatch) {
+        uint2 v[kPer];
 #pragma unroll
-      for (int k = 0; k < kPer; ++k) {
-        const int i = k * kDecideWarps * 32 + tid;
-        if (i < nrows * NC) {
-          const int r = i / NC;
-          const int row = r < nt ? r : K + 1 + (r - nt);
-          v[k] = __ldcg(base + static_cast<size_t>(row) * NC + (i - r * NC));
+        for (int k = 0; k < kPer; ++k) {
+          const int i = i0 + k * kDecideWarps * 32 + tid;
+          if (i < nrows * NC) {
+            const int r = i / NC;
+            const int row = r < nt ? r : K + 1 + (r - nt);
+            v[k] = __ldcg(base + static_cast<size_t>(row) * NC + (i - r * NC));
+          }
         }
-      }
 #pragma unroll
-      for (int k = 0; k < kPer; ++k) {
-        const int i = k * kDecideWarps * 32 + tid;
-        if (i < nrows * NC) D.rec[i] = v[k];
+        for (int k = 0; k < kPer; ++k) {
+          const int i = i0 + k * kDecideWarps * 32 + tid;
+          if (i < nrows * NC) D.rec[i] = v[k];
+        }
       }
     }
     if (tid < 32) {
@@ -1609,7 +1615,7 @@ __device__ void decide_request(const Params& P, DecideSmem& D, int b, const Deci
     const float Mq = __shfl_sync(0xffffffffu, Mq_l, j);
     const float Sq = __shfl_sync(0xffffffffu, Sq_l, j);
     if (lane == 0) {
-      store_req(P.req + atomicAdd(P.header + kHResid, 1), b, j, Sp, 0,
+      store_req(P.req + atomicAdd(P.header + kHResid, 1), b, j, Sp, __float_as_int(ur),
                 make_float4(Mp, Mq, sT, __fdiv_rn(Sp, Sq)));
     }
     write_outputs(P, b, j, -1, x_lane, lane);   // the residual kernel writes the token
@@ -1714,34 +1720,49 @@ __device__ void bonus_draw(const Params& P, uint4* stage, const Req& r, int lane
   __syncwarp();
 }
 
-// Whole warp: the residual draw of listed request b (entry e, rejected at
-// row j), with uniforms_resample[b]: the piece from the piece sums, the
-// sweep from that piece's sweep sums, the token from the sweep of both rows
-// read again.  A residual of exactly zero mass falls back to drawing from
-// p_j with the same uniform (its chunk masses from row j's records, the
-// token from one re-read chunk).  Slot 0 of the warp's ring is its scratch.
+// Whole warp: starts copying entry e's piece records into slot 0 of the
+// warp's ring (cp.async; residual_search waits), when they fit the slot.
+__device__ __forceinline__ void stage_pieces(const Params& P, Agent& ag, int e) {
+  if (P.NCd * kPieceRec * 4 > kSlotBytes) return;
+  const uint4* src = reinterpret_cast<const uint4*>(P.dpc + static_cast<size_t>(e) * P.NCd * kPieceRec);
+  uint4* dst = reinterpret_cast<uint4*>(ag.slot(0));
+  __syncwarp();   // every lane is done with the scratch
+  for (int i = ag.lane; i < P.NCd * kPieceRec / 4; i += 32) cp_async16(dst + i, src + i);
+}
+
+// Whole warp: the residual draw of list entry e (record r: request b,
+// rejected at row j, the resample uniform): the piece from the piece sums,
+// the sweep from that piece's sweep sums, the token from the sweep of both
+// rows read again.  A residual of exactly zero mass falls back to drawing
+// from p_j with the same uniform (its chunk masses from row j's records,
+// the token from one re-read chunk).  Slot 0 of the warp's ring is its
+// scratch; stage_pieces(e) has been called.
 template <int DT>
-__device__ void residual_search(const Params& P, Agent& ag, int e) {
+__device__ void residual_search(const Params& P, Agent& ag, int e, const Req& r) {
   constexpr int CH = Elt<DT>::kPerVec;
   const int lane = ag.lane, K = P.K, V = P.V, NC = P.NC, NCd = P.NCd;
-  const Req r = load_req(P.req + e);
   const int b = r.b, j = r.j;
   const float4 prm = r.prm;
+  const float ur = __int_as_float(r.chunk);
   float* mass = reinterpret_cast<float*>(ag.slot(0));
-  const float* dm = P.dmass + static_cast<size_t>(e) * NCd;
+  const float* pc = P.dpc + static_cast<size_t>(e) * NCd * kPieceRec;
+  const bool staged = NCd * kPieceRec * 4 <= kSlotBytes;
+  cp_async_wait_all();
   __syncwarp();
-  for (int c = lane; c < NCd; c += 32) mass[c] = __ldcg(dm + c);
-  __syncwarp();
-  const float ur = __ldg(P.uniforms_resample + b);
+  if (!staged) {   // the piece totals alone, gathered
+    for (int c = lane; c < NCd; c += 32) mass[c] = __ldcg(pc + c * kPieceRec + kDrawSweeps);
+    __syncwarp();
+  }
   float W = 0.0f, rem = 0.0f;
-  int chunk = pick_chunk(mass, NCd, ur, lane, W, rem);
+  int chunk = staged ? pick_chunk(mass + kDrawSweeps, NCd, ur, lane, W, rem, kPieceRec)
+                     : pick_chunk(mass, NCd, ur, lane, W, rem);
   const uintptr_t rp = target_row<DT>(P, b, j);
   int tok = -1;
   if (W > 0.0f) {
     if (chunk >= 0) {
-      const float sw = lane < kDrawSweeps
-          ? __ldcg(P.dsw + (static_cast<size_t>(e) * NCd + chunk) * kDrawSweeps + lane)
-          : 0.0f;
+      const float sw = lane < kDrawSweeps ? (staged ? mass[chunk * kPieceRec + lane]
+                                                    : __ldcg(pc + chunk * kPieceRec + lane))
+                                          : 0.0f;
       float rem2 = 0.0f;
       const int sweep = pick_lane(sw, kDrawSweeps, rem, lane, rem2);
       if (sweep >= 0) {
@@ -1930,9 +1951,9 @@ __device__ void consume_residual(const Params& P, Agent& ag, int s, const Item& 
   float mine;
   const float t = piece_sweeps<DT>(slot, kp, kq, it.prm, lane, mine);
   const int e = it.n;   // the request's entry in the list
-  if ((lane & 3) == 0 && (lane >> 2) < kDrawSweeps)
-    P.dsw[(static_cast<size_t>(e) * P.NCd + it.c) * kDrawSweeps + (lane >> 2)] = mine;
-  if (lane == 0) P.dmass[static_cast<size_t>(e) * P.NCd + it.c] = t;
+  float* pr = P.dpc + (static_cast<size_t>(e) * P.NCd + it.c) * kPieceRec;
+  if ((lane & 3) == 0 && (lane >> 2) < kDrawSweeps) pr[lane >> 2] = mine;
+  if (lane == 0) pr[kDrawSweeps] = t;
 }
 
 // One lane: residual item i (entry i / NCd, piece i mod NCd).
@@ -2052,9 +2073,20 @@ __global__ void __launch_bounds__(kDecideWarps * 32) search_kernel(const Params 
   ag.ring = dyn + static_cast<size_t>(warp) * kSlotBytes;
   ag.ph = 0;
   ag.lane = tid & 31;
+  // the first entry's records are requested before the list's length is
+  // known (entries past it read stale workspace, and are not used)
+  const int e0 = static_cast<int>(blockIdx.x) * kDecideWarps + warp;
+  Req r = load_req(P.req + min(e0, P.B - 1));
+  stage_pieces(P, ag, min(e0, P.B - 1));
   const int count = __ldcg(P.header + kHResid);
-  for (int e = blockIdx.x * kDecideWarps + warp; e < count; e += gridDim.x * kDecideWarps)
-    residual_search<DT>(P, ag, e);
+  for (int e = e0; e < count; e += gridDim.x * kDecideWarps) {
+    if (e != e0) {
+      r = load_req(P.req + e);
+      stage_pieces(P, ag, e);
+    }
+    residual_search<DT>(P, ag, e, r);
+  }
+  cp_async_wait_all();
   __syncthreads();
   if (tid == 0) {
     __threadfence();
@@ -2073,7 +2105,7 @@ __global__ void __launch_bounds__(kDecideWarps * 32) search_kernel(const Params 
 int elt_bytes(specv_dtype dt) { return dt == SPECV_BF16 ? 2 : 4; }
 
 struct Layout {
-  size_t header, req, part, zx, dmass, dsw, total;
+  size_t header, req, part, zx, dpc, total;
 };
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
@@ -2097,9 +2129,8 @@ Layout ws_layout(int B, int K, int V, specv_dtype dt) {
   L.req = kHeaderBytes;
   L.part = align256(L.req + sizeof(Req) * Bl);
   L.zx = align256(L.part + sizeof(uint2) * Bl * R * NC);
-  L.dmass = align256(L.zx + sizeof(float) * Bl * R);
-  L.dsw = align256(L.dmass + sizeof(float) * Bl * NCd);
-  L.total = align256(L.dsw + sizeof(float) * Bl * NCd * kDrawSweeps);
+  L.dpc = align256(L.zx + sizeof(float) * Bl * R);
+  L.total = align256(L.dpc + sizeof(float) * Bl * NCd * kPieceRec);
   return L;
 }
 
@@ -2244,8 +2275,7 @@ specv_status launch(const void* target, const void* draft, specv_dtype dtype,
     P.req = reinterpret_cast<Req*>(ws + L.req);
     P.part = reinterpret_cast<uint2*>(ws + L.part);
     P.zx = reinterpret_cast<float*>(ws + L.zx);
-    P.dmass = reinterpret_cast<float*>(ws + L.dmass);
-    P.dsw = reinterpret_cast<float*>(ws + L.dsw);
+    P.dpc = reinterpret_cast<float*>(ws + L.dpc);
     P.row_stats = row_stats ? row_stats + static_cast<size_t>(b0) * (K + 1) * 8 : nullptr;
     const cudaError_t e = dtype == SPECV_BF16 ? launch_sequence<SPECV_BF16>(P, grid, stream)
                                               : launch_sequence<SPECV_F32>(P, grid, stream);
