@@ -220,3 +220,27 @@ def test_ragged_full():
         want = np.mean([(1 - a ** (k + 1)) / (1 - a) for k in n[sel]])
         got = (acc_g[sel] + 1).mean()
         assert abs(got - want) < 4 * max((acc_g[sel] + 1).std(), 0.5) / np.sqrt(sel.sum())
+
+
+def test_batch_beyond_one_launch_sequence():
+    # 2100 requests run as three launch sequences (at most 1024 requests each)
+    # sharing one workspace: each must leave its draw lists empty for the next
+    inp = synth.random_case(31, 2100, 3, 700, "bf16", temperature=0.9, draft_len="random",
+                            greedy_frac=0.3)
+    _full_check(inp)
+
+
+@pytest.mark.parametrize("greedy_frac", [0.0, 1.0])
+def test_records_beyond_decide_staging(greedy_frac):
+    # K = 16 and 98 chunks per row: 33 rows x 98 records exceed the 2048
+    # records a decide CTA stages at once, so its warps combine a row each
+    inp = synth.random_case(32, 3, 16, 300000, "bf16", temperature=1.0, greedy_frac=greedy_frac)
+    _full_check(inp)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_vocabulary_at_the_row_limit(dtype):
+    import speculative_decoding_verify_sample_gb300 as sv
+    V = sv.max_vocab(dtype)   # 2 MB rows
+    inp = synth.random_case(33, 2, 2, V, dtype, temperature=1.0, draft_len=[2, 1])
+    _full_check(inp)
