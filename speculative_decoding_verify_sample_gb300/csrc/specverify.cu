@@ -49,9 +49,9 @@
 
 namespace {
 
-constexpr int kAgents = 16;                             // agent warps per CTA
+constexpr int kAgents = 32;                             // agent warps per CTA
 constexpr int kThreads = kAgents * 32;
-constexpr int kSlots = 2;                               // ring slots per agent
+constexpr int kSlots = 1;                               // ring slots per agent
 constexpr int kChunkBytes = 6144;                       // deciding / bonus item: one chunk of one row
 constexpr int kDrawBytes = 3072;                        // residual piece: this much of each row
 constexpr int kDrawSweeps = kDrawBytes / 512;           // 32 lanes x 16 bytes per sweep
