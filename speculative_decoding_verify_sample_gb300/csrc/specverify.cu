@@ -14,8 +14,10 @@
 //
 //  1. stats_kernel streams every row a request needs (target rows t <= n,
 //     draft rows t < n when sampled) once from HBM with TMA bulk copies,
-//     in 6 KB chunks.  Each warp is an agent with a private ring of two
-//     shared-memory slots; warp g of the grid's G takes chunks g, g + G,
+//     in 6 KB chunks.  Each warp is an agent with a private ring of
+//     kSlots shared-memory slots (32 warps with one slot each: the other
+//     warps' copies and reductions hide each one's wait); warp g of the
+//     grid's G takes chunks g, g + G,
 //     g + 2 G, ... (decoded 32 at a time, one per lane).  A chunk is
 //     reduced to a record: its maximum and sum of
 //     exp((z - max)/T), or at T = 0 its maximum and lowest argmax.  The
