@@ -47,7 +47,8 @@ METRIC = "verify rows/s (B×(K+1) rows of V logits) and achieved HBM GB/s vs GB3
 KERNEL_SRC = os.path.join(ROOT, "speculative_decoding_verify_sample_gb300", "csrc", "specverify.cu")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "verify_kernel_traffic.json")
 # A call launches four kernels (row statistics, decisions, residual piece
-# sums, residual searches) per sequence of at most 1024 requests.
+# sums with the bonus draws, residual searches) per sequence of at most 1024
+# requests.
 KERNELS_PER_SEQUENCE = 4
 REQUESTS_PER_SEQUENCE = 1024
 FALLBACK_HBM_GBS = 6800.0

@@ -106,12 +106,14 @@ int specv_max_vocab(specv_dtype dtype);
 const char* specv_status_string(specv_status status);
 
 /* Bytes of device workspace one call over B requests of up to K drafts of
- * a V-entry vocabulary needs: a header (status word, ticket and exit
- * counters, the residual list's length), 32 bytes of state per request, one
- * record per (row, 12 KB chunk), the drafted tokens' logits, the residual
- * list and one residual sum per (request, 6 KB piece).  Batches of more than
- * 1024 requests run as consecutive launch sequences that share it, so it is
- * sized for at most 1024 requests.  Returns 0 for sizes out of range. */
+ * a V-entry vocabulary needs: a header (status word, the residual and bonus
+ * lists' lengths, an exit counter), one 32-byte draw record per request
+ * (the residual and bonus lists), one 8-byte record per (row, 6 KB chunk),
+ * the drafted tokens' logits, and one 32-byte record per (listed request,
+ * 3 KB piece) holding the piece's residual sweep sums and total.  Batches
+ * of more than 1024 requests run as consecutive launch sequences that share
+ * it, so it is sized for at most 1024 requests.  Returns 0 for sizes out of
+ * range. */
 size_t specv_workspace_bytes(int B, int K, int V, specv_dtype dtype);
 
 /* Zero a workspace on `stream` (cudaMemsetAsync).  Must run once before the
@@ -139,8 +141,8 @@ specv_status specv_workspace_init(void* workspace, size_t workspace_bytes, specv
  *                     zeroed once with specv_workspace_init.  Calls that may
  *                     run concurrently need separate workspaces.
  * Enqueues four kernels on `stream` per 1024 requests (row statistics,
- * decisions, residual piece sums, residual searches; the last three as
- * programmatic dependent launches); no host synchronisation.
+ * decisions, residual piece sums with the bonus draws, residual searches;
+ * each as a programmatic dependent launch); no host synchronisation.
  */
 specv_status spec_verify_sample(const void* target_logits, const void* draft_logits,
                                 specv_dtype dtype, const int32_t* draft_tokens,
@@ -228,7 +230,7 @@ specv_status specv_launch_plan(int B, int K, int V, specv_dtype dtype, int with_
  *     (cudaGetSymbolAddress, with that device current) and caches it; make
  *     that first call before any stream capture.
  *   - Each call zeroes the part of the array it uses (cudaMemsetAsync on
- *     `stream`), then launches the kernel.  All calls on a device share the
+ *     `stream`), then launches the kernels.  All calls on a device share the
  *     one array: calls that may overlap on the GPU (different streams, or
  *     concurrent host threads) race and must be serialised by the caller.
  *   - The device status word is not exposed: bad data shows as
