@@ -99,3 +99,18 @@ def test_reference_arm_runs_on_rank_zero_only():
     class Args:
         impl, workload, seed, steps, warmup = "reference", "tiny", None, 1, 3
     assert bench.run_reference(Args, 2, 1) is None
+
+
+def test_reference_arm_json_line_keys():
+    # the reference arm's line carries the contract's keys (tiny workload, CPU)
+    class Args:
+        impl, workload, seed, steps, warmup = "reference", "tiny", None, 1, 3
+    line = bench.run_reference(Args, 1, 0)
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["value"] > 0 and line["higher_is_better"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert "workload" in line["config"]
