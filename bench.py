@@ -31,6 +31,7 @@ import hashlib
 import json
 import math
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -264,7 +265,36 @@ def host_inputs(torch, d):
     return {k: (None if v is None else v.cpu().pin_memory()) for k, v in d.items()}
 
 
-def cpu_oracle_rate(inp, budget_s=1.5, nthreads=None, max_requests=None):
+def cpu_model() -> str:
+    """The host CPU as /proc/cpuinfo names it (x86 "model name"; on Arm the
+    implementer and part codes), else the machine type."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            lines = f.read().splitlines()
+    except OSError:
+        lines = []
+    fields = {}
+    for line in lines:
+        if ":" in line:
+            key, val = line.split(":", 1)
+            fields.setdefault(key.strip(), val.strip())
+    for key in ("model name", "Model", "Hardware"):
+        if fields.get(key):
+            return fields[key]
+    if fields.get("CPU implementer") or fields.get("CPU part"):
+        return (f"{platform.machine()} implementer {fields.get('CPU implementer', '?')} "
+                f"part {fields.get('CPU part', '?')}")
+    return platform.machine() or "unknown"
+
+
+def cpu_oracle_single_thread_rate(inp, budget_s=0.5):
+    """The oracle on one host thread: rows/s over at least one call on the
+    first request of the batch."""
+    rate, _, _ = cpu_oracle_rate(inp, budget_s=budget_s, nthreads=1, max_requests=1, min_reps=1)
+    return rate
+
+
+def cpu_oracle_rate(inp, budget_s=1.5, nthreads=None, max_requests=None, min_reps=3):
     """The oracle as it stands on the host cores: rows/s over repeated calls
     on a bounded sample (the first m requests of the batch)."""
     import oracle
@@ -284,7 +314,7 @@ def cpu_oracle_rate(inp, budget_s=1.5, nthreads=None, max_requests=None):
         oracle.verify_sample(sub, nthreads=nthreads)
         reps += 1
         el = time.perf_counter() - t0
-        if el >= budget_s and reps >= 3:
+        if el >= budget_s and reps >= min_reps:
             break
     rows = reps * m * (inp["K"] + 1)
     return rows / el, nthreads, f"first {m} of {B} requests, {reps} repetitions, {el:.2f} s wall"
@@ -412,7 +442,9 @@ def run_ours(args, torch, world, rank, local):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, cores, sample = cpu_oracle_rate(inp)
         line["cpu_baseline"] = {"value": round(v, 1), "unit": "rows/s", "cores": cores,
-                                "kind": "oracle", "sample": sample}
+                                "kind": "oracle", "sample": sample,
+                                "single_thread_value": round(cpu_oracle_single_thread_rate(inp), 1),
+                                "cpu_model": cpu_model()}
     return line
 
 
@@ -488,7 +520,7 @@ def run_reference(args, world, rank):
                    "logits_dtype": inp["dtype"], "rows_per_step": m * (K + 1),
                    "parallelism": "CPU oracle, rank 0 only"},
         "cpu_baseline": {"value": round(value, 1), "unit": "rows/s", "cores": nthreads,
-                         "kind": "oracle", "sample": sample},
+                         "kind": "oracle", "sample": sample, "cpu_model": cpu_model()},
         "e2e": {"value": round(value, 1), "unit": "rows/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

@@ -114,3 +114,12 @@ def test_reference_arm_json_line_keys():
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert "workload" in line["config"]
+
+
+def test_cpu_baseline_helpers():
+    inp = synth.make_inputs("tiny")
+    rate, cores, sample = bench.cpu_oracle_rate(inp, budget_s=0.2)
+    assert rate > 0 and cores >= 1 and "requests" in sample
+    assert bench.cpu_oracle_single_thread_rate(inp, budget_s=0.05) > 0
+    model = bench.cpu_model()
+    assert isinstance(model, str) and model
