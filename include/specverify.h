@@ -205,9 +205,10 @@ specv_status spec_verify_sample_host(const void* target_logits, const void* draf
 
 /* The launch shape the library picks for these sizes (diagnostics): out[0]
  * CTAs of the row-statistics kernel, out[1] vocabulary elements per chunk,
- * out[2] shared-memory stages per CTA, out[3] chunks per row, out[4]
- * dynamic shared memory per CTA (bytes), out[5] threads per CTA.  Queries
- * the current device's occupancy; launches nothing. */
+ * out[2] shared-memory copy slots per agent warp, out[3] chunks per row,
+ * out[4] dynamic shared memory per CTA (bytes), out[5] threads per CTA
+ * (32 per agent warp).  Queries the current device's occupancy; launches
+ * nothing. */
 specv_status specv_launch_plan(int B, int K, int V, specv_dtype dtype, int with_draft,
                                int32_t* out);
 

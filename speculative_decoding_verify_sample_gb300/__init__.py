@@ -60,7 +60,7 @@ def launch_plan(B: int, K: int, V: int, dtype, with_draft: bool = True) -> dict:
     code = SPECV_BF16 if dtype in (torch.bfloat16, "bf16") else SPECV_F32
     out = (ctypes.c_int32 * 6)()
     check("specv_launch_plan", lib().specv_launch_plan(B, K, V, code, int(with_draft), out))
-    return dict(ctas=out[0], chunk=out[1], stages=out[2], chunks_per_row=out[3], smem=out[4],
+    return dict(ctas=out[0], chunk=out[1], slots_per_warp=out[2], chunks_per_row=out[3], smem=out[4],
                 threads=out[5])
 
 
