@@ -28,11 +28,16 @@ _lib = None
 
 # near-tie / condition flags (bitmask per request)
 TIE_ACCEPT = 1       # |u - p/q| < 1e-4 at an evaluated position
-TIE_CDF = 2          # the final draw's u*W lies within 1e-4*W of a bucket edge
-ILL_RESIDUAL = 4     # the final draw came from a residual holding < 1% of the mass
+TIE_CDF = 2          # the final draw's u*W lies within 1e-4*W of an edge of its bucket
+PRECISION_BAND = 4   # ... within EDGE_ABS of such an edge (not within 1e-4*W)
 RES_FALLBACK = 8     # residual mass exactly 0: the replacement was drawn from p
 BAD_INPUT = 16       # the request was rejected as invalid
-NEAR_TIE_MASK = TIE_ACCEPT | TIE_CDF | ILL_RESIDUAL | RES_FALLBACK
+NEAR_TIE_MASK = TIE_ACCEPT | TIE_CDF | PRECISION_BAND | RES_FALLBACK
+FLAG_NAMES = {TIE_ACCEPT: "tie_accept", TIE_CDF: "tie_cdf", PRECISION_BAND: "precision_band",
+              RES_FALLBACK: "res_fallback"}
+
+TIE_BAND = 1e-4      # relative band of the accept test and of a CDF edge (times W)
+EDGE_ABS = 2e-5      # absolute floor of the CDF-edge band, in probability mass
 
 ROW_INFO = 10        # doubles per row in row_stats()
 
@@ -115,7 +120,8 @@ def verify_sample(inp, nthreads: int = 1):
 def row_stats(inp, nthreads: int = 1):
     """Per-row quantities, float64 array [B, K+1, 10]:
     zmax_p, S_p, log p(x_t), zmax_q, S_q, log q(x_t), W, candidate token,
-    CDF near-tie flag, accept-test near-tie flag (NaN where a row is unused)."""
+    the candidate draw's flags (TIE_CDF, PRECISION_BAND, RES_FALLBACK bits),
+    accept-test near-tie flag (NaN where a row is unused)."""
     lib = _load()
     tgt, drf, dt, toks, dl, temp, uni, ur, B, K, V = _prep(inp)
     info = np.empty((B, K + 1, ROW_INFO), np.float64)

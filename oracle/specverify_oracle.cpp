@@ -48,14 +48,19 @@ constexpr int kF32 = 0;
 constexpr int kBF16 = 1;
 
 // near-tie / condition flags reported per request
-constexpr int kTieAccept = 1;     // |u - p/q| < 1e-4 at an evaluated position
-constexpr int kTieCdf = 2;        // u*W within 1e-4*W of a CDF bucket edge
-constexpr int kIllResidual = 4;   // final draw from a residual holding < 1% of the mass
-constexpr int kResFallback = 8;   // residual mass exactly 0: drawn from p instead
-constexpr int kBadInput = 16;     // request rejected as invalid
+constexpr int kTieAccept = 1;       // |u - p/q| < 1e-4 at an evaluated position
+constexpr int kTieCdf = 2;          // u*W within 1e-4*W of an edge of the chosen CDF bucket
+constexpr int kPrecisionBand = 4;   // u*W within kEdgeAbs of such an edge, but not within 1e-4*W
+constexpr int kResFallback = 8;     // residual mass exactly 0: drawn from p instead
+constexpr int kBadInput = 16;       // request rejected as invalid
 
 constexpr double kTieBand = 1e-4;
-constexpr double kIllResidualMass = 1e-2;
+// Absolute floor of the CDF-edge band, in units of probability mass.  If
+// every p_i and q_i carries a relative error of at most 1e-5 (the tolerance
+// fixed for normalised probabilities computed in fp32), a cumulative edge
+// C_i = sum_{k<=i} (p_k - q_k)+ and the draw target u*W move relative to one
+// another by at most 1e-5 * sum_k (p_k + q_k) = 2e-5.
+constexpr double kEdgeAbs = 2e-5;
 
 double widen(const void* base, int dtype, size_t idx) {
   if (dtype == kF32) return static_cast<double>(static_cast<const float*>(base)[idx]);
@@ -111,11 +116,37 @@ int argmax_lowest(const std::vector<double>& z) {
   return best;
 }
 
-// Inverse-CDF draw from non-negative weights w with total W and uniform u.
-// Sets *tie when u*W lies within kTieBand*W of either edge of the chosen
-// bucket.  Returns -1 only when every weight is zero.
-int inverse_cdf(const std::vector<double>& w, double W, double u, bool* tie) {
+// Near-tie class of a draw whose target u*W fell in the bucket [lo, hi):
+// kTieCdf when an edge with a bucket beyond it lies within 1e-4*W of the
+// target, kPrecisionBand when one lies within kEdgeAbs only, else 0.  The
+// edge below the first positive weight (0) and above the last (W) have no
+// bucket beyond them, so no rounding can move the draw across them.  W = 1
+// (a draw from p) makes the relative band the wider one.
+int edge_flag(double target, double lo, double hi, double W, bool lo_inner, bool hi_inner) {
+  double d = std::numeric_limits<double>::infinity();
+  if (lo_inner) d = std::min(d, std::fabs(target - lo));
+  if (hi_inner) d = std::min(d, std::fabs(target - hi));
+  if (d < kTieBand * W) return kTieCdf;
+  if (d < kEdgeAbs) return kPrecisionBand;
+  return 0;
+}
+
+// Inverse-CDF draw from non-negative weights w with total W and uniform u:
+// the smallest i with w_i > 0 and w_0 + ... + w_i > u*W.  *flag gets the
+// near-tie class of the chosen bucket (edge_flag).  Returns -1 only when
+// every weight is zero.  W must be the same compensated sum of w the loop
+// forms, so for u < 1 the target u*W < W is always passed; the "last
+// positive weight" return below is a guard for rounding the loop cannot
+// reach with such a W.
+int inverse_cdf(const std::vector<double>& w, double W, double u, int* flag) {
   const double target = u * W;
+  int first_pos = -1, final_pos = -1;
+  for (int i = 0; i < static_cast<int>(w.size()); ++i) {
+    if (w[i] > 0.0) {
+      if (first_pos < 0) first_pos = i;
+      final_pos = i;
+    }
+  }
   CompSum cum;
   int last_pos = -1;
   double last_lo = 0.0, last_hi = 0.0;
@@ -126,12 +157,12 @@ int inverse_cdf(const std::vector<double>& w, double W, double u, bool* tie) {
     const double hi = cum.value();
     last_pos = i; last_lo = lo; last_hi = hi;
     if (hi > target) {
-      *tie = std::fabs(target - lo) < kTieBand * W || std::fabs(target - hi) < kTieBand * W;
+      *flag = edge_flag(target, lo, hi, W, i != first_pos, i != final_pos);
       return i;
     }
   }
   if (last_pos >= 0)
-    *tie = std::fabs(target - last_lo) < kTieBand * W || std::fabs(target - last_hi) < kTieBand * W;
+    *flag = edge_flag(target, last_lo, last_hi, W, last_pos != first_pos, false);
   return last_pos;
 }
 
@@ -258,15 +289,14 @@ void verify_request(const Args& a, int b, std::vector<double>& zp, std::vector<d
     w.resize(a.V);
     for (int i = 0; i < a.V; ++i) w[i] = std::max(p[i] - q[i], 0.0);
     double W = comp_total(w);
-    if (W < kIllResidualMass) flags |= kIllResidual;
     if (!(W > 0.0)) {
       flags |= kResFallback;
       w = p;
       W = comp_total(w);
     }
-    bool tie = false;
-    const int tok = inverse_cdf(w, W, a.uniforms_resample[b], &tie);
-    if (tie) flags |= kTieCdf;
+    int edge = 0;
+    const int tok = inverse_cdf(w, W, a.uniforms_resample[b], &edge);
+    flags |= edge;
     tokens.push_back(tok);
     write_outputs(a, b, t, tokens, flags);
     return;
@@ -277,9 +307,9 @@ void verify_request(const Args& a, int b, std::vector<double>& zp, std::vector<d
     write_outputs(a, b, -1, {}, kBadInput);
     return;
   }
-  bool tie = false;
-  const int tok = inverse_cdf(p, comp_total(p), u[n], &tie);
-  if (tie) flags |= kTieCdf;
+  int edge = 0;
+  const int tok = inverse_cdf(p, comp_total(p), u[n], &edge);
+  flags |= edge;
   tokens.push_back(tok);
   write_outputs(a, b, n, tokens, flags);
 }
@@ -291,7 +321,8 @@ void verify_request(const Args& a, int b, std::vector<double>& zp, std::vector<d
 //   6 W (residual mass sum (p-q)+ at t < n; sum p at t = n)
 //   7 the final-draw token this row would give (residual with the resample
 //     uniform at t < n, bonus with u[n] at t = n; greedy: argmax)
-//   8 CDF near-tie flag of that draw   9 accept-test near-tie flag
+//   8 near-tie class of that draw (kTieCdf, kPrecisionBand or 0)
+//   9 accept-test near-tie flag
 // Rows a request does not need hold NaN.
 void row_stats_request(const Args& a, int b, std::vector<double>& zp, std::vector<double>& zq,
                        std::vector<double>& p, std::vector<double>& q, std::vector<double>& w) {
@@ -321,11 +352,11 @@ void row_stats_request(const Args& a, int b, std::vector<double>& zp, std::vecto
     r[0] = zmax_p;
     r[1] = S_p;
     if (t == n) {
-      bool tie = false;
+      int edge = 0;
       const double W = comp_total(p);
       r[6] = W;
-      r[7] = inverse_cdf(p, W, u[n], &tie);
-      r[8] = tie ? 1.0 : 0.0;
+      r[7] = inverse_cdf(p, W, u[n], &edge);
+      r[8] = edge;
       continue;
     }
     load_row(a.draft, a.dtype, drow0 + t, a.V, zq);
@@ -339,10 +370,11 @@ void row_stats_request(const Args& a, int b, std::vector<double>& zp, std::vecto
     for (int i = 0; i < a.V; ++i) w[i] = std::max(p[i] - q[i], 0.0);
     double W = comp_total(w);
     r[6] = W;
-    bool tie = false;
-    if (!(W > 0.0)) { w = p; W = comp_total(w); }
-    r[7] = inverse_cdf(w, W, a.uniforms_resample[b], &tie);
-    r[8] = tie ? 1.0 : 0.0;
+    int edge = 0;
+    if (!(W > 0.0)) { w = p; W = comp_total(w); edge = kResFallback; }
+    int e2 = 0;
+    r[7] = inverse_cdf(w, W, a.uniforms_resample[b], &e2);
+    r[8] = edge | e2;
   }
 }
 

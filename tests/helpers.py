@@ -4,9 +4,12 @@ CUDA path with the oracle under the parity rules.
 Parity rules (fixed for this sampler):
   * greedy requests (T = 0): accepted_len and out_tokens bit-exact;
   * sampled requests: accepted_len and out_tokens equal, except where the
-    oracle flags a near-tie (|u - p/q| < 1e-4 at an evaluated position, the
-    final draw's u*W within 1e-4*W of a bucket edge, a residual holding < 1%
-    of the mass, or a zero-mass residual); such mismatches are counted;
+    oracle flags a near-tie: |u - p/q| < 1e-4 at an evaluated position, the
+    final draw's target u*W within 1e-4*W of an edge of its CDF bucket, or
+    within 2e-5 of probability mass of such an edge (the shift a 1e-5
+    relative error on every p_i and q_i can cause), or a residual of exactly
+    zero mass.  Excused mismatches are counted per flag, reported, and held
+    under a ceiling;
   * per-row statistics: max logits exact; S_p, S_q within 1e-5 relative;
     ln p(x_t), ln q(x_t) within 1e-5 absolute (1e-5 relative on p, q); at
     the final row (t = accepted_len) the final-draw mass within 1e-5
@@ -61,8 +64,16 @@ def run_gpu(inp, debug=False, workspace=None, device="cuda"):
     return acc.cpu().numpy(), out.cpu().numpy()
 
 
-def assert_outputs_match(inp, acc_g, out_g, acc_o, out_o, flags_o, rows=None):
-    """Returns the number of (allowed) mismatches at flagged near-ties."""
+def excuse_ceiling(n_sampled: int) -> int:
+    """Most excused (flagged near-tie) mismatches a comparison may have: a
+    near-tie band of width ~1e-4 is hit by well under 1% of requests."""
+    return max(3, int(np.ceil(0.01 * n_sampled)))
+
+
+def assert_outputs_match(inp, acc_g, out_g, acc_o, out_o, flags_o, rows=None, label=None):
+    """Checks the parity rules; returns the excused-mismatch report: counts
+    of mismatched requests by oracle flag, the requests flagged, and the
+    total compared (also printed and appended to $SPECV_PARITY_LOG)."""
     idx = np.arange(inp["B"]) if rows is None else np.asarray(rows)
     T = np.asarray(inp["temperature"])[idx]
     mism = (acc_g[idx] != acc_o) | np.any(out_g[idx] != out_o, axis=1)
@@ -76,7 +87,28 @@ def assert_outputs_match(inp, acc_g, out_g, acc_o, out_o, flags_o, rows=None):
         f"unflagged mismatch at requests {idx[bad][:8]}: gpu acc {acc_g[idx][bad][:4]} "
         f"out {out_g[idx][bad][:4]} / oracle acc {acc_o[bad][:4]} out {out_o[bad][:4]} "
         f"flags {flags_o[bad][:4]}")
-    return int((mism & allowed).sum())
+    excused = mism & allowed
+    report = {"label": label, "compared": int(len(idx)), "sampled": int((T > 0).sum()),
+              "excused": int(excused.sum()),
+              "flagged": {name: int(((flags_o & bit) != 0).sum())
+                          for bit, name in oracle.FLAG_NAMES.items()},
+              "excused_by_flag": {name: int((excused & ((flags_o & bit) != 0)).sum())
+                                  for bit, name in oracle.FLAG_NAMES.items()}}
+    report_parity(report)
+    assert report["excused"] <= excuse_ceiling(report["sampled"]), report
+    return report
+
+
+def report_parity(report):
+    """Prints one parity report and appends it to $SPECV_PARITY_LOG (JSON lines)."""
+    import json
+    import os
+    line = json.dumps(report)
+    print("parity", line)
+    path = os.environ.get("SPECV_PARITY_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(line + "\n")
 
 
 def assert_row_stats_match(inp, rs_g, info_o, acc_g, rows=None):
@@ -105,7 +137,7 @@ def assert_row_stats_match(inp, rs_g, info_o, acc_g, rows=None):
             if t != acc_g[b]:
                 continue
             assert abs(g[6] - o[6]) <= MASS_ATOL, (b, t, "mass", g[6], o[6])
-            row_flag = o[8] != 0 or (t < n and not (o[6] >= 1e-2))
+            row_flag = o[8] != 0   # the draw's own CDF-edge or zero-residual flag
             if g[7] != o[7]:
                 assert row_flag, (b, t, "candidate", g[7], o[7], "mass", o[6])
                 flagged_rows += 1

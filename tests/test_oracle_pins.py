@@ -426,3 +426,148 @@ def test_sampled_request_with_unusable_row_is_flagged():
     inp["temperature"][:] = 0.0
     acc, out, flags = oracle.verify_sample(inp)
     assert np.all(flags == 0)
+
+
+# ---------------------------------------------------------------- near-tie flags
+#
+# The parity rules excuse a GPU/oracle mismatch only where the oracle sets a
+# near-tie flag, so each flag is pinned here on constructed inputs whose
+# ratio p(x)/q(x) and CDF edges are known (from scipy's softmax, not from the
+# oracle): just inside a band the flag is set, just outside it is not.
+
+
+def _one_request(zp, zq, x, u, ur, n=None):
+    zp = np.asarray(zp, np.float32)
+    zq = np.asarray(zq, np.float32)
+    K = zq.shape[0]
+    return dict(B=1, K=K, V=zp.shape[1], dtype="f32", target=zp[None].copy(),
+                draft=zq[None].copy(), draft_tokens=np.asarray([x], np.int32),
+                draft_len=None if n is None else np.asarray([n], np.int32),
+                temperature=np.ones(1, np.float32),
+                uniforms=np.asarray([u], np.float32), uniforms_resample=np.asarray([ur], np.float32))
+
+
+def _f32(v):
+    return float(np.float32(v))
+
+
+@pytest.mark.parametrize("delta,flagged", [(-5e-5, True), (5e-5, True), (-9e-5, True),
+                                           (9e-5, True), (-1.1e-4, False), (1.1e-4, False),
+                                           (-2e-4, False), (2e-4, False)])
+def test_tie_accept_band(delta, flagged):
+    # p = (0.5, 0.5), q = (0.8, 0.2), x = 0: p(x)/q(x) = 0.625
+    zp = np.log([[0.5, 0.5], [0.5, 0.5]])
+    zq = np.log([[0.8, 0.2]])
+    ratio = _dist(np.float32(zp[0]), 1.0)[0] / _dist(np.float32(zq[0]), 1.0)[0]
+    u0 = _f32(ratio + delta)
+    acc, out, flags = oracle.verify_sample(_one_request(zp, zq, [0], [u0, 0.25], 0.5))
+    assert bool(flags[0] & oracle.TIE_ACCEPT) == flagged, (delta, flags[0])
+    assert flags[0] & ~oracle.TIE_ACCEPT == 0          # no other flag on this input
+    assert acc[0] == (1 if u0 < ratio else 0)          # strict u < p/q decides
+    info = oracle.row_stats(_one_request(zp, zq, [0], [u0, 0.25], 0.5))
+    assert bool(info[0, 0, 9]) == flagged
+
+
+@pytest.mark.parametrize("edge_i,delta,flagged", [(1, -5e-5, True), (1, 5e-5, True),
+                                                  (2, -9e-5, True), (0, 5e-5, True),
+                                                  (1, -2e-4, False), (1, 2e-4, False),
+                                                  (2, 1.2e-4, False), (0, -3e-4, False)])
+def test_tie_cdf_band_bonus_draw(edge_i, delta, flagged):
+    # p = q = (0.1, 0.2, 0.3, 0.4): the draft is always accepted and the bonus
+    # token is drawn from p with uniforms[1]; CDF edges 0.1, 0.3, 0.6
+    z = np.log([[0.1, 0.2, 0.3, 0.4]] * 2)
+    edges = np.cumsum(_dist(np.float32(z[1]), 1.0))
+    u1 = _f32(edges[edge_i] + delta)
+    inp = _one_request(z, z[:1], [3], [0.5, u1], 0.5)
+    acc, out, flags = oracle.verify_sample(inp)
+    assert acc[0] == 1
+    assert out[0, 1] == int(np.searchsorted(edges, u1, side="right"))
+    assert bool(flags[0] & oracle.TIE_CDF) == flagged, (edge_i, delta, flags[0])
+    assert flags[0] & ~oracle.TIE_CDF == 0
+    info = oracle.row_stats(inp)
+    assert info[0, 1, 7] == out[0, 1] and bool(info[0, 1, 8]) == flagged
+
+
+def _small_residual_case():
+    # q uniform over 4, p = (0.2505, 0.2505, 0.249, 0.25): (p - q)+ is about
+    # (5e-4, 5e-4, 0, 0), W about 1e-3; x = 2 (p/q about 0.996) rejected by u = 0.999
+    zp = np.log([[0.2505, 0.2505, 0.249, 0.25], [0.25] * 4])
+    zq = np.zeros((1, 4))
+    p = _dist(np.float32(zp[0]), 1.0)
+    q = _dist(np.float32(zq[0]), 1.0)
+    w = np.maximum(p - q, 0.0)
+    return zp, zq, w
+
+
+@pytest.mark.parametrize("offset,expect", [
+    (6e-8, "tie_cdf"),        # |u'W - C_0| ~ 6e-11 < 1e-4 W
+    (-6e-8, "tie_cdf"),
+    (5e-3, "precision"),      # ~5e-6 of mass: inside 2e-5, outside 1e-4 W
+    (-1.5e-2, "precision"),   # ~1.5e-5
+    (3e-2, None),             # ~3e-5: outside both bands
+    (-0.2, None),
+    (0.3, None),
+])
+def test_residual_edge_bands_replace_small_mass_excuse(offset, expect):
+    zp, zq, w = _small_residual_case()
+    W = w.sum()
+    assert 5e-4 < W < 2e-3                         # a residual far below 1 % of the mass
+    c0 = w[0] / W                                  # the one interior edge, in u' units
+    ur = _f32(c0 + offset)
+    acc, out, flags = oracle.verify_sample(_one_request(zp, zq, [2], [0.999, 0.5], ur))
+    assert acc[0] == 0
+    assert out[0, 0] == (0 if ur * W < w[0] else 1)
+    cdf = flags[0] & (oracle.TIE_CDF | oracle.PRECISION_BAND)
+    want = {"tie_cdf": oracle.TIE_CDF, "precision": oracle.PRECISION_BAND, None: 0}[expect]
+    assert cdf == want, (offset, flags[0])
+    assert flags[0] & ~(oracle.TIE_CDF | oracle.PRECISION_BAND) == 0
+    info = oracle.row_stats(_one_request(zp, zq, [2], [0.999, 0.5], ur))
+    assert int(info[0, 0, 8]) == want and abs(info[0, 0, 6] - W) < 1e-15
+
+
+@pytest.mark.parametrize("ur,token", [(0.3, 0), (0.7, 1)])
+def test_zero_mass_residual_falls_back_to_p(ur, token):
+    # q(x) = e^-40 / S and p(x) = e^-40.5 / S with S = 2 in both rows: in
+    # double S_p == S_q, so p_i == q_i off x and p(x) < q(x); u = 0.9 rejects
+    # x (p/q = e^-0.5) and the residual (p - q)+ is exactly zero
+    zq = np.array([[0.0, 0.0, -40.0]])
+    zp = np.array([[0.0, 0.0, -40.5], [0.0, 0.0, 0.0]])
+    p = _dist(np.float32(zp[0]), 1.0)
+    q = _dist(np.float32(zq[0]), 1.0)
+    assert np.maximum(p - q, 0.0).sum() == 0.0 and p[2] < q[2]
+    inp = _one_request(zp, zq, [2], [0.9, 0.5], ur)
+    acc, out, flags = oracle.verify_sample(inp)
+    assert acc[0] == 0 and out[0, 0] == token
+    assert flags[0] & oracle.RES_FALLBACK
+    info = oracle.row_stats(inp)
+    assert info[0, 0, 6] == 0.0 and int(info[0, 0, 8]) & oracle.RES_FALLBACK
+    assert info[0, 0, 7] == token
+
+
+@pytest.mark.parametrize("u,token,tie", [(0.0, 1, False), (1 - 2 ** -24, 3, False),
+                                         (0.5, 3, True), (0.25, 1, False), (0.75, 3, False)])
+def test_inverse_cdf_never_emits_a_zero_weight_token(u, token, tie):
+    # p = (0, 0.5, 0, 0.5, 0): leading, interior and trailing zero weights
+    z = np.array([[-np.inf, 0.0, -np.inf, 0.0, -np.inf]] * 2)
+    inp = _one_request(z, z[:1], [1], [0.5, u], 0.5)
+    acc, out, flags = oracle.verify_sample(inp)
+    assert acc[0] == 1 and out[0, 1] == token
+    assert bool(flags[0] & oracle.TIE_CDF) == tie
+
+
+def test_flags_agree_with_row_stats_on_random_requests():
+    # the per-request flags are the union of the per-row flags of the rows the
+    # scan evaluated: accept ties at rows 0..min(j, n-1), CDF flags at row j
+    inp = synth.random_case(111, B=400, K=4, V=12, scale=1.0, noise=0.3, temperature=1.0,
+                            draft_len="random")
+    acc, out, flags = oracle.verify_sample(inp)
+    info = oracle.row_stats(inp)
+    n = inp["draft_len"]
+    for b in range(inp["B"]):
+        j = acc[b]
+        evaluated = range(min(j, n[b] - 1) + 1)
+        want_acc = any(info[b, t, 9] != 0 for t in evaluated)
+        assert bool(flags[b] & oracle.TIE_ACCEPT) == want_acc, b
+        assert flags[b] & (oracle.TIE_CDF | oracle.PRECISION_BAND | oracle.RES_FALLBACK) == \
+            int(info[b, j, 8]), b
+        assert out[b, j] == info[b, j, 7]
