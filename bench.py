@@ -1,21 +1,31 @@
 #!/usr/bin/env python
 """Benchmark of the speculative-decoding verification sampler on GB300.
 
-A step is one call of the sampler over one batch (every step of the rule, one
-kernel launch).  The default workload is the Llama-3-class batch: B = 32
-requests, K = 4 drafts, V = 128256, bf16 logits, T = 0.7 (synthetic, seeded).
+A step is one call of the sampler over one batch (every step of the rule, all
+of the call's kernel launches).  The headline workload is the largest
+single-GPU one, the long ragged batch: B = 128 requests, K = 8, V = 128256,
+f32 logits, draft lengths uniform in 1..8, constant-overlap pairs with alpha
+0.5 / 0.8 / 0.95 (synthetic, seeded).  The same invocation also times the
+other three workloads the HBM bar applies to (Llama-3-class, greedy,
+DeepSeek-V3 MTP) and reports them under "workloads".
 
 Metric: verified rows/s, rows = B*(K+1) per step, whole job (all ranks).
-Timing: W eager warm-up steps, then exactly K steps replayed from CUDA graphs,
-bracketed by a barrier and a device synchronise, timed with CUDA events on
-the launching stream, max over ranks.  Inputs rotate over enough device copies
-to exceed 3x the L2 cache, so every step streams its logits from HBM.
+Timing: W eager warm-up steps, then a region of exactly K steps replayed from
+CUDA graphs, bracketed by a barrier and a device synchronise and timed with
+CUDA events on the launching stream (max over ranks).  The region is
+repeated (at least 5 times and at least ~1 s of device time per workload);
+ms_per_step is the median region / K, with the spread beside it.  Inputs
+rotate over enough device copies to exceed 3x the L2 cache, so every step
+streams its logits from HBM.
 
-Also reported: the roofline of the sampler kernel (algorithmic bytes per
-launch / average launch time vs the measured HBM copy bandwidth), the same
-metric end to end through the host-buffer entry point (pinned host inputs
-copied in, results copied out, every step), SM clocks sampled during the
-timed region, and the CPU oracle timed on the host cores (rank 0, N = 1).
+Also reported: the roofline of the call (algorithmic bytes per call / call
+time vs the measured HBM copy bandwidth), acceptance statistics of the
+outputs (mean accepted length; per-alpha acceptance rate on the ragged
+batch), the same metric end to end through the host-buffer entry point
+(pinned host inputs copied in, results copied out, every step; headline
+only), SM clocks sampled during each workload's timed regions, and, in the
+CPU-baseline leg (rank 0, N = 1), the CPU oracle timed on the host cores plus
+the excused-mismatch counts of the GPU outputs against the oracle.
 
 --impl reference times the CPU oracle instead (the only reference this
 sampler has), rank 0 only, on bounded samples of the same workload.
@@ -56,7 +66,8 @@ FALLBACK_HBM_GBS = 6800.0
 
 WORKLOAD_TEXT = {
     "llama3": "Llama-3-class verify: B=32 K=4 V=128256 bf16, draft~N(0,3^2), target=draft+N(0,1), T=0.7",
-    "greedy": "greedy verify: B=256 K=4 V=128256 bf16, T=0, target argmax = draft w.p. 0.8",
+    "greedy": "greedy verify: B=256 K=4 V=128256 bf16 N(0,3^2), T=0, target argmax = draft w.p. 0.8",
+    "greedy_planted": "greedy verify, planted argmax: B=256 K=4 V=128256 bf16, T=0",
     "dsv3_mtp": "DeepSeek-V3 MTP: B=512 K=1 V=129280 bf16, 25% T=0, else T~U(0,1.2]",
     "ragged": "long ragged: B=128 K=8 V=128256 f32, draft_len~U{1..8}, constant overlap 0.5/0.8/0.95",
     "tiny": "tiny: B=4 K=4 V=1024 f32, T=1",
@@ -69,7 +80,12 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default="llama3", choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--workload", default="ragged", choices=sorted(WORKLOAD_TEXT),
+                    help="headline workload (the JSON line's top level)")
+    ap.add_argument("--also", default="llama3,greedy,dsv3_mtp",
+                    help="comma-separated workloads timed in the same run ('' for none)")
+    ap.add_argument("--min-region-s", type=float, default=1.0,
+                    help="device time per workload over the repeated K-step regions")
     ap.add_argument("--seed", type=int, default=None)
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-e2e", action="store_true")
@@ -80,7 +96,11 @@ def parse_args():
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.steps is None:
-        args.steps = 20000 if args.impl == "ours" else 10
+        args.steps = 200 if args.impl == "ours" else 10
+    args.also = [w for w in args.also.split(",") if w and w != args.workload]
+    for w in args.also:
+        if w not in WORKLOAD_TEXT:
+            ap.error(f"unknown workload {w}")
     return args
 
 
@@ -320,15 +340,61 @@ def cpu_oracle_rate(inp, budget_s=1.5, nthreads=None, max_requests=None, min_rep
     return rows / el, nthreads, f"first {m} of {B} requests, {reps} repetitions, {el:.2f} s wall"
 
 
-def run_ours(args, torch, world, rank, local):
-    import speculative_decoding_verify_sample_gb300 as sv
-    from speculative_decoding_verify_sample_gb300 import synth
+def acceptance_stats(inp, acc):
+    """Acceptance statistics of one call's outputs (GPU results only): mean
+    accepted length and emitted tokens; per constructed alpha, the empirical
+    per-position acceptance rate (accepted drafts / accept tests taken)."""
+    acc = np.asarray(acc)
+    B, K = inp["B"], inp["K"]
+    n = np.full(B, K) if inp.get("draft_len") is None else np.asarray(inp["draft_len"])
+    ok = acc >= 0
+    out = {"mean_accepted_len": round(float(acc[ok].mean()), 4),
+           "mean_emitted": round(float(acc[ok].mean() + 1.0), 4),
+           "bad_requests": int((~ok).sum())}
+    T = np.asarray(inp["temperature"])
+    if (T > 0).any() and (T == 0).any():
+        for name, sel in (("sampled", T > 0), ("greedy", T == 0)):
+            s = sel & ok
+            out[f"mean_accepted_len_{name}"] = round(float(acc[s].mean()), 4)
+    if inp.get("alpha") is not None:
+        per = {}
+        for a in sorted(set(np.asarray(inp["alpha"]).tolist())):
+            s = (np.asarray(inp["alpha"]) == a) & ok
+            tests = np.minimum(acc[s] + 1, n[s]).sum()
+            per[str(a)] = {"constructed": a, "empirical": round(float(acc[s].sum() / tests), 4),
+                           "accept_tests": int(tests),
+                           "mean_emitted": round(float(acc[s].mean() + 1.0), 4),
+                           "closed_form_mean_emitted": round(float(np.mean(
+                               [(1 - a ** (k + 1)) / (1 - a) for k in n[s]])), 4)}
+        out["per_alpha"] = per
+    return out
 
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    sv.build()
-    seed = rank_seed(args.seed if args.seed is not None else synth.DEFAULT_SEED[args.workload], rank)
-    inp = synth.make_inputs(args.workload, seed)
+
+def oracle_parity(inp, acc_g, out_g):
+    """CPU-baseline leg: the oracle on the whole workload (untimed) against
+    one call's GPU outputs; returns the mismatch counts under the parity rules
+    (greedy bit-exact; sampled requests equal except at oracle-flagged
+    near-ties, counted per flag)."""
+    import oracle
+    acc_o, out_o, flags_o = oracle.verify_sample(inp, nthreads=os.cpu_count() or 1)
+    T = np.asarray(inp["temperature"])
+    mism = (np.asarray(acc_g) != acc_o) | np.any(np.asarray(out_g) != out_o, axis=1)
+    allowed = (flags_o & oracle.NEAR_TIE_MASK) != 0
+    return {"compared": int(inp["B"]), "sampled": int((T > 0).sum()),
+            "mismatched": int(mism.sum()),
+            "unexcused": int((mism & (~allowed | (T == 0))).sum()),
+            "excused": int((mism & allowed & (T > 0)).sum()),
+            "flagged": {name: int(((flags_o & bit) != 0).sum())
+                        for bit, name in oracle.FLAG_NAMES.items()}}
+
+
+def time_workload(args, torch, sv, name, dev, world, rank):
+    """Times one workload: W eager warm-ups, then the K-step region replayed
+    from CUDA graphs, repeated; returns (summary dict, inp, device inputs,
+    workspace, outputs of one call on the first copy)."""
+    from speculative_decoding_verify_sample_gb300 import synth
+    seed = rank_seed(args.seed if args.seed is not None else synth.DEFAULT_SEED[name], rank)
+    inp = synth.make_inputs(name, seed)
     B, K, V = inp["B"], inp["K"], inp["V"]
     rows_per_step = B * (K + 1)
     req_bytes = required_bytes(inp)
@@ -355,7 +421,7 @@ def run_ours(args, torch, world, rank, local):
     torch.cuda.synchronize(dev)
     status = ws.read_status()
     if status:
-        raise RuntimeError(f"device status {status:#x} after warm-up")
+        raise RuntimeError(f"{name}: device status {status:#x} after warm-up")
 
     K_steps = args.steps
     stream = torch.cuda.current_stream(dev)
@@ -374,77 +440,132 @@ def run_ours(args, torch, world, rank, local):
         g_cycle = capture(cycle) if full else None
         g_rem = capture(rem) if rem else None
         graphs = [g_cycle] * full + ([g_rem] if g_rem else [])
-        for g in graphs[:1]:
-            g.replay()      # one untimed replay of the captured graph
+        graphs[0].replay()      # one untimed replay of the captured graph
         torch.cuda.synchronize(dev)
 
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+
+    def region():
+        """Exactly K steps between a barrier + synchronise on both sides."""
+        barrier(torch, world)
+        torch.cuda.synchronize(dev)
+        ev0.record(stream)
+        if graphs:
+            for g in graphs:
+                g.replay()
+        else:
+            for i in range(K_steps):
+                step(i)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(torch, world)
+        return max_over_ranks(torch, world, ev0.elapsed_time(ev1), dev)
+
+    first = region()          # calibration (untimed): sets the repeat count
+    reps = int(min(2000, max(5, math.ceil(args.min_region_s * 1e3 / max(first, 1e-3)))))
+    reps = int(max_over_ranks(torch, world, float(reps), dev))
     clocks = None
     if not args.no_clocks:
         clocks = ClockSampler(gpu_id_for(torch, dev))
         clocks.wait_first()
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    barrier(torch, world)
-    torch.cuda.synchronize(dev)
-    if clocks:
         clocks.start()
-    ev0.record(stream)
-    if graphs:
-        for g in graphs:
-            g.replay()
-    else:
-        for i in range(K_steps):
-            step(i)
-    ev1.record(stream)
-    torch.cuda.synchronize(dev)
+    times = [region() for _ in range(reps)]
     if clocks:
         clocks.stop()
-    barrier(torch, world)
-    ms = ev0.elapsed_time(ev1)
-    ms = max_over_ranks(torch, world, ms, dev)
     status = ws.read_status()
     if status:
-        raise RuntimeError(f"device status {status:#x} after the timed region")
+        raise RuntimeError(f"{name}: device status {status:#x} after the timed regions")
 
+    times.sort()
+    ms = statistics.median(times)
     ms_per_step = ms / K_steps
     value = job_rate(rows_per_step, K_steps, world, ms / 1e3)
     achieved = req_bytes / (ms_per_step / 1e3) / 1e9
     peak, peak_src = measured_hbm_peak()
-    line = {
-        "metric": METRIC, "value": round(value, 1), "unit": "rows/s", "n_gpus": world,
-        "steps": K_steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic (seeded; logits generated, no model weights)",
-        "config": {
-            "workload": WORKLOAD_TEXT[args.workload], "B": B, "K": K, "V": V,
-            "logits_dtype": inp["dtype"], "rows_per_step": rows_per_step,
-            "required_bytes_per_step": req_bytes,
-            "l2": f"rotating {n_copies} device copies of the logits "
-                  f"({n_copies * req_bytes / 1e6:.0f} MB read per cycle, L2 {l2 / 1e6:.0f} MB)",
-            "launch": "CUDA graphs of the step launches" if graphs else "eager launches",
-            "kernel_plan": sv.launch_plan(B, K, V, inp["dtype"], inp.get("draft") is not None),
-            "parallelism": f"{world} independent replica(s), requests sharded per rank"},
+
+    # one more call on the first copy, for the outputs' statistics
+    c = copies[0]
+    acc1, out1 = sv.spec_verify_sample(c["target"], c["draft"], c["draft_tokens"], c["draft_len"],
+                                       c["temperature"], c["uniforms"], c["uniforms_resample"],
+                                       workspace=ws)
+    torch.cuda.synchronize(dev)
+    acc1, out1 = acc1.cpu().numpy(), out1.cpu().numpy()
+
+    def pct(q):
+        return round(times[min(len(times) - 1, int(q * (len(times) - 1) + 0.5))] / K_steps, 6)
+
+    summary = {
+        "workload": WORKLOAD_TEXT[name], "B": B, "K": K, "V": V, "logits_dtype": inp["dtype"],
+        "value": round(value, 1), "unit": "rows/s", "ms_per_step": round(ms_per_step, 6),
+        "ms_per_step_spread": {"min": pct(0.0), "p10": pct(0.1), "median": round(ms_per_step, 6),
+                               "p90": pct(0.9), "max": pct(1.0), "regions": reps,
+                               "steps_per_region": K_steps},
+        "rows_per_step": rows_per_step, "required_bytes_per_step": req_bytes,
+        "l2": f"rotating {n_copies} device copies of the logits "
+              f"({n_copies * req_bytes / 1e6:.0f} MB read per cycle, L2 {l2 / 1e6:.0f} MB)",
+        "launch": "CUDA graphs of the step launches" if graphs else "eager launches",
+        "kernel_plan": sv.launch_plan(B, K, V, inp["dtype"], inp.get("draft") is not None),
         "roofline": {
-            "kernel": "spec_verify_sample (stats_kernel + decide_kernel + residual_kernel + "
-                      "search_kernel, one call)",
+            "kernel": "spec_verify_sample (all kernels of one call, timed together)",
             "bound": "hbm", "achieved": round(achieved, 1),
             "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-            "traffic": recorded_traffic(args.workload),
-            "peak_source": f"{peak_src} HBM copy bandwidth",
+            "traffic": recorded_traffic(name),
+            "peak_source": f"{peak_src} HBM copy bandwidth ({'of measured' if peak_src == 'measured' else 'of fallback'})",
             "algorithmic_bytes_per_launch": req_bytes},
         "gpu_launches": K_steps * KERNELS_PER_SEQUENCE * math.ceil(B / REQUESTS_PER_SEQUENCE),
+        "acceptance": acceptance_stats(inp, acc1),
     }
     if clocks:
-        line["clocks"] = clocks.summary()
+        summary["clocks"] = clocks.summary()
+    del copies, graphs
+    return summary, inp, d0, ws, (acc1, out1)
 
+
+def run_ours(args, torch, world, rank, local):
+    import speculative_decoding_verify_sample_gb300 as sv
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    sv.build()
+    cpu_leg = rank == 0 and world == 1 and not args.no_cpu_baseline
+    head, inp, d0, ws, outs = time_workload(args, torch, sv, args.workload, dev, world, rank)
+    line = {
+        "metric": METRIC, "value": head["value"], "unit": "rows/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded; logits generated, no model weights)",
+        "config": {k: head[k] for k in ("workload", "B", "K", "V", "logits_dtype", "rows_per_step",
+                                        "required_bytes_per_step", "l2", "launch", "kernel_plan")},
+        "ms_per_step_spread": head["ms_per_step_spread"],
+        "roofline": head["roofline"],
+        "gpu_launches": head["gpu_launches"],
+        "acceptance": head["acceptance"],
+    }
+    line["config"]["parallelism"] = f"{world} independent replica(s), requests sharded per rank"
+    if "clocks" in head:
+        line["clocks"] = head["clocks"]
     if not args.no_e2e:
-        line["e2e"] = e2e_rate(args, torch, sv, inp, d0, dev, ws, rows_per_step, world)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, cores, sample = cpu_oracle_rate(inp)
+        line["e2e"] = e2e_rate(args, torch, sv, inp, d0, dev, ws, head["rows_per_step"], world)
+    if cpu_leg:
+        v, cores, sample = cpu_oracle_rate(inp, budget_s=10.0)
         line["cpu_baseline"] = {"value": round(v, 1), "unit": "rows/s", "cores": cores,
                                 "kind": "oracle", "sample": sample,
                                 "single_thread_value": round(cpu_oracle_single_thread_rate(inp), 1),
                                 "cpu_model": cpu_model()}
+        line["parity"] = oracle_parity(inp, *outs)
+    del d0, ws
+    torch.cuda.empty_cache()
+    extra = {}
+    for name in args.also:
+        summ, inp_w, d_w, ws_w, outs_w = time_workload(args, torch, sv, name, dev, world, rank)
+        if cpu_leg:
+            summ["parity"] = oracle_parity(inp_w, *outs_w)
+        extra[name] = summ
+        del inp_w, d_w, ws_w
+        torch.cuda.empty_cache()
+    if extra:
+        line["workloads"] = extra
     return line
 
 

@@ -86,7 +86,9 @@ typedef enum specv_dtype {
 #define SPECV_DEV_BAD_DRAFT_LEN   0x01  /* draft_len[b] outside 1..K               */
 #define SPECV_DEV_BAD_TOKEN       0x02  /* draft_tokens[b,t] outside [0,V), t<n_b  */
 #define SPECV_DEV_BAD_TEMPERATURE 0x04  /* negative, NaN or infinite temperature   */
-#define SPECV_DEV_BAD_UNIFORM     0x08  /* a uniform the request uses not in [0,1) */
+#define SPECV_DEV_BAD_UNIFORM     0x08  /* a value of uniforms[b,0..n_b] or
+                                           uniforms_resample[b] outside [0,1), for
+                                           greedy requests too                   */
 #define SPECV_DEV_BAD_ROW         0x10  /* a row the request needs has no finite max */
 #define SPECV_DEV_NO_DRAFT        0x20  /* T_b > 0 but draft_logits is NULL        */
 #define SPECV_DEV_TIMEOUT         0x40  /* a bounded wait on a copy gave up        */
@@ -98,7 +100,7 @@ typedef enum specv_dtype {
 /* Library version (major*10000 + minor*100 + patch). */
 int specv_version(void);
 
-/* Largest vocabulary supported for a dtype (128 chunks of 16 KB per row):
+/* Largest vocabulary supported for a dtype (2 MB rows, 342 chunks of 6 KB):
  * 1048576 for bf16, 524288 for f32. */
 int specv_max_vocab(specv_dtype dtype);
 
@@ -140,6 +142,7 @@ specv_status specv_workspace_init(void* workspace, size_t workspace_bytes, specv
  *   workspace         specv_workspace_bytes(B, K, V, dtype) bytes, 256-byte aligned,
  *                     zeroed once with specv_workspace_init.  Calls that may
  *                     run concurrently need separate workspaces.
+ *   stream            a stream of the current device (all buffers on it).
  * Enqueues four kernels on `stream` per 1024 requests (row statistics,
  * decisions, residual piece sums with the bonus draws, residual searches;
  * each as a programmatic dependent launch); no host synchronisation.
@@ -227,9 +230,10 @@ specv_status specv_launch_plan(int B, int K, int V, specv_dtype dtype, int with_
  * holds it until the process exits.  Shapes whose workspace
  * (specv_workspace_bytes) exceeds it return SPECV_ERR_UNSUPPORTED.
  *   - It calls no cudaMalloc, cudaFree or allocating library routine.
- *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current) and caches it; make
- *     that first call before any stream capture.
+ *   - Every call looks up the array's device address in the current
+ *     device's context (cudaGetSymbolAddress); the first call on a device
+ *     may load the library's module there, so make it before any stream
+ *     capture.  `stream` must belong to the current device.
  *   - Each call zeroes the part of the array it uses (cudaMemsetAsync on
  *     `stream`), then launches the kernels.  All calls on a device share the
  *     one array: calls that may overlap on the GPU (different streams, or

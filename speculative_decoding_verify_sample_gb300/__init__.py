@@ -151,8 +151,9 @@ def _run(fn_name, target, draft, draft_tokens, draft_len, temperature, uniforms,
             _ptr(accepted_len), _ptr(out_tokens), workspace.tensor.data_ptr(), workspace.nbytes]
     if row_stats is not None:
         args.append(_ptr(row_stats))
-    args.append(_stream_ptr(stream, dev))
-    check(fn_name, getattr(lib(), fn_name)(*args))
+    with torch.cuda.device(dev):   # the library works on the current device
+        args.append(_stream_ptr(stream, dev))
+        check(fn_name, getattr(lib(), fn_name)(*args))
     return accepted_len, out_tokens
 
 
@@ -221,12 +222,20 @@ def spec_verify_sample_host(target_logits, draft_logits, draft_tokens, draft_len
     if out_tokens is None:
         out_tokens = torch.empty((B, K + 1), dtype=torch.int32).pin_memory()
     dev = staging.tensor.device
+    with torch.cuda.device(dev):
+        _host_call(target_logits, draft_logits, draft_tokens, draft_len, temperature, uniforms,
+                   uniforms_resample, B, K, V, accepted_len, out_tokens, staging, workspace,
+                   _stream_ptr(stream, dev))
+    return accepted_len, out_tokens
+
+
+def _host_call(target_logits, draft_logits, draft_tokens, draft_len, temperature, uniforms,
+               uniforms_resample, B, K, V, accepted_len, out_tokens, staging, workspace, stream):
     check("spec_verify_sample_host", lib().spec_verify_sample_host(
         _ptr(target_logits), _ptr(draft_logits), _dtype_code(target_logits), _ptr(draft_tokens),
         _ptr(draft_len), _ptr(temperature), _ptr(uniforms), _ptr(uniforms_resample), B, K, V,
         _ptr(accepted_len), _ptr(out_tokens), staging.tensor.data_ptr(), staging.nbytes,
-        workspace.tensor.data_ptr(), workspace.nbytes, _stream_ptr(stream, dev)))
-    return accepted_len, out_tokens
+        workspace.tensor.data_ptr(), workspace.nbytes, stream))
 
 
 def spec_verify_sample_noalloc(target_logits, draft_logits, draft_tokens, draft_len, temperature,
@@ -249,8 +258,10 @@ def spec_verify_sample_noalloc(target_logits, draft_logits, draft_tokens, draft_
         if (t is None or tuple(t.shape) != shape or t.dtype != torch.int32 or t.device != dev
                 or not t.is_contiguous()):
             raise ValueError(f"{name} must be a preallocated int32 tensor {shape} on {dev}")
-    check("spec_verify_sample_noalloc", lib().spec_verify_sample_noalloc(
-        _ptr(target_logits), _ptr(draft_logits), _dtype_code(target_logits), _ptr(draft_tokens),
-        _ptr(draft_len), _ptr(temperature), _ptr(uniforms), _ptr(uniforms_resample), B, K, V,
-        _ptr(accepted_len), _ptr(out_tokens), _stream_ptr(stream, dev)))
+    with torch.cuda.device(dev):   # its scratch array is the current device's
+        check("spec_verify_sample_noalloc", lib().spec_verify_sample_noalloc(
+            _ptr(target_logits), _ptr(draft_logits), _dtype_code(target_logits),
+            _ptr(draft_tokens), _ptr(draft_len), _ptr(temperature), _ptr(uniforms),
+            _ptr(uniforms_resample), B, K, V, _ptr(accepted_len), _ptr(out_tokens),
+            _stream_ptr(stream, dev)))
     return accepted_len, out_tokens

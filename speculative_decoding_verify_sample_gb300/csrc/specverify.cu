@@ -35,8 +35,9 @@
 //     piece from the piece sums, the sweep from that piece's sweep sums,
 //     the token from the sweep of both rows read again.
 //
-// Every wait (a bulk copy, the queue, a record another warp writes) is
-// bounded in time and sets a status bit when it gives up.
+// The only waits are a warp's waits on its own bulk copies; each is
+// bounded in time and sets a status bit when it gives up.  No warp waits on
+// data another warp or CTA produces: kernel boundaries order all of it.
 
 #include <cuda_runtime.h>
 
@@ -143,7 +144,6 @@ struct __align__(16) Item {
   int n;        // the request's draft length
   float sT;     // log2(e)/T (0: greedy)
   int x;        // drafted token of the row (rows t < n of sampled requests), else -1
-  int bonus;    // unused (0)
   float4 prm;   // residual: the decision's Mp, Mq, log2(e)/T, S_p/S_q
 };
 
@@ -629,13 +629,10 @@ __device__ __forceinline__ int count_le(const int* a, int n, int x) {
   return lo;
 }
 
-// A decoded item in 16 bytes: bonus row << 30 | kind << 28 | b << 15 |
-// row << 9 | chunk, the
-// drafted token of the row (or -1), log2(e)/T (0: greedy), draft length.
-__device__ __forceinline__ uint4 pack_item(int kind, int b, int row, int c, int x, float sT, int n,
-                                           bool bonus) {
-  return make_uint4((bonus ? 0x40000000u : 0u) | (static_cast<uint32_t>(kind) << 28) |
-                        (static_cast<uint32_t>(b) << 15) |
+// A decoded item in 16 bytes: kind << 28 | b << 15 | row << 9 | chunk,
+// the drafted token of the row (or -1), log2(e)/T (0: greedy), draft length.
+__device__ __forceinline__ uint4 pack_item(int kind, int b, int row, int c, int x, float sT, int n) {
+  return make_uint4((static_cast<uint32_t>(kind) << 28) | (static_cast<uint32_t>(b) << 15) |
                         (static_cast<uint32_t>(row) << 9) | static_cast<uint32_t>(c),
                     static_cast<uint32_t>(x), __float_as_uint(sT), static_cast<uint32_t>(n));
 }
@@ -648,7 +645,6 @@ __device__ __forceinline__ Item unpack_item(uint4 e) {
   it.x = static_cast<int>(e.y);
   it.sT = __uint_as_float(e.z);
   it.n = static_cast<int>(e.w);
-  it.bonus = (e.x >> 30) & 1u;
   it.prm = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
   return it;
 }
@@ -667,7 +663,7 @@ __device__ uint4 decode_ticket(const Params& P, const Plan& pl, int t) {
   const int row = slot_row(slot, sampled, n, P.K);
   int x = -1;
   if (sampled && slot < 2 * n) x = __ldg(P.draft_tokens + static_cast<size_t>(b) * P.K + (slot >> 1));
-  return pack_item(kItemA, b, row, c, x, sT, n, false);
+  return pack_item(kItemA, b, row, c, x, sT, n);
 }
 // ---------------------------------------------------------------- chunk reductions
 
@@ -872,34 +868,10 @@ __device__ __forceinline__ void vector_weights(const unsigned char* slot, const 
   }
 }
 
-// Whole warp: the final-draw mass of a draw chunk: per sweep of 32 vectors
-// (sweep s = vectors [32 s, 32 s + 32) of the target part) each lane's
-// elements in order, then across the warp, then the sweeps in order (as
-// draw_in_slot walks them).
-template <int DT>
-__device__ __forceinline__ float chunk_draw(const unsigned char* slot, const Chunk& kp,
-                                            const Chunk& kq, bool residual, const float4& prm,
-                                            int lane) {
-  constexpr int CH = Elt<DT>::kPerVec;
-  const Vecs vs = vecs_of<DT>(kp);
-  const bool same = kq.off0 == kp.off0;   // draft elements at the target's positions
-  float t = 0.0f;
-#pragma unroll 1
-  for (int s = 0; s < kDrawSweeps; ++s) {
-    float w[CH];
-    vector_weights<DT>(slot, vs, kp, kq, residual, same, prm, s * 32 + lane, w);
-    float s0 = 0.0f;
-#pragma unroll
-    for (int q = 0; q < CH; ++q) s0 = __fadd_rn(s0, w[q]);
-    t = __fadd_rn(t, warp_sum(s0));
-  }
-  return t;
-}
-
 // Whole warp: the final draw's token inside a chunk staged in a slot.
 // `tau` is the target mass left for this chunk; sweeps (32 vectors each)
-// are summed in order as chunk_draw sums them, then lanes in order, then
-// the lane's elements.  Rounding that leaves tau beyond the chunk's mass
+// are summed in order (each lane's elements, then across the warp), then
+// lanes in order, then the lane's elements.  Rounding that leaves tau beyond the chunk's mass
 // falls on the chunk's last positive element.  -1 if nothing weighs > 0.
 template <int DT>
 __device__ int draw_in_slot(const unsigned char* slot, const Chunk& kp, const Chunk& kq,
@@ -989,7 +961,7 @@ __device__ __forceinline__ float sweep_totals(float (&v)[N], int lane) {
 }
 
 // Whole warp: the residual mass of a piece pair in a slot, sweep by sweep
-// (as chunk_draw forms the weights).  Returns the piece's total; `mine`
+// (weights formed by vector_weights, as the search forms them).  Returns the piece's total; `mine`
 // gets the sum of sweep lane >> 2 (lanes 4 s hold sweep s).
 template <int DT>
 __device__ float piece_sweeps(const unsigned char* slot, const Chunk& kp, const Chunk& kq,
@@ -1971,14 +1943,13 @@ __device__ __forceinline__ Item residual_item(const Params& P, int i) {
   it.prm = r.prm;
   it.sT = 0.0f;
   it.x = -1;
-  it.bonus = 0;
   return it;
 }
 
 __device__ __forceinline__ Item residual_pick_init() {
   Item it;
   it.kind = kItemR;
-  it.b = it.row = it.c = it.n = it.x = it.bonus = 0;
+  it.b = it.row = it.c = it.n = it.x = 0;
   it.sT = 0.0f;
   it.prm = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
   return it;
@@ -1998,7 +1969,6 @@ __device__ __forceinline__ Item residual_pick(const Item& mine, int l) {
   it.prm.w = __shfl_sync(0xffffffffu, mine.prm.w, l);
   it.sT = 0.0f;
   it.x = -1;
-  it.bonus = 0;
   return it;
 }
 
@@ -2296,25 +2266,17 @@ size_t pad256(size_t x) { return align256(x); }
 // process exits, and every call on a device shares it.
 __device__ __align__(256) unsigned char g_noalloc_scratch[SPECV_NOALLOC_SCRATCH_BYTES];
 
-// Device address of g_noalloc_scratch on the current device.  In host code
-// the symbol's name is only a host-side handle, so the address is looked up
-// once per device with cudaGetSymbolAddress (with that device current) and
-// cached.
+// Device address of g_noalloc_scratch in the current device's context.  In
+// host code the symbol's name is only a host-side handle, so the address is
+// looked up with cudaGetSymbolAddress, with the device current, on every
+// call: a lookup is a host-side table read once the module is loaded, and a
+// context that was reset and recreated (cudaDeviceReset) gets its new
+// address instead of a stale one.
 cudaError_t noalloc_scratch(void** out) {
-  static std::mutex mu;
-  static void* addr[64] = {nullptr};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return e;
-    addr[dev] = p;
-  }
-  *out = addr[dev];
+  *out = p;
   return cudaSuccess;
 }
 

@@ -14,10 +14,16 @@ sharing any of the method.
   needs no normaliser.  A T = 0 request drafts the draft row's own argmax.
 * bf16 logits are rounded from fp32 with round-to-nearest-even and stored as
   raw uint16.
-* The greedy workload plants the target row's maximum: every target row gets
-  the value 16.0 at a random index g and every other entry clipped to at most
-  15.9375, so argmax = g by construction; the draft token is g with
-  probability 0.8 and otherwise uniform over the other V - 1 tokens.
+* The greedy workload draws target logits N(0, 3^2) in bf16 with nothing
+  planted, so exact ties at a row's maximum occur (about one row in ten at
+  V = 128256).  The draft model is the target itself at a position with
+  probability 0.8 and an independent N(0, 3^2) row otherwise, and it
+  proposes its own top token (lowest index on ties), so the drafted token
+  is the target's argmax with probability about 0.8.
+* The planted greedy workload instead gives every target row the value 16.0
+  at a random index g and clips every other entry to at most 15.9375, so
+  argmax = g by construction; the draft token is g with probability 0.8 and
+  otherwise uniform over the other V - 1 tokens.
 * The long ragged workload uses constant-overlap pairs: r = softmax(3 * N(0,1))
   over V, a random half A of the vocabulary and its complement A', and
   p = alpha*r + (1-alpha)*r|A, q = alpha*r + (1-alpha)*r|A' (each restriction
@@ -38,11 +44,13 @@ WORKLOADS = {
     "tiny_greedy": (4, 4, 1024, "f32"),
     "llama3": (32, 4, 128256, "bf16"),
     "greedy": (256, 4, 128256, "bf16"),
+    "greedy_planted": (256, 4, 128256, "bf16"),
     "dsv3_mtp": (512, 1, 129280, "bf16"),
     "ragged": (128, 8, 128256, "f32"),
 }
 
-DEFAULT_SEED = {"tiny": 0, "tiny_greedy": 0, "llama3": 1, "greedy": 2, "dsv3_mtp": 3, "ragged": 4}
+DEFAULT_SEED = {"tiny": 0, "tiny_greedy": 0, "llama3": 1, "greedy": 2, "dsv3_mtp": 3, "ragged": 4,
+                "greedy_planted": 5}
 
 RAGGED_ALPHAS = (0.5, 0.8, 0.95)
 
@@ -78,8 +86,11 @@ def gumbel_draw(rng: np.random.Generator, z: np.ndarray, T: np.ndarray) -> np.nd
     out = np.empty(R, np.int32)
     for lo in range(0, R, _ROW_CHUNK):
         hi = min(R, lo + _ROW_CHUNK)
-        zz = np.asarray(z[lo:hi], np.float64)
         tt = np.asarray(T[lo:hi], np.float64)
+        if not np.any(tt > 0):     # every row drafts its own top token: no noise drawn
+            out[lo:hi] = np.argmax(np.asarray(z[lo:hi]), axis=1)
+            continue
+        zz = np.asarray(z[lo:hi], np.float64)
         u = rng.random(zz.shape)
         g = -np.log(-np.log(np.clip(u, 1e-300, 1.0 - 1e-16)))
         hot = tt > 0
@@ -137,6 +148,26 @@ def _llama3(seed):
 
 def _greedy(seed):
     B, K, V, dt = WORKLOADS["greedy"]
+    rng = np.random.default_rng(seed)
+    urng = np.random.default_rng(seed + 1000)
+    tgt = bf16_bits(3.0 * rng.standard_normal((B, K + 1, V), dtype=np.float32))
+    # the draft model: the target's own row at a position w.p. 0.8, else an
+    # independent row; it proposes its top token (T = 0 drafting)
+    same = rng.random((B, K)) < 0.8
+    toks = np.empty((B, K), np.int32)
+    for b in range(B):
+        rows = bf16_to_f32(tgt[b, :K]).copy()
+        other = ~same[b]
+        if other.any():
+            rows[other] = bf16_to_f32(bf16_bits(
+                3.0 * rng.standard_normal((int(other.sum()), V), dtype=np.float32)))
+        toks[b] = gumbel_draw(rng, rows, np.zeros(K))
+    T = np.zeros(B, np.float32)
+    return _pack(B, K, V, dt, tgt, None, toks, None, T, urng, draft_is_target=same)
+
+
+def _greedy_planted(seed):
+    B, K, V, dt = WORKLOADS["greedy_planted"]
     rng = np.random.default_rng(seed)
     urng = np.random.default_rng(seed + 1000)
     z = 3.0 * rng.standard_normal((B, K + 1, V), dtype=np.float32)
@@ -210,7 +241,8 @@ def make_inputs(name: str, seed: int | None = None) -> dict:
         seed = DEFAULT_SEED[name]
     if name in ("tiny", "tiny_greedy"):
         return _tiny(seed, name == "tiny_greedy")
-    return {"llama3": _llama3, "greedy": _greedy, "dsv3_mtp": _dsv3, "ragged": _ragged}[name](seed)
+    return {"llama3": _llama3, "greedy": _greedy, "greedy_planted": _greedy_planted,
+            "dsv3_mtp": _dsv3, "ragged": _ragged}[name](seed)
 
 
 def random_case(seed: int, B: int, K: int, V: int, dtype: str = "f32", *, scale: float = 2.0,

@@ -49,7 +49,7 @@ def test_limits_and_sizes(L):
     assert L.specv_workspace_bytes(4, 4, 0, 1) == 0
     assert L.specv_workspace_bytes(4, 4, 1000, 5) == 0
     assert L.specv_workspace_bytes(4, 4, L.specv_max_vocab(1) + 1, 1) == 0
-    # at least one 8-byte partial per (request, row, 16 KB chunk)
+    # at least one 8-byte record per (request, row, chunk of at most 16 KB)
     assert L.specv_workspace_bytes(32, 4, 128256, 1) >= 32 * 9 * 16 * 8
     assert L.specv_workspace_bytes(32, 4, 128256, 0) > L.specv_workspace_bytes(32, 4, 128256, 1)
     assert L.specv_host_staging_bytes(2, 2, 100, 1, 1) >= 2 * 3 * 100 * 2 + 2 * 2 * 100 * 2

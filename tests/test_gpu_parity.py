@@ -8,8 +8,8 @@ import numpy as np
 import pytest
 
 import oracle
-from helpers import (assert_outputs_match, assert_row_stats_match, oracle_subset, run_gpu,
-                     to_device)
+from helpers import (assert_outputs_match, assert_row_stats_match, oracle_subset, report_parity,
+                     run_gpu, to_device)
 from speculative_decoding_verify_sample_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -26,10 +26,10 @@ def _lib():
     sv.lib()
 
 
-def _full_check(inp, debug=True, nthreads=8):
+def _full_check(inp, debug=True, nthreads=8, label=None):
     acc_o, out_o, flags_o = oracle.verify_sample(inp, nthreads=nthreads)
     acc_g, out_g = run_gpu(inp)
-    ties = assert_outputs_match(inp, acc_g, out_g, acc_o, out_o, flags_o)
+    ties = assert_outputs_match(inp, acc_g, out_g, acc_o, out_o, flags_o, label=label)
     if debug:
         acc_d, out_d, rs = run_gpu(inp, debug=True)
         assert np.array_equal(acc_d, acc_g) and np.array_equal(out_d, out_g)
@@ -39,7 +39,7 @@ def _full_check(inp, debug=True, nthreads=8):
 
 
 def test_tiny_sampled():
-    _full_check(synth.make_inputs("tiny"))
+    _full_check(synth.make_inputs("tiny"), label="tiny")
 
 
 def test_tiny_greedy_bit_exact():
@@ -70,7 +70,7 @@ RANDOM_CASES = [
 def test_random_shapes(seed, B, K, V, dtype, T, draft_len, greedy_frac):
     inp = synth.random_case(seed, B, K, V, dtype, scale=2.0, noise=0.6, temperature=T,
                             draft_len=draft_len, greedy_frac=greedy_frac)
-    _full_check(inp)
+    _full_check(inp, label=f"random{seed}")
 
 
 def test_greedy_ties_lowest_index_bf16():
@@ -175,19 +175,39 @@ def test_host_entry_point_matches_device():
 # ---------------------------------------------------------------- full sizes
 
 
-def test_llama3_full():
-    inp = synth.make_inputs("llama3")
-    acc_o, out_o, flags_o = oracle.verify_sample(inp, nthreads=16)
-    acc_g, out_g, rs = run_gpu(inp, debug=True)
-    assert_outputs_match(inp, acc_g, out_g, acc_o, out_o, flags_o)
-    rows = np.arange(0, inp["B"], 4)
+def _row_stats_check(inp, rs, acc_g, rows):
     sub, *_ = oracle_subset(inp, rows)
     info = oracle.row_stats(sub, nthreads=16)
     assert_row_stats_match(inp, rs, info, acc_g, rows=rows)
 
 
-def test_greedy_full_bit_exact_against_planted_argmax():
+def test_llama3_full():
+    inp = synth.make_inputs("llama3")
+    acc_o, out_o, flags_o = oracle.verify_sample(inp, nthreads=16)
+    acc_g, out_g, rs = run_gpu(inp, debug=True)
+    assert_outputs_match(inp, acc_g, out_g, acc_o, out_o, flags_o, label="llama3")
+    _row_stats_check(inp, rs, acc_g, np.arange(inp["B"]))
+
+
+def test_greedy_full_bit_exact_with_ties_at_the_maximum():
+    # N(0, 3^2) bf16 logits, nothing planted: some rows hold their maximum
+    # at several indices, and the lowest must win
     inp = synth.make_inputs("greedy")
+    z = synth.bf16_to_f32(inp["target"])
+    tied_rows = int(((z == z.max(axis=2, keepdims=True)).sum(axis=2) > 1).sum())
+    del z
+    assert tied_rows >= 20
+    acc_o, out_o, _ = oracle.verify_sample(inp, nthreads=16)
+    acc_g, out_g, rs = run_gpu(inp, debug=True)
+    assert np.array_equal(acc_g, acc_o) and np.array_equal(out_g, out_o)
+    info = oracle.row_stats(inp, nthreads=16)
+    assert_row_stats_match(inp, rs, info, acc_g)     # every row's argmax and maximum
+    report_parity({"label": "greedy", "compared": int(inp["B"]), "sampled": 0, "excused": 0,
+                   "tied_rows": tied_rows})
+
+
+def test_greedy_planted_full_against_construction():
+    inp = synth.make_inputs("greedy_planted")
     acc_g, out_g = run_gpu(inp)
     g = inp["planted_argmax"]
     x = inp["draft_tokens"]
@@ -196,23 +216,24 @@ def test_greedy_full_bit_exact_against_planted_argmax():
         j = next((t for t in range(K) if g[b, t] != x[b, t]), K)
         assert acc_g[b] == j
         assert list(out_g[b]) == list(x[b, :j]) + [g[b, j]] + [-1] * (K - j)
-    rows = np.arange(0, inp["B"], 8)
-    _, acc_o, out_o, flags_o = oracle_subset(inp, rows, nthreads=16)
-    assert_outputs_match(inp, acc_g, out_g, acc_o, out_o, flags_o, rows=rows)
+    acc_o, out_o, flags_o = oracle.verify_sample(inp, nthreads=16)
+    assert np.array_equal(acc_g, acc_o) and np.array_equal(out_g, out_o)
 
 
 def test_dsv3_mtp_full():
     inp = synth.make_inputs("dsv3_mtp")
     acc_o, out_o, flags_o = oracle.verify_sample(inp, nthreads=16)
-    acc_g, out_g = run_gpu(inp)
-    assert_outputs_match(inp, acc_g, out_g, acc_o, out_o, flags_o)
+    acc_g, out_g, rs = run_gpu(inp, debug=True)
+    assert_outputs_match(inp, acc_g, out_g, acc_o, out_o, flags_o, label="dsv3_mtp")
+    _row_stats_check(inp, rs, acc_g, np.arange(0, inp["B"], 2))
 
 
 def test_ragged_full():
     inp = synth.make_inputs("ragged")
     acc_o, out_o, flags_o = oracle.verify_sample(inp, nthreads=16)
-    acc_g, out_g = run_gpu(inp)
-    assert_outputs_match(inp, acc_g, out_g, acc_o, out_o, flags_o)
+    acc_g, out_g, rs = run_gpu(inp, debug=True)
+    assert_outputs_match(inp, acc_g, out_g, acc_o, out_o, flags_o, label="ragged")
+    _row_stats_check(inp, rs, acc_g, np.arange(0, inp["B"], 2))
     # the realised mean of emitted tokens follows the closed form per alpha
     n = inp["draft_len"]
     for a in synth.RAGGED_ALPHAS:
@@ -220,6 +241,49 @@ def test_ragged_full():
         want = np.mean([(1 - a ** (k + 1)) / (1 - a) for k in n[sel]])
         got = (acc_g[sel] + 1).mean()
         assert abs(got - want) < 4 * max((acc_g[sel] + 1).std(), 0.5) / np.sqrt(sel.sum())
+
+
+def test_constructed_near_ties_and_zero_residual():
+    # requests built so that the oracle's flags are known: a zero-mass
+    # residual (both sides must fall back to p), a residual of mass ~1e-3
+    # drawn far from its one interior edge (no flag: must match exactly), and
+    # accept ratios a little off u (flagged or not)
+    rows_p, rows_q, toks, us, urs = [], [], [], [], []
+
+    def add(zp, zq, x, u, ur):
+        rows_p.append(np.asarray(zp, np.float32))
+        rows_q.append(np.asarray(zq, np.float32))
+        toks.append(x)
+        us.append(u)
+        urs.append(ur)
+
+    V = 8
+    pad = np.full(V - 3, -np.inf)
+    zq0 = np.r_[0.0, 0.0, -40.0, pad]
+    zp0 = np.r_[0.0, 0.0, -40.5, pad]
+    for ur in (0.1, 0.3, 0.7, 0.9):                        # zero residual: draw from p
+        add([zp0, np.r_[0.0, 0.0, 0.0, pad]], [zq0], [2], [0.9, 0.5], ur)
+    zp1 = np.r_[np.log([0.2505, 0.2505, 0.249, 0.25]), np.full(V - 4, -np.inf)]
+    zq1 = np.r_[np.zeros(4), np.full(V - 4, -np.inf)]
+    for ur in (0.1, 0.25, 0.75, 0.95):                      # residual of mass ~1e-3
+        add([zp1, zq1], [zq1], [2], [0.999, 0.5], ur)
+    zp2 = np.r_[np.log([0.5, 0.5]), np.full(V - 2, -np.inf)]
+    zq2 = np.r_[np.log([0.8, 0.2]), np.full(V - 2, -np.inf)]
+    for d in (-3e-4, -5e-5, 5e-5, 3e-4):                    # accept ratio 0.625 +- d
+        add([zp2, zp2], [zq2], [0], [0.625 + d, 0.3], 0.5)
+    B = len(toks)
+    inp = dict(B=B, K=1, V=V, dtype="f32", target=np.stack([np.stack(r) for r in rows_p]),
+               draft=np.stack([np.stack(r) for r in rows_q]),
+               draft_tokens=np.asarray(toks, np.int32).reshape(B, 1), draft_len=None,
+               temperature=np.ones(B, np.float32),
+               uniforms=np.asarray(us, np.float32).reshape(B, 2),
+               uniforms_resample=np.asarray(urs, np.float32))
+    acc_o, out_o, flags_o = oracle.verify_sample(inp)
+    assert np.all(flags_o[:4] & oracle.RES_FALLBACK)
+    assert np.all(flags_o[4:8] == 0)
+    acc_g, out_g = run_gpu(inp)
+    assert np.array_equal(acc_g[:8], acc_o[:8]) and np.array_equal(out_g[:8], out_o[:8])
+    assert_outputs_match(inp, acc_g, out_g, acc_o, out_o, flags_o, label="constructed")
 
 
 def test_batch_beyond_one_launch_sequence():
