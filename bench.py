@@ -507,7 +507,7 @@ def time_workload(args, torch, sv, name, dev, world, rank):
         "launch": "CUDA graphs of the step launches" if graphs else "eager launches",
         "kernel_plan": sv.launch_plan(B, K, V, inp["dtype"], inp.get("draft") is not None),
         "roofline": {
-            "kernel": "spec_verify_sample (all kernels of one call, timed together)",
+            "kernel": "spec_verify_sample (stats_kernel + decide_kernel + residual_kernel + search_kernel, one call, timed together)",
             "bound": "hbm", "achieved": round(achieved, 1),
             "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
             "traffic": recorded_traffic(name),
