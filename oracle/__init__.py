@@ -70,6 +70,20 @@ def _load():
                                              ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, ctypes.c_int]
             lib.oracle_row_stats.restype = ctypes.c_int
             lib.oracle_version.restype = ctypes.c_int
+            lib.oracle_sample_draft.argtypes = [vp, ctypes.c_int, f32p, f32p, ctypes.c_int,
+                                                ctypes.c_int, i32p, i32p, ctypes.c_int]
+            lib.oracle_sample_draft.restype = ctypes.c_int
+            lib.oracle_verify_onehot.argtypes = [vp, ctypes.c_int, i32p, i32p, f32p, f32p, f32p,
+                                                 ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                 i32p, i32p, i32p, ctypes.c_int]
+            lib.oracle_verify_onehot.restype = ctypes.c_int
+            lib.oracle_tree_greedy.argtypes = [vp, ctypes.c_int, i32p, i32p, i32p, ctypes.c_int,
+                                               ctypes.c_int, ctypes.c_int, i32p, i32p, i32p,
+                                               ctypes.c_int]
+            lib.oracle_tree_greedy.restype = ctypes.c_int
+            lib.oracle_insert_accepted.argtypes = [i32p, i32p, ctypes.c_int, ctypes.c_int, i32p,
+                                                   i32p, ctypes.c_int, i32p, i32p, i32p, i32p]
+            lib.oracle_insert_accepted.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -130,3 +144,90 @@ def row_stats(inp, nthreads: int = 1):
     if rc != 0:
         raise ValueError("oracle_row_stats rejected its arguments")
     return info
+
+
+def _logits(a, dtype):
+    return np.ascontiguousarray(a, dtype=np.uint16 if dtype == "bf16" else np.float32)
+
+
+def sample_draft(logits, dtype, temperature, uniforms, nthreads: int = 1):
+    """The draft-side sampler ("Decodificación Especulativa y EAGLE", sections
+    "La Configuración de Dos Modelos", "Desarrolla"): one token per row of
+    ``logits`` [R, V] from softmax(z / T) by inverse CDF with ``uniforms``
+    [R]; the row's lowest-index argmax at T = 0.  Returns (tokens [R],
+    flags [R]) int32 (flags: TIE_CDF / PRECISION_BAND near-ties, BAD_INPUT)."""
+    lib = _load()
+    z = _logits(logits, dtype)
+    R, V = z.shape
+    T = np.ascontiguousarray(temperature, np.float32)
+    u = np.ascontiguousarray(uniforms, np.float32)
+    assert T.size == R and u.size == R
+    tok = np.empty(R, np.int32)
+    flags = np.empty(R, np.int32)
+    rc = lib.oracle_sample_draft(_ptr(z), DTYPES[dtype], _ptr(T), _ptr(u), R, V, _ptr(tok),
+                                 _ptr(flags), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_sample_draft rejected its arguments")
+    return tok, flags
+
+
+def verify_onehot(inp, nthreads: int = 1):
+    """The verification rule for a draft that proposes its top token (q is
+    the point mass at the drafted token; ``inp`` as for verify_sample, draft
+    logits unused).  Returns (accepted_len [B], out_tokens [B,K+1], flags [B])."""
+    lib = _load()
+    tgt, _, dt, toks, dl, temp, uni, ur, B, K, V = _prep(dict(inp, draft=None))
+    acc = np.empty(B, np.int32)
+    out = np.empty((B, K + 1), np.int32)
+    flags = np.empty(B, np.int32)
+    rc = lib.oracle_verify_onehot(_ptr(tgt), dt, _ptr(toks), _ptr(dl), _ptr(temp), _ptr(uni),
+                                  _ptr(ur), B, K, V, _ptr(acc), _ptr(out), _ptr(flags),
+                                  int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_verify_onehot rejected its arguments")
+    return acc, out, flags
+
+
+def tree_greedy(target, dtype, parents, tokens, n_nodes, nthreads: int = 1):
+    """Greedy verification of a token tree ("Decodificación Especulativa y
+    EAGLE", section "Verificación de Atención en Árvore"): ``target`` [B, N, V]
+    logits per tree node, ``parents`` [B, N] (-1 at the root, else < i),
+    ``tokens`` [B, N], ``n_nodes`` [B].  Returns (accepted_len [B],
+    out_tokens [B, N], path_nodes [B, N]) int32."""
+    lib = _load()
+    z = _logits(target, dtype)
+    B, N, V = z.shape
+    par = np.ascontiguousarray(parents, np.int32).reshape(B, N)
+    tok = np.ascontiguousarray(tokens, np.int32).reshape(B, N)
+    nn = np.ascontiguousarray(n_nodes, np.int32).reshape(B)
+    acc = np.empty(B, np.int32)
+    out = np.empty((B, N), np.int32)
+    path = np.empty((B, N), np.int32)
+    rc = lib.oracle_tree_greedy(_ptr(z), DTYPES[dtype], _ptr(par), _ptr(tok), _ptr(nn), B, N, V,
+                                _ptr(acc), _ptr(out), _ptr(path), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_tree_greedy rejected its arguments")
+    return acc, out, path
+
+
+def insert_accepted(accepted_len, out_tokens, seq_lens, history):
+    """The post-accept insert ("Accelerating Sonar through speculation",
+    section "Programación MTP para un solo token").  Returns (seq_lens [B],
+    history [B, L], next_tokens [B], cu_emitted [B+1], packed [B*(K+1)],
+    status [B]); the inputs are not modified."""
+    lib = _load()
+    acc = np.ascontiguousarray(accepted_len, np.int32)
+    out = np.ascontiguousarray(out_tokens, np.int32)
+    B, K1 = out.shape
+    seq = np.array(seq_lens, np.int32, copy=True)
+    hist = np.array(history, np.int32, copy=True)
+    L = hist.shape[1]
+    nxt = np.empty(B, np.int32)
+    cu = np.empty(B + 1, np.int32)
+    packed = np.full(B * K1, -1, np.int32)
+    status = np.empty(B, np.int32)
+    rc = lib.oracle_insert_accepted(_ptr(acc), _ptr(out), B, K1, _ptr(seq), _ptr(hist), L,
+                                    _ptr(nxt), _ptr(cu), _ptr(packed), _ptr(status))
+    if rc != 0:
+        raise ValueError("oracle_insert_accepted rejected its arguments")
+    return seq, hist, nxt, cu, packed, status

@@ -378,6 +378,150 @@ void row_stats_request(const Args& a, int b, std::vector<double>& zp, std::vecto
   }
 }
 
+// ---------------------------------------------------------------- draft-side sampler
+//
+// "Decodificación Especulativa y EAGLE", sections "La Configuración de Dos
+// Modelos" and "Desarrolla": the draft model proposes each token by sampling
+// x ~ softmax(z / T) from its logits at temperature T (its top token at
+// T = 0).  One row per request; the uniform u drives the inverse CDF.
+
+void sample_row(const void* logits, int dtype, size_t row, int V, double T, double u,
+                std::vector<double>& z, std::vector<double>& p, int32_t* token, int32_t* flag) {
+  load_row(logits, dtype, row, V, z);
+  if (T == 0.0) {
+    *token = argmax_lowest(z);
+    *flag = 0;
+    return;
+  }
+  double zmax, S;
+  if (!softmax_T(z, T, p, zmax, S)) {
+    *token = -1;
+    *flag = kBadInput;
+    return;
+  }
+  int edge = 0;
+  *token = inverse_cdf(p, comp_total(p), u, &edge);
+  *flag = edge;
+}
+
+// ---------------------------------------------------------------- one-hot draft
+//
+// "Accelerating Sonar through speculation", section "Objetivo-Borrador": the
+// draft proposes its top token, so the distribution x was drawn from is the
+// point mass q = 1{x}.  The rule of "La Regla de Exactitud" with that q:
+// accept x_t iff u_t < p_t(x_t) / 1; at the first rejection j draw from
+// (p_j - 1{x_j})+ / ||.||_1, which is p_j with x_j removed and renormalised
+// (p_j(x_j) - 1 <= 0); if every draft is accepted, the bonus token from p_n.
+
+void onehot_request(const Args& a, int b, std::vector<double>& zp, std::vector<double>& p,
+                    std::vector<double>& w) {
+  const int n = a.draft_len ? a.draft_len[b] : a.K;
+  const double T = a.temperature[b];
+  bool ok = n >= 1 && n <= a.K && T >= 0.0 && std::isfinite(T);
+  const int32_t* x = a.draft_tokens + static_cast<size_t>(b) * a.K;
+  const float* u = a.uniforms + static_cast<size_t>(b) * (a.K + 1);
+  for (int t = 0; ok && t < n; ++t) ok = x[t] >= 0 && x[t] < a.V;
+  for (int t = 0; ok && t <= n; ++t) ok = u[t] >= 0.0f && u[t] < 1.0f;
+  ok = ok && a.uniforms_resample[b] >= 0.0f && a.uniforms_resample[b] < 1.0f;
+  const size_t trow0 = static_cast<size_t>(b) * (a.K + 1);
+  if (ok && T > 0.0)
+    for (int t = 0; t <= n; ++t) ok = ok && row_has_finite_max(a.target, a.dtype, trow0 + t, a.V);
+  if (!ok) {
+    write_outputs(a, b, -1, {}, kBadInput);
+    return;
+  }
+  std::vector<int> tokens;
+  int flags = 0;
+  if (T == 0.0) {   // the greedy rule, as for any draft ("Caso codicioso")
+    for (int t = 0; t <= n; ++t) {
+      load_row(a.target, a.dtype, trow0 + t, a.V, zp);
+      const int g = argmax_lowest(zp);
+      if (t < n && g == x[t]) { tokens.push_back(x[t]); continue; }
+      tokens.push_back(g);
+      write_outputs(a, b, t, tokens, 0);
+      return;
+    }
+  }
+  double zmax, S;
+  for (int t = 0; t < n; ++t) {
+    load_row(a.target, a.dtype, trow0 + t, a.V, zp);
+    softmax_T(zp, T, p, zmax, S);
+    const double logp = (zp[x[t]] - zmax) / T - std::log(S);
+    if (std::fabs(u[t] - std::exp(logp)) < kTieBand) flags |= kTieAccept;
+    if (std::log(static_cast<double>(u[t])) < logp) {   // u < p(x) / q(x), q(x) = 1
+      tokens.push_back(x[t]);
+      continue;
+    }
+    w = p;
+    w[x[t]] = 0.0;   // (p - 1{x})+
+    double W = comp_total(w);
+    if (!(W > 0.0)) {   // only through rounding: p(x) = 1 cannot be rejected
+      flags |= kResFallback;
+      w = p;
+      W = comp_total(w);
+    }
+    int edge = 0;
+    tokens.push_back(inverse_cdf(w, W, a.uniforms_resample[b], &edge));
+    write_outputs(a, b, t, tokens, flags | edge);
+    return;
+  }
+  load_row(a.target, a.dtype, trow0 + n, a.V, zp);
+  softmax_T(zp, T, p, zmax, S);
+  int edge = 0;
+  tokens.push_back(inverse_cdf(p, comp_total(p), u[n], &edge));
+  write_outputs(a, b, n, tokens, flags | edge);
+}
+
+// ---------------------------------------------------------------- greedy token tree
+//
+// "Decodificación Especulativa y EAGLE", section "Verificación de Atención en
+// Árvore", and "Accelerating Sonar through speculation", section "EAGLE":
+// the draft proposes a tree of tokens, the target scores every node in one
+// pass, and the longest path the target agrees with is kept.  The greedy
+// reading of "agrees" (section "Caso codicioso"): node i, with parent
+// parents[i] < i and token tokens[i], is accepted iff its parent is accepted
+// and argmax(p at the parent) = tokens[i]; node 0 is the root (the last
+// verified token) and always accepted.  The deepest accepted node (lowest
+// index among equally deep ones) ends the path; the emitted tokens are the
+// path's tokens and then argmax(p at that node).
+
+int tree_request(const void* target, int dtype, const int32_t* parents, const int32_t* tokens,
+                 int n, int N, int V, size_t row0, int32_t* out_tokens, int32_t* path_nodes,
+                 std::vector<double>& z) {
+  for (int i = 0; i < N; ++i) out_tokens[i] = path_nodes[i] = -1;
+  if (n < 1 || n > N || parents[0] != -1) return -1;
+  for (int i = 1; i < n; ++i)
+    if (parents[i] < 0 || parents[i] >= i || tokens[i] < 0 || tokens[i] >= V) return -1;
+  std::vector<int> g(n), depth(n, 0);
+  std::vector<char> acc(n, 0);
+  for (int i = 0; i < n; ++i) {
+    load_row(target, dtype, row0 + i, V, z);
+    g[i] = argmax_lowest(z);
+  }
+  acc[0] = 1;
+  int best = 0;
+  for (int i = 1; i < n; ++i) {
+    const int par = parents[i];
+    acc[i] = acc[par] && tokens[i] == g[par];
+    if (acc[i]) {
+      depth[i] = depth[par] + 1;
+      if (depth[i] > depth[best]) best = i;
+    }
+  }
+  // the path from the root to `best`, root excluded
+  std::vector<int> path;
+  for (int v = best; v != 0; v = parents[v]) path.push_back(v);
+  const int L = static_cast<int>(path.size());
+  path_nodes[0] = 0;
+  for (int k = 0; k < L; ++k) {
+    const int v = path[L - 1 - k];
+    out_tokens[k] = tokens[v];
+    path_nodes[k + 1] = v;
+  }
+  out_tokens[L] = g[best];
+  return L;
+}
+
 template <class F>
 void for_requests(const Args& a, int nthreads, F body) {
   if (nthreads < 1) nthreads = 1;
@@ -435,6 +579,139 @@ int oracle_row_stats(const void* target_logits, const void* draft_logits, int dt
   Args a{target_logits, draft_logits, dtype, draft_tokens, draft_len, temperature, uniforms,
          uniforms_resample, B, K, V, nullptr, nullptr, nullptr, row_info};
   for_requests(a, nthreads, row_stats_request);
+  return 0;
+}
+
+// Draft-side sampler on host buffers: logits [R, V] (dtype 0 = f32, 1 = bf16
+// as raw uint16), temperature [R] (0 = top token), uniforms [R] in [0, 1).
+// tokens [R] get the drawn tokens (-1 for an unusable row), flags [R] (may
+// be null) the near-tie flags of each draw.  Returns 0, or 1 on bad
+// arguments.
+int oracle_sample_draft(const void* logits, int dtype, const float* temperature,
+                        const float* uniforms, int R, int V, int32_t* tokens, int32_t* flags,
+                        int nthreads) {
+  if (R < 1 || V < 1 || !logits || !temperature || !uniforms || !tokens ||
+      (dtype != kF32 && dtype != kBF16))
+    return 1;
+  auto work = [&](int lo, int hi) {
+    std::vector<double> z, p;
+    for (int r = lo; r < hi; ++r) {
+      int32_t flag = 0;
+      const double T = temperature[r];
+      const double u = uniforms[r];
+      if (!(T >= 0.0) || !std::isfinite(T) || !(u >= 0.0 && u < 1.0)) {
+        tokens[r] = -1;
+        flag = kBadInput;
+      } else {
+        sample_row(logits, dtype, static_cast<size_t>(r), V, T, u, z, p, tokens + r, &flag);
+      }
+      if (flags) flags[r] = flag;
+    }
+  };
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > R) nthreads = R;
+  std::vector<std::thread> pool;
+  for (int k = 0; k < nthreads; ++k)
+    pool.emplace_back(work, static_cast<int>(static_cast<long long>(R) * k / nthreads),
+                      static_cast<int>(static_cast<long long>(R) * (k + 1) / nthreads));
+  for (auto& th : pool) th.join();
+  return 0;
+}
+
+// The verification rule for a draft that proposes its top token (q one-hot
+// at the drafted token; no draft logits).  Same arguments and outputs as
+// oracle_verify_sample without draft_logits.
+int oracle_verify_onehot(const void* target_logits, int dtype, const int32_t* draft_tokens,
+                         const int32_t* draft_len, const float* temperature,
+                         const float* uniforms, const float* uniforms_resample, int B, int K,
+                         int V, int32_t* accepted_len, int32_t* out_tokens, int32_t* flags,
+                         int nthreads) {
+  if (!shape_ok(B, K, V) || !target_logits || !draft_tokens || !temperature || !uniforms ||
+      !uniforms_resample || !accepted_len || !out_tokens || (dtype != kF32 && dtype != kBF16))
+    return 1;
+  Args a{target_logits, nullptr, dtype, draft_tokens, draft_len, temperature, uniforms,
+         uniforms_resample, B, K, V, accepted_len, out_tokens, flags, nullptr};
+  for_requests(a, nthreads, [](const Args& aa, int b, std::vector<double>& zp,
+                               std::vector<double>&, std::vector<double>& p,
+                               std::vector<double>&, std::vector<double>& w) {
+    onehot_request(aa, b, zp, p, w);
+  });
+  return 0;
+}
+
+// Greedy verification of a token tree: target_logits [B, N, V] (row i of a
+// request: the target's logits at tree node i), parents [B, N] (parents[0] =
+// -1, parents[i] < i), tokens [B, N] (node i's drafted token; tokens[0]
+// unused), n_nodes [B] in 1..N (nodes >= n_nodes ignored).  accepted_len [B]
+// = the accepted path's length (-1 for an unusable tree); out_tokens [B, N]
+// = the path's tokens, then the target's argmax at its last node, then -1;
+// path_nodes [B, N] = 0, then the path's node indices, then -1.
+int oracle_tree_greedy(const void* target_logits, int dtype, const int32_t* parents,
+                       const int32_t* tokens, const int32_t* n_nodes, int B, int N, int V,
+                       int32_t* accepted_len, int32_t* out_tokens, int32_t* path_nodes,
+                       int nthreads) {
+  if (B < 1 || N < 1 || V < 1 || !target_logits || !parents || !tokens || !n_nodes ||
+      !accepted_len || !out_tokens || !path_nodes || (dtype != kF32 && dtype != kBF16))
+    return 1;
+  auto work = [&](int lo, int hi) {
+    std::vector<double> z;
+    for (int b = lo; b < hi; ++b) {
+      const size_t o = static_cast<size_t>(b) * N;
+      accepted_len[b] = tree_request(target_logits, dtype, parents + o, tokens + o, n_nodes[b],
+                                     N, V, o, out_tokens + o, path_nodes + o, z);
+    }
+  };
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > B) nthreads = B;
+  std::vector<std::thread> pool;
+  for (int k = 0; k < nthreads; ++k)
+    pool.emplace_back(work, static_cast<int>(static_cast<long long>(B) * k / nthreads),
+                      static_cast<int>(static_cast<long long>(B) * (k + 1) / nthreads));
+  for (auto& th : pool) th.join();
+  return 0;
+}
+
+// Post-accept insert ("Accelerating Sonar through speculation", sections
+// "Programación MTP para un solo token" and "Inferencia con decodificación
+// especulativa": a kernel writes the next step's tokens on the device, so
+// the host need not read the accepted lengths).  For request b with
+// j = accepted_len[b]: the j + 1 emitted tokens out_tokens[b, 0..j] are
+// appended to its token history at history[b, seq_lens[b]..] and
+// seq_lens[b] grows by j + 1; next_tokens[b] = out_tokens[b, j] (the next
+// step's input); cu_emitted[b + 1] = cu_emitted[b] + j + 1 and the emitted
+// tokens of all requests are packed, in request order, at packed[cu_emitted[b]..].
+// A request with j outside [0, K] emits nothing (status 1); one whose
+// history would overflow L emits nothing (status 2); both get
+// next_tokens[b] = -1 and keep their history and length.
+int oracle_insert_accepted(const int32_t* accepted_len, const int32_t* out_tokens, int B, int K1,
+                           int32_t* seq_lens, int32_t* history, int L, int32_t* next_tokens,
+                           int32_t* cu_emitted, int32_t* packed, int32_t* status) {
+  if (B < 1 || K1 < 1 || L < 1 || !accepted_len || !out_tokens || !seq_lens || !history ||
+      !next_tokens || !cu_emitted || !packed || !status)
+    return 1;
+  cu_emitted[0] = 0;
+  for (int b = 0; b < B; ++b) {
+    const int j = accepted_len[b];
+    const int32_t* out = out_tokens + static_cast<size_t>(b) * K1;
+    int emitted = 0;
+    if (j < 0 || j >= K1) {
+      status[b] = 1;
+      next_tokens[b] = -1;
+    } else if (seq_lens[b] < 0 || seq_lens[b] + j + 1 > L) {
+      status[b] = 2;
+      next_tokens[b] = -1;
+    } else {
+      status[b] = 0;
+      emitted = j + 1;
+      for (int i = 0; i <= j; ++i) {
+        history[static_cast<size_t>(b) * L + seq_lens[b] + i] = out[i];
+        packed[cu_emitted[b] + i] = out[i];
+      }
+      seq_lens[b] += emitted;
+      next_tokens[b] = out[j];
+    }
+    cu_emitted[b + 1] = cu_emitted[b] + emitted;
+  }
   return 0;
 }
 
