@@ -92,6 +92,8 @@ typedef enum specv_dtype {
 #define SPECV_DEV_BAD_ROW         0x10  /* a row the request needs has no finite max */
 #define SPECV_DEV_NO_DRAFT        0x20  /* T_b > 0 but draft_logits is NULL        */
 #define SPECV_DEV_TIMEOUT         0x40  /* a bounded wait on a copy gave up        */
+#define SPECV_DEV_BAD_TREE        0x80  /* a token tree whose parent of node i is not
+                                           below i, or a node token outside [0,V) */
 
 /* Limits. */
 #define SPECV_MAX_DRAFT 16      /* K <= 16                               */
@@ -214,6 +216,119 @@ specv_status spec_verify_sample_host(const void* target_logits, const void* draf
  * nothing. */
 specv_status specv_launch_plan(int B, int K, int V, specv_dtype dtype, int with_draft,
                                int32_t* out);
+
+/* ------------------------------------------------------------------------
+ * Steps around the verification (same conventions: device buffers, the
+ * caller's workspace zeroed once with specv_workspace_init, asynchronous on
+ * `stream`, data errors in the workspace's status word).
+ * ---------------------------------------------------------------------- */
+
+/* Bytes of workspace spec_sample_draft needs for R rows of V logits (0 for
+ * sizes out of range). */
+size_t specv_sample_workspace_bytes(int R, int V, specv_dtype dtype);
+
+/*
+ * The draft-side sampler ("Decodificación Especulativa y EAGLE", sections
+ * "La Configuración de Dos Modelos" and "Desarrolla": the draft model
+ * proposes each token by sampling softmax(z / T) of its logits):
+ *   logits       [R, V] of `dtype`, one row per request.
+ *   temperature  [R] float32 >= 0; 0 takes the row's argmax (lowest index).
+ *   uniforms     [R] float32 in [0,1): tokens[r] is the smallest i with
+ *                p_0 + ... + p_i > u * sum(p) and p_i > 0 (the same inverse
+ *                CDF as the verification's final draws).
+ *   tokens       [R] int32 output (-1 for a row flagged bad: temperature or
+ *                uniform out of range, no finite maximum).
+ *   workspace    specv_sample_workspace_bytes(R, V, dtype) bytes.
+ *   row_stats    NULL, or [R, 8] float32: slot 0 the row maximum, 1 its
+ *                normaliser sum exp((z - max)/T), 6 the drawn mass
+ *                (sum of p, ~1), 7 the token; at T = 0 slots 0 and 7.
+ * Enqueues the same kernels as spec_verify_sample (a request with no drafts
+ * whose bonus draw is the sample).
+ */
+specv_status spec_sample_draft(const void* logits, specv_dtype dtype, const float* temperature,
+                               const float* uniforms, int R, int V, int32_t* tokens,
+                               void* workspace, size_t workspace_bytes, float* row_stats,
+                               specv_stream_t stream);
+
+/*
+ * Verification for a draft that proposes its top token ("Accelerating Sonar
+ * through speculation", section "Objetivo-Borrador"): the distribution the
+ * drafted token came from is the point mass q = 1{x}, so the rule of "La
+ * Regla de Exactitud" accepts x_t iff u_t < p_t(x_t), and at the first
+ * rejection j draws the replacement from (p_j - 1{x_j})+, i.e. from p_j with
+ * x_j removed; every draft accepted draws the bonus from p_n.  No draft
+ * logits.  Arguments, outputs, readings and errors as spec_verify_sample
+ * without draft_logits (T = 0 is the greedy rule); workspace
+ * specv_workspace_bytes(B, K, V, dtype); row_stats NULL or as
+ * spec_verify_sample_debug (slots 3..5 unused; slot 6 at a rejected row is
+ * 1 - p_j(x_j)).
+ */
+specv_status spec_verify_sample_onehot(const void* target_logits, specv_dtype dtype,
+                                       const int32_t* draft_tokens, const int32_t* draft_len,
+                                       const float* temperature, const float* uniforms,
+                                       const float* uniforms_resample, int B, int K, int V,
+                                       int32_t* accepted_len, int32_t* out_tokens,
+                                       void* workspace, size_t workspace_bytes,
+                                       float* row_stats, specv_stream_t stream);
+
+/* Bytes of workspace spec_verify_tree_greedy needs (0 for sizes out of
+ * range; N <= 64). */
+size_t specv_tree_workspace_bytes(int B, int N, int V, specv_dtype dtype);
+
+/*
+ * Greedy verification of a token tree ("Decodificación Especulativa y EAGLE",
+ * section "Verificación de Atención en Árvore"; "Accelerating Sonar through
+ * speculation", section "EAGLE"): the target scores every node of a drafted
+ * tree in one pass; node i is accepted iff its parent is accepted and the
+ * target's argmax at the parent (lowest index) is node i's token; the root
+ * (node 0, the last verified position) is always accepted.  The deepest
+ * accepted node (lowest index among the deepest) ends the kept path.
+ *   target_logits [B, N, V] of `dtype`: row i = the target's logits at node i.
+ *   parents       [B, N] int32: parents[b,0] = -1, 0 <= parents[b,i] < i.
+ *   tokens        [B, N] int32: node i's drafted token (tokens[b,0] unused).
+ *   n_nodes       [B] int32 in 1..N: nodes >= n_nodes[b] are not read.
+ *   accepted_len  [B] int32 output: the path's length (accepted drafts), or
+ *                 -1 for a malformed tree (status SPECV_DEV_BAD_TREE) or bad
+ *                 node count (SPECV_DEV_BAD_DRAFT_LEN).
+ *   out_tokens    [B, N] int32 output: the path's tokens, then the argmax at
+ *                 its last node, then -1.
+ *   path_nodes    [B, N] int32 output: 0, then the path's node indices, then
+ *                 -1 (the cache rows to keep).
+ *   workspace     specv_tree_workspace_bytes(B, N, V, dtype) bytes.
+ *   row_stats     NULL, or [B, N, 8] float32: slot 0 each node's maximum,
+ *                 slot 7 its argmax.
+ * The sampled (multi-branch) tree rule is not on the pages and not built.
+ */
+specv_status spec_verify_tree_greedy(const void* target_logits, specv_dtype dtype,
+                                     const int32_t* parents, const int32_t* tokens,
+                                     const int32_t* n_nodes, int B, int N, int V,
+                                     int32_t* accepted_len, int32_t* out_tokens,
+                                     int32_t* path_nodes, void* workspace,
+                                     size_t workspace_bytes, float* row_stats,
+                                     specv_stream_t stream);
+
+/*
+ * The post-accept insert ("Accelerating Sonar through speculation", sections
+ * "Programación MTP para un solo token" and "Inferencia con decodificación
+ * especulativa": a kernel writes the next step's tokens on the device, so
+ * the host need not read the accepted lengths between steps).  For request
+ * b with j = accepted_len[b] (as spec_verify_sample writes it):
+ *   history[b, seq_lens[b] .. seq_lens[b] + j] = out_tokens[b, 0 .. j];
+ *   seq_lens[b] += j + 1;  next_tokens[b] = out_tokens[b, j];
+ *   cu_emitted[b + 1] = cu_emitted[b] + j + 1 (cu_emitted[0] = 0) and
+ *   packed[cu_emitted[b] .. cu_emitted[b + 1]) = out_tokens[b, 0 .. j].
+ * A request with j outside [0, K] emits nothing (status[b] = 1), one whose
+ * history would pass L emits nothing (status[b] = 2); both keep their
+ * history and length and get next_tokens[b] = -1.  status[b] = 0 otherwise.
+ *   accepted_len [B], out_tokens [B, K+1], seq_lens [B] (in/out),
+ *   history [B, L] (in/out), next_tokens [B], cu_emitted [B+1],
+ *   packed [B*(K+1)] (only the first cu_emitted[B] written), status [B]:
+ *   int32 device buffers.  One kernel of one CTA; no workspace.
+ */
+specv_status spec_insert_accepted(const int32_t* accepted_len, const int32_t* out_tokens, int B,
+                                  int K, int32_t* seq_lens, int32_t* history, int L,
+                                  int32_t* next_tokens, int32_t* cu_emitted, int32_t* packed,
+                                  int32_t* status, specv_stream_t stream);
 
 /*
  * The sampler without any allocation, for callers that cannot allocate

@@ -11,13 +11,15 @@ status codes into exceptions.  Nothing here computes any step of the rule.
 from __future__ import annotations
 
 from ._native import (DEV_BAD_DRAFT_LEN, DEV_BAD_ROW, DEV_BAD_TEMPERATURE, DEV_BAD_TOKEN,
-                      DEV_BAD_UNIFORM, DEV_NO_DRAFT, DEV_TIMEOUT, SPECV_BF16, SPECV_F32,
-                      SpecVerifyError, check, lib)
+                      DEV_BAD_TREE, DEV_BAD_UNIFORM, DEV_NO_DRAFT, DEV_TIMEOUT, SPECV_BF16,
+                      SPECV_F32, SpecVerifyError, check, lib)
 from .build import build
 
 __all__ = [
     "build", "lib", "Workspace", "HostStaging", "spec_verify_sample", "spec_verify_sample_debug",
-    "spec_verify_sample_host", "spec_verify_sample_noalloc", "launch_plan", "workspace_bytes", "max_vocab", "SpecVerifyError",
+    "spec_verify_sample_host", "spec_verify_sample_noalloc", "sample_draft",
+    "spec_verify_sample_onehot", "verify_tree_greedy", "insert_accepted", "launch_plan",
+    "workspace_bytes", "max_vocab", "SpecVerifyError", "DEV_BAD_TREE",
     "DEV_BAD_DRAFT_LEN", "DEV_BAD_TOKEN", "DEV_BAD_TEMPERATURE", "DEV_BAD_UNIFORM",
     "DEV_BAD_ROW", "DEV_NO_DRAFT", "DEV_TIMEOUT",
 ]
@@ -73,11 +75,17 @@ def max_vocab(dtype) -> int:
 class Workspace:
     """Device workspace for calls over B requests of up to K drafts of a
     V-entry vocabulary, zeroed once on creation (every call leaves it ready
-    for the next)."""
+    for the next).  kind "sample": B rows for sample_draft (K unused);
+    kind "tree": B trees of up to K nodes for verify_tree_greedy."""
 
-    def __init__(self, B: int, K: int, V: int, dtype, device=None, stream=None):
+    def __init__(self, B: int, K: int, V: int, dtype, device=None, stream=None, kind="verify"):
         torch = _torch()
-        n = workspace_bytes(B, K, V, dtype)
+        if kind == "sample":
+            n = int(lib().specv_sample_workspace_bytes(B, V, _code(dtype)))
+        elif kind == "tree":
+            n = int(lib().specv_tree_workspace_bytes(B, K, V, _code(dtype)))
+        else:
+            n = workspace_bytes(B, K, V, dtype)
         if n == 0:
             raise ValueError(f"unsupported workspace shape B={B} K={K} V={V}")
         self.B, self.K, self.V, self.nbytes = B, K, V, n
@@ -265,3 +273,126 @@ def spec_verify_sample_noalloc(target_logits, draft_logits, draft_tokens, draft_
             _ptr(uniforms_resample), B, K, V, _ptr(accepted_len), _ptr(out_tokens),
             _stream_ptr(stream, dev)))
     return accepted_len, out_tokens
+
+
+def _need(name, t, shape, dtype, dev):
+    torch = _torch()
+    if t is None or tuple(t.shape) != tuple(shape) or t.dtype != dtype or t.device != dev \
+            or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor of shape {tuple(shape)} "
+                         f"on {dev}")
+
+
+def sample_draft(logits, temperature, uniforms, *, workspace=None, tokens=None, row_stats=None,
+                 stream=None):
+    """The draft-side sampler: one token per row of ``logits`` [R, V]
+    (bf16/f32) from softmax(z / T) with ``uniforms`` [R]; the row's argmax
+    where T = 0.  Returns tokens [R] int32 (asynchronous)."""
+    torch = _torch()
+    if logits.dim() != 2:
+        raise ValueError("logits must be [R, V]")
+    R, V = logits.shape
+    dev = logits.device
+    _need("logits", logits, (R, V), logits.dtype, dev)
+    _need("temperature", temperature, (R,), torch.float32, dev)
+    _need("uniforms", uniforms, (R,), torch.float32, dev)
+    if tokens is None:
+        tokens = torch.empty(R, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = Workspace(R, 0, V, logits.dtype, dev, stream, kind="sample")
+    with torch.cuda.device(dev):
+        check("spec_sample_draft", lib().spec_sample_draft(
+            _ptr(logits), _dtype_code(logits), _ptr(temperature), _ptr(uniforms), R, V,
+            _ptr(tokens), workspace.tensor.data_ptr(), workspace.nbytes, _ptr(row_stats),
+            _stream_ptr(stream, dev)))
+    return tokens
+
+
+def spec_verify_sample_onehot(target_logits, draft_tokens, draft_len, temperature, uniforms,
+                              uniforms_resample, *, workspace=None, accepted_len=None,
+                              out_tokens=None, row_stats=None, stream=None):
+    """Verification for a draft that proposes its top token (no draft
+    logits: q is the point mass at each drafted token).  Tensors as for
+    spec_verify_sample without draft_logits.  Returns (accepted_len [B],
+    out_tokens [B, K+1]) int32 (asynchronous)."""
+    torch = _torch()
+    B, K, V = _check_inputs(target_logits, None, draft_tokens, draft_len, temperature, uniforms,
+                            uniforms_resample)
+    dev = target_logits.device
+    if accepted_len is None:
+        accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = Workspace(B, K, V, target_logits.dtype, dev, stream)
+    with torch.cuda.device(dev):
+        check("spec_verify_sample_onehot", lib().spec_verify_sample_onehot(
+            _ptr(target_logits), _dtype_code(target_logits), _ptr(draft_tokens), _ptr(draft_len),
+            _ptr(temperature), _ptr(uniforms), _ptr(uniforms_resample), B, K, V,
+            _ptr(accepted_len), _ptr(out_tokens), workspace.tensor.data_ptr(), workspace.nbytes,
+            _ptr(row_stats), _stream_ptr(stream, dev)))
+    return accepted_len, out_tokens
+
+
+def verify_tree_greedy(target_logits, parents, tokens, n_nodes, *, workspace=None,
+                       accepted_len=None, out_tokens=None, path_nodes=None, row_stats=None,
+                       stream=None):
+    """Greedy verification of token trees: ``target_logits`` [B, N, V] (row i
+    = the target's logits at node i), ``parents`` [B, N] int32 (-1 at the
+    root, else < i), ``tokens`` [B, N] int32, ``n_nodes`` [B] int32.  Returns
+    (accepted_len [B], out_tokens [B, N], path_nodes [B, N]) int32."""
+    torch = _torch()
+    if target_logits.dim() != 3:
+        raise ValueError("target_logits must be [B, N, V]")
+    B, N, V = target_logits.shape
+    dev = target_logits.device
+    _need("target_logits", target_logits, (B, N, V), target_logits.dtype, dev)
+    _dtype_code(target_logits)
+    _need("parents", parents, (B, N), torch.int32, dev)
+    _need("tokens", tokens, (B, N), torch.int32, dev)
+    _need("n_nodes", n_nodes, (B,), torch.int32, dev)
+    if accepted_len is None:
+        accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, N), dtype=torch.int32, device=dev)
+    if path_nodes is None:
+        path_nodes = torch.empty((B, N), dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = Workspace(B, N, V, target_logits.dtype, dev, stream, kind="tree")
+    with torch.cuda.device(dev):
+        check("spec_verify_tree_greedy", lib().spec_verify_tree_greedy(
+            _ptr(target_logits), _dtype_code(target_logits), _ptr(parents), _ptr(tokens),
+            _ptr(n_nodes), B, N, V, _ptr(accepted_len), _ptr(out_tokens), _ptr(path_nodes),
+            workspace.tensor.data_ptr(), workspace.nbytes, _ptr(row_stats),
+            _stream_ptr(stream, dev)))
+    return accepted_len, out_tokens, path_nodes
+
+
+def insert_accepted(accepted_len, out_tokens, seq_lens, history, *, next_tokens=None,
+                    cu_emitted=None, packed=None, status=None, stream=None):
+    """The post-accept insert on the device: appends each request's emitted
+    tokens (out_tokens[b, :accepted_len[b] + 1]) to ``history`` [B, L] at
+    ``seq_lens`` [B] (both updated in place) and returns (next_tokens [B],
+    cu_emitted [B+1], packed [B*(K+1)], status [B]) int32 (asynchronous)."""
+    torch = _torch()
+    B, K1 = out_tokens.shape
+    L = history.shape[1]
+    dev = out_tokens.device
+    _need("accepted_len", accepted_len, (B,), torch.int32, dev)
+    _need("out_tokens", out_tokens, (B, K1), torch.int32, dev)
+    _need("seq_lens", seq_lens, (B,), torch.int32, dev)
+    _need("history", history, (B, L), torch.int32, dev)
+    if next_tokens is None:
+        next_tokens = torch.empty(B, dtype=torch.int32, device=dev)
+    if cu_emitted is None:
+        cu_emitted = torch.empty(B + 1, dtype=torch.int32, device=dev)
+    if packed is None:
+        packed = torch.full((B * K1,), -1, dtype=torch.int32, device=dev)
+    if status is None:
+        status = torch.empty(B, dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        check("spec_insert_accepted", lib().spec_insert_accepted(
+            _ptr(accepted_len), _ptr(out_tokens), B, K1 - 1, _ptr(seq_lens), _ptr(history), L,
+            _ptr(next_tokens), _ptr(cu_emitted), _ptr(packed), _ptr(status),
+            _stream_ptr(stream, dev)))
+    return next_tokens, cu_emitted, packed, status

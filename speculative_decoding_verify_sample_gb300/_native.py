@@ -25,6 +25,7 @@ DEV_BAD_UNIFORM = 0x08
 DEV_BAD_ROW = 0x10
 DEV_NO_DRAFT = 0x20
 DEV_TIMEOUT = 0x40
+DEV_BAD_TREE = 0x80
 
 # exported function -> (restype, argtypes)
 _vp = ctypes.c_void_p
@@ -46,6 +47,14 @@ SIGNATURES = {
     "specv_launch_plan": (_i, [_i, _i, _i, _i, _i, _vp]),
     "spec_verify_sample_noalloc": (_i, [_vp, _vp, _i, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _vp, _vp,
                                         _vp]),
+    "specv_sample_workspace_bytes": (_sz, [_i, _i, _i]),
+    "spec_sample_draft": (_i, [_vp, _i, _vp, _vp, _i, _i, _vp, _vp, _sz, _vp, _vp]),
+    "spec_verify_sample_onehot": (_i, [_vp, _i, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _vp, _vp,
+                                       _vp, _sz, _vp, _vp]),
+    "specv_tree_workspace_bytes": (_sz, [_i, _i, _i, _i]),
+    "spec_verify_tree_greedy": (_i, [_vp, _i, _vp, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _sz,
+                                     _vp, _vp]),
+    "spec_insert_accepted": (_i, [_vp, _vp, _i, _i, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp]),
 }
 
 NOALLOC_SCRATCH_BYTES = 4 << 20

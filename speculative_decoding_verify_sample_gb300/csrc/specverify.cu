@@ -87,6 +87,13 @@ static_assert((kHBonus + 1) * 4 <= kHeaderBytes, "header words fit the header");
 
 constexpr int kItemA = 1, kItemR = 3;
 
+// What a launch sequence computes (Params::mode).
+constexpr int kModeVerify = 0;   // the verification rule, draft logits given
+constexpr int kModeSample = 1;   // the draft-side sampler: one row per request, no drafts
+constexpr int kModeOnehot = 2;   // the rule for a draft that proposes its top token (q one-hot)
+constexpr int kModeTree = 3;     // greedy verification of a token tree (rows = tree nodes)
+constexpr int kMaxTreeNodes = 64;
+
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -111,6 +118,9 @@ struct Params {
   const float* uniforms;
   const float* uniforms_resample;
   int B, K, V;
+  int mode;         // kModeVerify / kModeSample / kModeOnehot / kModeTree
+  const int32_t* parents;   // tree mode: [B][K+1] parent of each node (-1 at the root)
+  int32_t* path_nodes;      // tree mode: [B][K+1] the accepted path's nodes
   int R;            // record rows per request: K+1 target, then K draft
   int NC;           // stats chunks per row
   int NCd;          // residual pieces per row
@@ -131,7 +141,7 @@ struct Params {
 // request needs (prefix sums) and its length.
 struct Plan {
   int rb[kPlanMax + 1];       // rows before request b
-  uint8_t info[kPlanMax];     // draft length | 0x80 if the request samples (0: unusable)
+  uint8_t info[kPlanMax];     // draft length | 0x40 | 0x80 if the request samples (0: unusable)
   int total;                  // tickets: chunks of every needed row
 };
 
@@ -536,26 +546,43 @@ __device__ __forceinline__ void masked_vec(const unsigned char* slot, const Vecs
 
 // ---------------------------------------------------------------- requests
 
-__device__ __forceinline__ int request_bad(const Params& P, int n, float T) {
-  if (n < 1 || n > P.K) return SPECV_DEV_BAD_DRAFT_LEN;
-  if (!(T >= 0.0f) || isinf(T)) return SPECV_DEV_BAD_TEMPERATURE;
-  if (T > 0.0f && P.draft == nullptr) return SPECV_DEV_NO_DRAFT;
-  return 0;
-}
-
+// A request's draft length n: its drafted tokens, or (sampler) 0, or (tree)
+// its node count less the root.
 __device__ __forceinline__ int request_len(const Params& P, int b) {
+  if (P.mode == kModeTree) return __ldg(P.draft_len + b) - 1;
   return P.draft_len ? __ldg(P.draft_len + b) : P.K;
 }
 
-// Rows a usable request needs: target rows t <= n, and draft rows t < n
-// when it samples.
-__device__ __forceinline__ int request_rows(int n, float T) { return T > 0.0f ? 2 * n + 1 : n + 1; }
+__device__ __forceinline__ float request_T(const Params& P, int b) {
+  return P.temperature ? __ldg(P.temperature + b) : 0.0f;
+}
 
-// Record row of a request's row slot: a sampled request's first 2n slots
-// alternate target row t and draft row t, slot 2n is target row n; a greedy
-// request's slots are its target rows.
-__device__ __forceinline__ int slot_row(int slot, bool sampled, int n, int K) {
-  if (!sampled || slot == 2 * n) return sampled ? n : slot;
+__device__ __forceinline__ int request_bad(const Params& P, int n, float T) {
+  const int lo = (P.mode == kModeSample || P.mode == kModeTree) ? 0 : 1;
+  if (n < lo || n > P.K) return SPECV_DEV_BAD_DRAFT_LEN;
+  if (!(T >= 0.0f) || isinf(T)) return SPECV_DEV_BAD_TEMPERATURE;
+  if (T > 0.0f && P.draft == nullptr && P.mode == kModeVerify) return SPECV_DEV_NO_DRAFT;
+  return 0;
+}
+
+// Whether a request's rows include draft rows: a sampled request of the
+// verification rule (a one-hot draft has no logits; the sampler and trees
+// have no drafts).
+__device__ __forceinline__ bool two_rows(const Params& P, bool sampled) {
+  return sampled && P.mode == kModeVerify;
+}
+
+// Rows a usable request needs: target rows t <= n, and draft rows t < n
+// when it samples with draft logits.
+__device__ __forceinline__ int request_rows(const Params& P, int n, float T) {
+  return two_rows(P, T > 0.0f) ? 2 * n + 1 : n + 1;
+}
+
+// Record row of a request's row slot: a request with draft rows alternates
+// target row t and draft row t in its first 2n slots, slot 2n is target row
+// n; otherwise its slots are its target rows.
+__device__ __forceinline__ int slot_row(int slot, bool both, int n, int K) {
+  if (!both || slot == 2 * n) return both ? n : slot;
   return (slot & 1) ? K + 1 + (slot >> 1) : (slot >> 1);
 }
 
@@ -566,7 +593,7 @@ __device__ __forceinline__ void write_outputs(const Params& P, int b, int j, int
   for (int s = lane; s <= P.K; s += 32)
     P.out_tokens[static_cast<size_t>(b) * (P.K + 1) + s] =
         j < 0 ? -1 : (s < j ? x_lane : (s == j ? tok : -1));
-  if (lane == 0) P.accepted_len[b] = j;
+  if (lane == 0 && P.accepted_len) P.accepted_len[b] = j;
 }
 
 // ---------------------------------------------------------------- plan
@@ -582,8 +609,8 @@ __device__ void build_plan(const Params& P, Plan& pl, int* red) {
   int rows = 0;
   for (int b = b0; b < b1; ++b) {
     const int n = request_len(P, b);
-    const float T = __ldg(P.temperature + b);
-    if (!request_bad(P, n, T)) rows += request_rows(n, T);
+    const float T = request_T(P, b);
+    if (!request_bad(P, n, T)) rows += request_rows(P, n, T);
   }
   const int ir = warp_incl_scan_int(rows, lane);
   if (lane == 31) red[w] = ir;
@@ -596,11 +623,11 @@ __device__ void build_plan(const Params& P, Plan& pl, int* red) {
   }
   for (int b = b0; b < b1; ++b) {
     const int n = request_len(P, b);
-    const float T = __ldg(P.temperature + b);
+    const float T = request_T(P, b);
     const bool bad = request_bad(P, n, T) != 0;
     pl.rb[b] = r;
-    pl.info[b] = static_cast<uint8_t>(bad ? 0 : (n | (T > 0.0f ? 0x80 : 0)));
-    if (!bad) r += request_rows(n, T);
+    pl.info[b] = static_cast<uint8_t>(bad ? 0 : (n | 0x40 | (T > 0.0f ? 0x80 : 0)));
+    if (!bad) r += request_rows(P, n, T);
   }
   if (tid == 0) {
     pl.rb[B] = tr;
@@ -659,10 +686,13 @@ __device__ uint4 decode_ticket(const Params& P, const Plan& pl, int t) {
   const int info = pl.info[b];
   const bool sampled = (info & 0x80) != 0;
   const int n = info & 0x3F;
-  const float sT = sampled ? temp_scale(__ldg(P.temperature + b)) : 0.0f;
-  const int row = slot_row(slot, sampled, n, P.K);
-  int x = -1;
-  if (sampled && slot < 2 * n) x = __ldg(P.draft_tokens + static_cast<size_t>(b) * P.K + (slot >> 1));
+  const float sT = sampled ? temp_scale(request_T(P, b)) : 0.0f;
+  const bool both = two_rows(P, sampled);
+  const int row = slot_row(slot, both, n, P.K);
+  int x = -1;   // the drafted token whose logit this row's chunks record
+  if (both && slot < 2 * n) x = __ldg(P.draft_tokens + static_cast<size_t>(b) * P.K + (slot >> 1));
+  else if (sampled && P.mode == kModeOnehot && slot < n)
+    x = __ldg(P.draft_tokens + static_cast<size_t>(b) * P.K + slot);
   return pack_item(kItemA, b, row, c, x, sT, n);
 }
 // ---------------------------------------------------------------- chunk reductions
@@ -1233,7 +1263,8 @@ __device__ __forceinline__ void p_masses(const uint2* rec, int NC, float Mp, flo
 
 // ---------------------------------------------------------------- decisions
 
-constexpr int kMaxRows = 2 * SPECV_MAX_DRAFT + 1;
+constexpr int kMaxRows = 2 * SPECV_MAX_DRAFT + 1 > kMaxTreeNodes ? 2 * SPECV_MAX_DRAFT + 1
+                                                                  : kMaxTreeNodes;
 constexpr int kDecideRecs = 2048;   // records a decide CTA stages at once (in batches of 1024)
 constexpr int kDecideBuf = kDecideRecs > kDecideWarps * kMaxChunks ? kDecideRecs
                                                                     : kDecideWarps * kMaxChunks;
@@ -1263,6 +1294,7 @@ struct DecideSmem {
   float u[SPECV_MAX_DRAFT + 1];     // its uniforms
   float zp[SPECV_MAX_DRAFT], zq[SPECV_MAX_DRAFT];   // the drafted tokens' logits
   float ur;                         // its resample uniform
+  int par[kMaxTreeNodes], tok[kMaxTreeNodes], depth[kMaxTreeNodes];   // tree mode
   alignas(16) uint2 rec[kDecideBuf];   // the request's row records (else each warp's row), staged
 };
 
@@ -1388,17 +1420,128 @@ __device__ __forceinline__ DecideIn decide_inputs(const Params& P, int b) {
   const int tid = threadIdx.x, K = P.K;
   DecideIn in;
   in.n = request_len(P, b);
-  in.T = __ldg(P.temperature + b);
+  in.T = request_T(P, b);
   in.bad = request_bad(P, in.n, in.T);
   in.x = -1;
   in.u = 0.0f;
   in.ur = 0.0f;
-  if (!in.bad && tid < 32) {
+  if (!in.bad && tid < 32 && P.mode != kModeTree) {
     if (tid < in.n) in.x = __ldg(P.draft_tokens + static_cast<size_t>(b) * K + tid);
     if (tid <= in.n) in.u = __ldg(P.uniforms + static_cast<size_t>(b) * (K + 1) + tid);
-    if (tid == 0) in.ur = __ldg(P.uniforms_resample + b);
+    if (tid == 0 && P.uniforms_resample) in.ur = __ldg(P.uniforms_resample + b);
   }
   return in;
+}
+
+// Warp 0: a one-hot draft rejected at j.  The replacement comes from
+// (p_j - 1{x_j})+, which is p_j with x_j removed: row j's chunk masses of p
+// (from its records, staged or in global memory), less x_j's own weight in
+// its chunk, pick the chunk; the request joins the bonus list with that
+// chunk and x_j excluded from the walk.  If nothing but x_j weighs (p_j(x_j)
+// = 1 in fp32, only through rounding), the draw is from p_j itself.
+template <int DT>
+__device__ void onehot_rejection(const Params& P, DecideSmem& D, int b, int j, float Mp, float Sp,
+                                 float sT, float ur, bool staged, int x_lane, int lane) {
+  const int NC = P.NC;
+  const uint2* rec = staged ? D.rec + j * NC
+                            : P.part + (static_cast<size_t>(b) * P.R + j) * NC;
+  const int x = __shfl_sync(0xffffffffu, x_lane, j);
+  const float ex = scaled_exp(D.zp[j], Mp, sT);   // x_j's weight, on the scale of the masses
+  const uintptr_t ra = target_row<DT>(P, b, j);
+  const int cx = static_cast<int>(((ra & 15) + static_cast<uintptr_t>(x) * Elt<DT>::kBytes) /
+                                  kChunkBytes);   // the chunk holding x_j
+  __syncwarp();
+  for (int c = lane; c < NC; c += 32) {
+    const uint2 r = staged ? rec[c] : __ldcg(rec + c);
+    const float m = __uint_as_float(r.x);
+    float w = m > -INFINITY ? __fmul_rn(__uint_as_float(r.y), scaled_exp(m, Mp, sT)) : 0.0f;
+    if (c == cx) w = fmaxf(__fsub_rn(w, ex), 0.0f);
+    D.mass[c] = w;
+  }
+  __syncwarp();
+  float W, rem;
+  int chunk = pick_chunk(D.mass, NC, ur, lane, W, rem);
+  int excl = x;
+  if (!(W > 0.0f)) {   // only x_j weighs: draw from p_j with the same uniform
+    __syncwarp();
+    if (lane == (cx & 31)) D.mass[cx] = fmaxf(__fadd_rn(D.mass[cx], ex), ex);
+    __syncwarp();
+    chunk = pick_chunk(D.mass, NC, ur, lane, W, rem);
+    excl = -1;
+  }
+  float* rs = P.row_stats ? P.row_stats + static_cast<size_t>(b) * (P.K + 1) * 8 : nullptr;
+  if (rs && lane == 0) {
+    rs[j * 8 + 6] = excl >= 0 ? __fdiv_rn(W, Sp) : 0.0f;
+    if (chunk < 0) rs[j * 8 + 7] = -1.0f;
+  }
+  if (chunk < 0) {
+    if (lane == 0) atomicOr(P.header + kHStatus, SPECV_DEV_BAD_ROW);
+    write_outputs(P, b, -1, -1, x_lane, lane);
+    return;
+  }
+  if (lane == 0)
+    store_req(P.req + (P.B - 1 - atomicAdd(P.header + kHBonus, 1)), b, j, rem, chunk,
+              make_float4(Mp, __int_as_float(excl), sT, 0.0f));
+  write_outputs(P, b, j, -1, x_lane, lane);   // the bonus walk writes the token
+}
+
+// Warp 0, tree mode: greedy verification of request b's token tree.  D.arg
+// holds the argmax of every node's row (nodes 0..n).  Node i >= 1 is
+// accepted iff its parent is and the parent's argmax is its token; the
+// deepest accepted node (lowest index among the deepest) ends the path.
+// Writes accepted_len = the path's length, out_tokens = the path's tokens
+// then the argmax at its last node, path_nodes = 0 then the path's nodes.
+// A malformed tree (a parent not below its node, a token outside [0, V))
+// gets -1 throughout and a status bit.
+__device__ void tree_decide(const Params& P, DecideSmem& D, int b, int n, int lane) {
+  const int N = P.K + 1, V = P.V;
+  const size_t o = static_cast<size_t>(b) * N;
+  int bad = 0;
+  for (int i = lane; i <= n; i += 32) {
+    const int par = __ldg(P.parents + o + i);
+    const int tok = __ldg(P.draft_tokens + o + i);
+    D.par[i] = par;
+    D.tok[i] = tok;
+    if (i == 0 ? par != -1 : (par < 0 || par >= i || tok < 0 || tok >= V)) bad = 1;
+    if (D.arg[i] < 0 || D.arg[i] >= V) bad = 1;
+  }
+  bad = __any_sync(0xffffffffu, bad);
+  __syncwarp();
+  int len = -1;
+  if (!bad && lane == 0) {
+    // nodes in index order: a parent is decided before its children
+    int best = 0;
+    D.depth[0] = 0;
+    for (int i = 1; i <= n; ++i) {
+      const int par = D.par[i];
+      const bool acc = D.depth[par] >= 0 && D.tok[i] == D.arg[par];
+      D.depth[i] = acc ? D.depth[par] + 1 : -1;
+      if (acc && D.depth[i] > D.depth[best]) best = i;
+    }
+    len = D.depth[best];
+    for (int v = best, k = len; v != 0; v = D.par[v], --k) {
+      P.out_tokens[o + k - 1] = D.tok[v];
+      P.path_nodes[o + k] = v;
+    }
+    P.out_tokens[o + len] = D.arg[best];
+    P.path_nodes[o] = 0;
+    P.accepted_len[b] = len;
+    if (P.row_stats)
+      for (int i = 0; i <= n; ++i) {
+        P.row_stats[(o + i) * 8 + 0] = D.M[i];
+        P.row_stats[(o + i) * 8 + 7] = static_cast<float>(D.arg[i]);
+      }
+  }
+  len = __shfl_sync(0xffffffffu, bad ? -1 : len, 0);
+  // the padding after the path (everything, for a malformed tree)
+  for (int s = lane; s < N; s += 32) {
+    if (s > len) P.out_tokens[o + s] = -1;
+    if (s > len) P.path_nodes[o + s] = -1;
+  }
+  if (bad && lane == 0) {
+    P.accepted_len[b] = -1;
+    atomicOr(P.header + kHStatus, SPECV_DEV_BAD_TREE);
+  }
 }
 
 template <int DT>
@@ -1417,7 +1560,8 @@ __device__ void decide_request(const Params& P, DecideSmem& D, int b, const Deci
   }
   const bool greedy = !(T > 0.0f);
   const float sT = greedy ? 0.0f : temp_scale(T);
-  const int nt = n + 1, nd = greedy ? 0 : n;
+  const bool both = two_rows(P, !greedy);
+  const int nt = n + 1, nd = both ? n : 0;
   // The request's records and warp 0's inputs (drafted tokens, uniforms,
   // the drafted tokens' logits) in one batch of loads, every load issued
   // before any is stored; records that do not fit are staged a row at a
@@ -1428,7 +1572,7 @@ __device__ void decide_request(const Params& P, DecideSmem& D, int b, const Deci
     float zpf = 0.0f, zqf = 0.0f;
     if (!greedy && tid < n) {
       zpf = __ldcg(P.zx + static_cast<size_t>(b) * R + tid);
-      zqf = __ldcg(P.zx + static_cast<size_t>(b) * R + K + 1 + tid);
+      if (both) zqf = __ldcg(P.zx + static_cast<size_t>(b) * R + K + 1 + tid);
     }
     constexpr int kPer = 8;
     constexpr int kBatch = kPer * kDecideWarps * 32;
@@ -1452,7 +1596,7 @@ __device__ void decide_request(const Params& P, DecideSmem& D, int b, const Deci
         }
       }
     }
-    if (tid < 32) {
+    if (tid < 32 && P.mode != kModeTree) {
       if (tid < SPECV_MAX_DRAFT) {
         D.x[tid] = in.x;
         D.zp[tid] = zpf;
@@ -1510,6 +1654,10 @@ __device__ void decide_request(const Params& P, DecideSmem& D, int b, const Deci
   }
   __syncthreads();
   if (warp != 0) return;
+  if (P.mode == kModeTree) {
+    tree_decide(P, D, b, n, lane);
+    return;
+  }
   const int x_lane = lane < n ? D.x[lane] : -1;
   const float u_lane = lane <= n ? D.u[lane] : 0.0f;
   const float ur = D.ur;
@@ -1554,8 +1702,9 @@ __device__ void decide_request(const Params& P, DecideSmem& D, int b, const Deci
   }
 
   // every row a sampled request needs must have a finite maximum
-  if (!bad && __any_sync(0xffffffffu, (lane < n && !(isfinite(Mp_l) && isfinite(Mq_l))) ||
-                                          (lane == n && !isfinite(Mp_l))))
+  if (!bad && __any_sync(0xffffffffu,
+                         (lane < n && !(isfinite(Mp_l) && (!both || isfinite(Mq_l)))) ||
+                             (lane == n && !isfinite(Mp_l))))
     bad = SPECV_DEV_BAD_ROW;
   if (bad) {
     if (lane == 0) atomicOr(P.header + kHStatus, bad);
@@ -1566,7 +1715,8 @@ __device__ void decide_request(const Params& P, DecideSmem& D, int b, const Deci
   bool accept = false;
   if (lane < n) {
     lp = __fsub_rn(__fmul_rn(__fsub_rn(zp, Mp_l), sT), __log2f(Sp_l));
-    lq = __fsub_rn(__fmul_rn(__fsub_rn(zq, Mq_l), sT), __log2f(Sq_l));
+    // a one-hot draft's q(x) = 1: accept iff u < p(x)
+    lq = both ? __fsub_rn(__fmul_rn(__fsub_rn(zq, Mq_l), sT), __log2f(Sq_l)) : 0.0f;
     accept = __fadd_rn(__log2f(u_lane), lq) < lp;
   }
   const unsigned rej = __ballot_sync(0xffffffffu, lane < n && !accept);
@@ -1578,13 +1728,19 @@ __device__ void decide_request(const Params& P, DecideSmem& D, int b, const Deci
     }
     if (lane < n) {
       rs[lane * 8 + 2] = lp * kLn2;
-      rs[lane * 8 + 3] = Mq_l;
-      rs[lane * 8 + 4] = Sq_l;
-      rs[lane * 8 + 5] = lq * kLn2;
+      if (both) {
+        rs[lane * 8 + 3] = Mq_l;
+        rs[lane * 8 + 4] = Sq_l;
+        rs[lane * 8 + 5] = lq * kLn2;
+      }
     }
   }
   const float Mp = __shfl_sync(0xffffffffu, Mp_l, j);
   const float Sp = __shfl_sync(0xffffffffu, Sp_l, j);
+  if (j < n && !both) {
+    onehot_rejection<DT>(P, D, b, j, Mp, Sp, sT, ur, all_at_once, x_lane, lane);
+    return;
+  }
   if (j < n) {
     const float Mq = __shfl_sync(0xffffffffu, Mq_l, j);
     const float Sq = __shfl_sync(0xffffffffu, Sq_l, j);
@@ -1612,7 +1768,7 @@ __device__ void decide_request(const Params& P, DecideSmem& D, int b, const Deci
   }
   if (lane == 0) {
     store_req(P.req + (P.B - 1 - atomicAdd(P.header + kHBonus, 1)), b, n, rem, chunk,
-              make_float4(Mp, 0.0f, sT, 0.0f));   // the bonus list grows down
+              make_float4(Mp, __int_as_float(-1), sT, 0.0f));   // the bonus list grows down
   }
   write_outputs(P, b, n, -1, x_lane, lane);
 }
@@ -1630,6 +1786,7 @@ __device__ void bonus_draw(const Params& P, uint4* stage, const Req& r, int lane
   const int b = r.b, n = r.j, chunk = r.chunk;
   const float rem = r.aux;
   const float4 prm = r.prm;
+  const int excl = __float_as_int(prm.y);   // a token the draw leaves out (-1: none)
   const Chunk kp = chunk_of<DT>(target_row<DT>(P, b, n), V, chunk, kChunkBytes);
   // every 16-byte vector of the chunk copied at once into the staging area
   // with cp.async; the few partly outside the chunk (row edges) are read
@@ -1656,9 +1813,10 @@ __device__ void bonus_draw(const Params& P, uint4* stage, const Req& r, int lane
     if ((whole >> s) & 1u) Elt<DT>::unpack(stage[s * 32 + lane], v);
     else global_vec<DT>(kp, P.t_lo, P.t_hi, s * 32 + lane, v);
     float a = 0.0f;
+    const int e0 = -kp.off0 / Elt<DT>::kBytes + (s * 32 + lane) * CH;
 #pragma unroll
     for (int q = 0; q < CH; ++q) {
-      w[q] = weight(v[q], 0.0f, false, prm);
+      w[q] = e0 + q == excl ? 0.0f : weight(v[q], 0.0f, false, prm);
       a = __fadd_rn(a, w[q]);
     }
     const float ssum = warp_sum(a);
@@ -1679,7 +1837,10 @@ __device__ void bonus_draw(const Params& P, uint4* stage, const Req& r, int lane
     if ((whole >> last) & 1u) Elt<DT>::unpack(stage[last * 32 + lane], v);
     else global_vec<DT>(kp, P.t_lo, P.t_hi, last * 32 + lane, v);
 #pragma unroll
-    for (int q = 0; q < CH; ++q) w[q] = weight(v[q], 0.0f, false, prm);
+    for (int q = 0; q < CH; ++q) {
+      const int e = -kp.off0 / Elt<DT>::kBytes + (last * 32 + lane) * CH + q;
+      w[q] = e == excl ? 0.0f : weight(v[q], 0.0f, false, prm);
+    }
   }
   const int tok = found >= 0 ? pick_in_sweep<CH>(w, rem2, -kp.off0 / Elt<DT>::kBytes + (found * 32 + lane) * CH, lane)
                              : -1;
@@ -2071,6 +2232,68 @@ __global__ void __launch_bounds__(kDecideWarps * 32) search_kernel(const Params 
   }
 }
 
+// ---------------------------------------------------------------- post-accept insert
+
+constexpr int kInsertThreads = 1024;
+
+// One CTA: request b = tile base + thread.  Each emits j + 1 tokens when
+// j = accepted_len[b] is in [0, K] and its history has room (else nothing,
+// with status 1 or 2); cu_emitted is the exclusive prefix of the emitted
+// counts over requests (a block-wide scan per tile of 1024, carried from
+// tile to tile), and the emitted tokens are written both behind the
+// request's history and packed at cu_emitted[b].
+__global__ void __launch_bounds__(kInsertThreads) insert_kernel(
+    const int32_t* __restrict__ accepted_len, const int32_t* __restrict__ out_tokens, int B, int K1,
+    int32_t* seq_lens, int32_t* history, int L, int32_t* next_tokens, int32_t* cu_emitted,
+    int32_t* packed, int32_t* status) {
+  __shared__ int wsum[kInsertThreads / 32];
+  __shared__ int tile_total;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int carry = 0;
+  for (int base = 0; base < B; base += kInsertThreads) {
+    const int b = base + tid;
+    int j = -1, s0 = 0, em = 0, st = 0;
+    if (b < B) {
+      j = accepted_len[b];
+      s0 = seq_lens[b];
+      if (j < 0 || j >= K1) st = 1;
+      else if (s0 < 0 || s0 > L - (j + 1)) st = 2;
+      else em = j + 1;
+    }
+    const int incl = warp_incl_scan_int(em, lane);
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      const int v = wsum[lane];
+      const int wi = warp_incl_scan_int(v, lane);
+      wsum[lane] = wi - v;
+      if (lane == 31) tile_total = wi;
+    }
+    __syncthreads();
+    const int excl = carry + wsum[warp] + incl - em;
+    if (b < B) {
+      const int32_t* out = out_tokens + static_cast<size_t>(b) * K1;
+      cu_emitted[b] = excl;
+      status[b] = st;
+      if (em) {
+        int32_t* h = history + static_cast<size_t>(b) * L + s0;
+        for (int i = 0; i < em; ++i) {
+          const int32_t t = out[i];
+          h[i] = t;
+          packed[excl + i] = t;
+        }
+        seq_lens[b] = s0 + em;
+        next_tokens[b] = out[j];
+      } else {
+        next_tokens[b] = -1;
+      }
+      if (b == B - 1) cu_emitted[B] = excl + em;
+    }
+    carry += tile_total;
+    __syncthreads();   // wsum and tile_total are rewritten by the next tile
+  }
+}
+
 // ---------------------------------------------------------------- host side
 
 
@@ -2172,11 +2395,11 @@ cudaError_t launch_dependent(Kern kernel, int grid, int block, int smem, cudaStr
 }
 
 template <int DT>
-cudaError_t launch_sequence(const Params& P, int grid, cudaStream_t stream) {
+cudaError_t launch_sequence(const Params& P, int grid, bool decide_only, cudaStream_t stream) {
   cudaError_t e = launch_dependent(stats_kernel<DT>, grid, kThreads, kRingBytes, stream, P);
   if (e != cudaSuccess) return e;
   e = launch_dependent(decide_kernel<DT>, P.B, kDecideWarps * 32, 0, stream, P);
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess || decide_only) return e;   // greedy trees list no draws
   e = launch_dependent(residual_kernel<DT>, grid, kThreads, kRingBytes, stream, P);
   if (e != cudaSuccess) return e;
   return launch_dependent(search_kernel<DT>, (P.B + kDecideWarps - 1) / kDecideWarps,
@@ -2188,26 +2411,65 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 uintptr_t up16(uintptr_t x) { return (x + 15) & ~static_cast<uintptr_t>(15); }
 uintptr_t down16(uintptr_t x) { return x & ~static_cast<uintptr_t>(15); }
 
-specv_status launch(const void* target, const void* draft, specv_dtype dtype,
-                    const int32_t* draft_tokens, const int32_t* draft_len,
-                    const float* temperature, const float* uniforms,
-                    const float* uniforms_resample, int B, int K, int V, int32_t* accepted_len,
-                    int32_t* out_tokens, void* workspace, size_t workspace_bytes,
-                    float* row_stats, cudaStream_t stream) {
-  if (!target || !draft_tokens || !temperature || !uniforms || !uniforms_resample ||
-      !accepted_len || !out_tokens || !workspace)
+// Everything one call of the library's sampling entry points passes down:
+// the verification rule and its variants share the launch sequence.
+struct Call {
+  int mode = kModeVerify;
+  const void* target = nullptr;
+  const void* draft = nullptr;
+  specv_dtype dtype = SPECV_F32;
+  const int32_t* draft_tokens = nullptr;   // tree mode: node tokens [B][K+1]
+  const int32_t* draft_len = nullptr;      // tree mode: node counts [B]
+  const int32_t* parents = nullptr;        // tree mode
+  const float* temperature = nullptr;
+  const float* uniforms = nullptr;
+  const float* uniforms_resample = nullptr;
+  int B = 0, K = 0, V = 0;
+  int32_t* accepted_len = nullptr;
+  int32_t* out_tokens = nullptr;
+  int32_t* path_nodes = nullptr;           // tree mode
+  void* workspace = nullptr;
+  size_t workspace_bytes = 0;
+  float* row_stats = nullptr;
+};
+
+bool ok4(const void* p) { return p == nullptr || reinterpret_cast<uintptr_t>(p) % 4 == 0; }
+
+specv_status launch_call(const Call& c, cudaStream_t stream) {
+  const int mode = c.mode;
+  const int B = c.B, K = c.K, V = c.V;
+  const specv_dtype dtype = c.dtype;
+  const bool tree = mode == kModeTree, sample = mode == kModeSample;
+  // required pointers per mode
+  if (!c.target || !c.out_tokens || !c.workspace) return SPECV_ERR_INVALID_ARG;
+  if (!sample && (!c.draft_tokens || !c.accepted_len)) return SPECV_ERR_INVALID_ARG;
+  if (!tree && (!c.temperature || !c.uniforms)) return SPECV_ERR_INVALID_ARG;
+  if ((mode == kModeVerify || mode == kModeOnehot) && !c.uniforms_resample)
     return SPECV_ERR_INVALID_ARG;
+  if (tree && (!c.parents || !c.draft_len || !c.path_nodes)) return SPECV_ERR_INVALID_ARG;
   if (dtype != SPECV_F32 && dtype != SPECV_BF16) return SPECV_ERR_INVALID_ARG;
-  if (B < 1 || K < 1 || V < 1) return SPECV_ERR_INVALID_ARG;
-  if (B > SPECV_MAX_BATCH || K > SPECV_MAX_DRAFT || V > specv_max_vocab(dtype))
+  if (B < 1 || K < (sample || tree ? 0 : 1) || V < 1) return SPECV_ERR_INVALID_ARG;
+  if (B > SPECV_MAX_BATCH || K > (tree ? kMaxTreeNodes - 1 : SPECV_MAX_DRAFT) ||
+      V > specv_max_vocab(dtype))
     return SPECV_ERR_UNSUPPORTED;
   const size_t eb = static_cast<size_t>(elt_bytes(dtype));
-  if (!aligned(target, eb) || (draft && !aligned(draft, eb)) || !aligned(draft_tokens, 4) ||
-      (draft_len && !aligned(draft_len, 4)) || !aligned(temperature, 4) ||
-      !aligned(uniforms, 4) || !aligned(uniforms_resample, 4) || !aligned(accepted_len, 4) ||
-      !aligned(out_tokens, 4) || !aligned(workspace, 256) || (row_stats && !aligned(row_stats, 4)))
+  if (!aligned(c.target, eb) || (c.draft && !aligned(c.draft, eb)) || !ok4(c.draft_tokens) ||
+      !ok4(c.draft_len) || !ok4(c.parents) || !ok4(c.temperature) || !ok4(c.uniforms) ||
+      !ok4(c.uniforms_resample) || !ok4(c.accepted_len) || !ok4(c.out_tokens) ||
+      !ok4(c.path_nodes) || !aligned(c.workspace, 256) || !ok4(c.row_stats))
     return SPECV_ERR_INVALID_ARG;
-  if (workspace_bytes < specv_workspace_bytes(B, K, V, dtype)) return SPECV_ERR_WORKSPACE;
+  if (c.workspace_bytes < ws_layout(B, K, V, dtype).total) return SPECV_ERR_WORKSPACE;
+  const void* target = c.target;
+  const void* draft = mode == kModeVerify ? c.draft : nullptr;
+  const int32_t* draft_tokens = c.draft_tokens;
+  const int32_t* draft_len = c.draft_len;
+  const float* temperature = c.temperature;
+  const float* uniforms = c.uniforms;
+  const float* uniforms_resample = c.uniforms_resample;
+  int32_t* accepted_len = c.accepted_len;
+  int32_t* out_tokens = c.out_tokens;
+  void* workspace = c.workspace;
+  float* row_stats = c.row_stats;
 
   int ctas = 0;
   if (resident_ctas_for(dtype, &ctas) != cudaSuccess || ctas < 1) return SPECV_ERR_CUDA;
@@ -2223,14 +2485,17 @@ specv_status launch(const void* target, const void* draft, specv_dtype dtype,
     P.target = static_cast<const unsigned char*>(target) + static_cast<size_t>(b0) * (K + 1) * V * eb;
     P.draft = draft ? static_cast<const unsigned char*>(draft) + static_cast<size_t>(b0) * K * V * eb
                     : nullptr;
-    P.draft_tokens = draft_tokens + static_cast<size_t>(b0) * K;
+    const size_t tok_stride = tree ? static_cast<size_t>(K + 1) : static_cast<size_t>(K);
+    P.draft_tokens = draft_tokens ? draft_tokens + static_cast<size_t>(b0) * tok_stride : nullptr;
     P.draft_len = draft_len ? draft_len + b0 : nullptr;
-    P.temperature = temperature + b0;
-    P.uniforms = uniforms + static_cast<size_t>(b0) * (K + 1);
-    P.uniforms_resample = uniforms_resample + b0;
+    P.parents = c.parents ? c.parents + static_cast<size_t>(b0) * (K + 1) : nullptr;
+    P.temperature = temperature ? temperature + b0 : nullptr;
+    P.uniforms = uniforms ? uniforms + static_cast<size_t>(b0) * (K + 1) : nullptr;
+    P.uniforms_resample = uniforms_resample ? uniforms_resample + b0 : nullptr;
     P.B = Bl;
     P.K = K;
     P.V = V;
+    P.mode = mode;
     P.R = 2 * K + 1;
     P.NC = chunks_per_row(V, dtype, kChunkBytes);
     P.NCd = chunks_per_row(V, dtype, kDrawBytes);
@@ -2241,19 +2506,47 @@ specv_status launch(const void* target, const void* draft, specv_dtype dtype,
     P.t_hi = down16(t0 + static_cast<size_t>(Bl) * (K + 1) * V * eb);
     P.d_lo = draft ? up16(d0) : 0;
     P.d_hi = draft ? down16(d0 + static_cast<size_t>(Bl) * K * V * eb) : 0;
-    P.accepted_len = accepted_len + b0;
+    P.accepted_len = accepted_len ? accepted_len + b0 : nullptr;
     P.out_tokens = out_tokens + static_cast<size_t>(b0) * (K + 1);
+    P.path_nodes = c.path_nodes ? c.path_nodes + static_cast<size_t>(b0) * (K + 1) : nullptr;
     P.header = reinterpret_cast<int32_t*>(ws + L.header);
     P.req = reinterpret_cast<Req*>(ws + L.req);
     P.part = reinterpret_cast<uint2*>(ws + L.part);
     P.zx = reinterpret_cast<float*>(ws + L.zx);
     P.dpc = reinterpret_cast<float*>(ws + L.dpc);
     P.row_stats = row_stats ? row_stats + static_cast<size_t>(b0) * (K + 1) * 8 : nullptr;
-    const cudaError_t e = dtype == SPECV_BF16 ? launch_sequence<SPECV_BF16>(P, grid, stream)
-                                              : launch_sequence<SPECV_F32>(P, grid, stream);
+    const cudaError_t e = dtype == SPECV_BF16 ? launch_sequence<SPECV_BF16>(P, grid, tree, stream)
+                                              : launch_sequence<SPECV_F32>(P, grid, tree, stream);
     if (e != cudaSuccess) return SPECV_ERR_CUDA;
   }
   return SPECV_OK;
+}
+
+specv_status launch(const void* target, const void* draft, specv_dtype dtype,
+                    const int32_t* draft_tokens, const int32_t* draft_len,
+                    const float* temperature, const float* uniforms,
+                    const float* uniforms_resample, int B, int K, int V, int32_t* accepted_len,
+                    int32_t* out_tokens, void* workspace, size_t workspace_bytes,
+                    float* row_stats, cudaStream_t stream) {
+  Call c;
+  c.mode = kModeVerify;
+  c.target = target;
+  c.draft = draft;
+  c.dtype = dtype;
+  c.draft_tokens = draft_tokens;
+  c.draft_len = draft_len;
+  c.temperature = temperature;
+  c.uniforms = uniforms;
+  c.uniforms_resample = uniforms_resample;
+  c.B = B;
+  c.K = K;
+  c.V = V;
+  c.accepted_len = accepted_len;
+  c.out_tokens = out_tokens;
+  c.workspace = workspace;
+  c.workspace_bytes = workspace_bytes;
+  c.row_stats = row_stats;
+  return launch_call(c, stream);
 }
 
 size_t pad256(size_t x) { return align256(x); }
@@ -2442,6 +2735,112 @@ specv_status specv_launch_plan(int B, int K, int V, specv_dtype dtype, int with_
   out[4] = kRingBytes;
   out[5] = kThreads;
   return SPECV_OK;
+}
+
+size_t specv_sample_workspace_bytes(int R, int V, specv_dtype dtype) {
+  if (R < 1 || V < 1 || R > SPECV_MAX_BATCH || (dtype != SPECV_F32 && dtype != SPECV_BF16) ||
+      V > specv_max_vocab(dtype))
+    return 0;
+  return ws_layout(R, 0, V, dtype).total;
+}
+
+specv_status spec_sample_draft(const void* logits, specv_dtype dtype, const float* temperature,
+                               const float* uniforms, int R, int V, int32_t* tokens,
+                               void* workspace, size_t workspace_bytes, float* row_stats,
+                               specv_stream_t stream) {
+  Call c;
+  c.mode = kModeSample;
+  c.target = logits;
+  c.dtype = dtype;
+  c.temperature = temperature;
+  c.uniforms = uniforms;
+  c.B = R;
+  c.K = 0;
+  c.V = V;
+  c.out_tokens = tokens;
+  c.workspace = workspace;
+  c.workspace_bytes = workspace_bytes;
+  c.row_stats = row_stats;
+  return launch_call(c, reinterpret_cast<cudaStream_t>(stream));
+}
+
+specv_status spec_verify_sample_onehot(const void* target_logits, specv_dtype dtype,
+                                       const int32_t* draft_tokens, const int32_t* draft_len,
+                                       const float* temperature, const float* uniforms,
+                                       const float* uniforms_resample, int B, int K, int V,
+                                       int32_t* accepted_len, int32_t* out_tokens,
+                                       void* workspace, size_t workspace_bytes,
+                                       float* row_stats, specv_stream_t stream) {
+  Call c;
+  c.mode = kModeOnehot;
+  c.target = target_logits;
+  c.dtype = dtype;
+  c.draft_tokens = draft_tokens;
+  c.draft_len = draft_len;
+  c.temperature = temperature;
+  c.uniforms = uniforms;
+  c.uniforms_resample = uniforms_resample;
+  c.B = B;
+  c.K = K;
+  c.V = V;
+  c.accepted_len = accepted_len;
+  c.out_tokens = out_tokens;
+  c.workspace = workspace;
+  c.workspace_bytes = workspace_bytes;
+  c.row_stats = row_stats;
+  return launch_call(c, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t specv_tree_workspace_bytes(int B, int N, int V, specv_dtype dtype) {
+  if (B < 1 || N < 1 || V < 1 || B > SPECV_MAX_BATCH || N > kMaxTreeNodes ||
+      (dtype != SPECV_F32 && dtype != SPECV_BF16) || V > specv_max_vocab(dtype))
+    return 0;
+  return ws_layout(B, N - 1, V, dtype).total;
+}
+
+specv_status spec_verify_tree_greedy(const void* target_logits, specv_dtype dtype,
+                                     const int32_t* parents, const int32_t* tokens,
+                                     const int32_t* n_nodes, int B, int N, int V,
+                                     int32_t* accepted_len, int32_t* out_tokens,
+                                     int32_t* path_nodes, void* workspace,
+                                     size_t workspace_bytes, float* row_stats,
+                                     specv_stream_t stream) {
+  if (N < 1) return SPECV_ERR_INVALID_ARG;
+  Call c;
+  c.mode = kModeTree;
+  c.target = target_logits;
+  c.dtype = dtype;
+  c.draft_tokens = tokens;
+  c.draft_len = n_nodes;
+  c.parents = parents;
+  c.B = B;
+  c.K = N - 1;
+  c.V = V;
+  c.accepted_len = accepted_len;
+  c.out_tokens = out_tokens;
+  c.path_nodes = path_nodes;
+  c.workspace = workspace;
+  c.workspace_bytes = workspace_bytes;
+  c.row_stats = row_stats;
+  return launch_call(c, reinterpret_cast<cudaStream_t>(stream));
+}
+
+specv_status spec_insert_accepted(const int32_t* accepted_len, const int32_t* out_tokens, int B,
+                                  int K, int32_t* seq_lens, int32_t* history, int L,
+                                  int32_t* next_tokens, int32_t* cu_emitted, int32_t* packed,
+                                  int32_t* status, specv_stream_t stream) {
+  if (!accepted_len || !out_tokens || !seq_lens || !history || !next_tokens || !cu_emitted ||
+      !packed || !status)
+    return SPECV_ERR_INVALID_ARG;
+  if (B < 1 || K < 0 || L < 1) return SPECV_ERR_INVALID_ARG;
+  if (B > SPECV_MAX_BATCH || K > kMaxTreeNodes) return SPECV_ERR_UNSUPPORTED;
+  if (!ok4(accepted_len) || !ok4(out_tokens) || !ok4(seq_lens) || !ok4(history) ||
+      !ok4(next_tokens) || !ok4(cu_emitted) || !ok4(packed) || !ok4(status))
+    return SPECV_ERR_INVALID_ARG;
+  insert_kernel<<<1, kInsertThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      accepted_len, out_tokens, B, K + 1, seq_lens, history, L, next_tokens, cu_emitted, packed,
+      status);
+  return cudaGetLastError() == cudaSuccess ? SPECV_OK : SPECV_ERR_CUDA;
 }
 
 specv_status spec_verify_sample_noalloc(const void* target_logits, const void* draft_logits,

@@ -278,3 +278,64 @@ def rows_needed(inp: dict):
     n = np.full(B, K) if inp.get("draft_len") is None else np.asarray(inp["draft_len"])
     T = np.asarray(inp["temperature"])
     return int(np.sum(n + 1)), int(np.sum(np.where(T > 0, n, 0)))
+
+
+def draft_rows(seed: int, R: int, V: int, dtype: str = "bf16", *, scale: float = 3.0,
+               greedy_frac: float = 0.25, t_max: float = 1.2) -> dict:
+    """Inputs of the draft-side sampler: R rows of draft logits N(0, scale^2),
+    per-row T uniform in (0, t_max] with greedy_frac of the rows at T = 0,
+    and one uniform per row (the DeepSeek-class MTP draft step at
+    R = 512, V = 129280)."""
+    rng = np.random.default_rng(seed)
+    urng = np.random.default_rng(seed + 1000)
+    z = (scale * rng.standard_normal((R, V), dtype=np.float32))
+    logits = bf16_bits(z) if dtype == "bf16" else np.ascontiguousarray(z)
+    T = (t_max * (1.0 - uniforms24(rng, (R,)).astype(np.float64))).astype(np.float32)
+    T[rng.permutation(R)[: int(round(greedy_frac * R))]] = 0.0
+    return dict(R=R, V=V, dtype=dtype, logits=logits, temperature=T,
+                uniforms=uniforms24(urng, (R,)))
+
+
+def onehot_case(seed: int, B: int, K: int, V: int, dtype: str = "bf16", *, temperature=0.7,
+                draft_len=None, greedy_frac: float = 0.0) -> dict:
+    """Inputs of the one-hot (top-token) draft rule: target = draft + noise
+    as in random_case, and each drafted token is the draft row's own top
+    token (the draft logits are then dropped: the rule takes none)."""
+    inp = random_case(seed, B, K, V, dtype, scale=3.0, noise=1.0, temperature=temperature,
+                      draft_len=draft_len, greedy_frac=greedy_frac, draft_greedy_frac=1.0)
+    inp["draft"] = None
+    return inp
+
+
+def tree_case(seed: int, B: int, N: int, V: int, dtype: str = "bf16", *, agree: float = 0.7,
+              n_nodes=None, scale: float = 3.0) -> dict:
+    """Token trees for greedy tree verification: node i >= 1 gets a parent
+    uniform in [0, i) (random recursive trees), target logits N(0, scale^2)
+    per node.  A node's token is drafted by a draft model that, with
+    probability `agree`, scores its parent position exactly as the target
+    does and proposes its top token (lowest index); otherwise it proposes a
+    uniform token.  n_nodes: None (all N) or "random" (uniform 1..N)."""
+    rng = np.random.default_rng(seed)
+    z = scale * rng.standard_normal((B, N, V), dtype=np.float32)
+    logits = bf16_bits(z) if dtype == "bf16" else np.ascontiguousarray(z)
+    del z
+    parents = np.full((B, N), -1, np.int32)
+    for i in range(1, N):
+        parents[:, i] = rng.integers(0, i, size=B)
+    tokens = rng.integers(0, V, size=(B, N)).astype(np.int32)
+    tokens[:, 0] = 0
+    same = rng.random((B, N)) < agree
+    same[:, 0] = False
+    for b in range(B):
+        idx = np.nonzero(same[b])[0]
+        if len(idx):
+            rows = as_f32(logits[b, parents[b, idx]], dtype)   # the draft's copy of the parent rows
+            tokens[b, idx] = gumbel_draw(rng, rows, np.zeros(len(idx)))
+    if n_nodes is None:
+        nn = np.full(B, N, np.int32)
+    elif isinstance(n_nodes, str) and n_nodes == "random":
+        nn = rng.integers(1, N + 1, size=B).astype(np.int32)
+    else:
+        nn = np.broadcast_to(np.asarray(n_nodes, np.int32), (B,)).copy()
+    return dict(B=B, N=N, V=V, dtype=dtype, target=logits, parents=parents, tokens=tokens,
+                n_nodes=nn)

@@ -105,3 +105,28 @@ def test_noalloc_rejects_shapes_beyond_its_array(L):
     rc = L.spec_verify_sample_noalloc(FAKE, FAKE, 1, FAKE, FAKE, FAKE, FAKE, FAKE, B, K, V, FAKE,
                                       FAKE, None)
     assert rc == 2
+
+
+def test_new_entry_points_reject_bad_host_arguments(L):
+    # draft-side sampler: null logits, zero rows, a too-small workspace
+    assert L.spec_sample_draft(None, 1, FAKE, FAKE, 4, 100, FAKE, FAKE, 1 << 20, None, None) == 1
+    assert L.spec_sample_draft(FAKE, 1, FAKE, FAKE, 0, 100, FAKE, FAKE, 1 << 20, None, None) == 1
+    assert L.spec_sample_draft(FAKE, 1, FAKE, FAKE, 4, 100, FAKE, FAKE, 8, None, None) == 3
+    assert L.specv_sample_workspace_bytes(4, 100, 1) > 0
+    assert L.specv_sample_workspace_bytes(0, 100, 1) == 0
+    # one-hot rule: no resample uniforms, K beyond the limit
+    assert L.spec_verify_sample_onehot(FAKE, 1, FAKE, FAKE, FAKE, FAKE, None, 4, 4, 100, FAKE,
+                                       FAKE, FAKE, 1 << 20, None, None) == 1
+    assert L.spec_verify_sample_onehot(FAKE, 1, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 17, 100, FAKE,
+                                       FAKE, FAKE, 1 << 20, None, None) == 2
+    # tree: N beyond 64 nodes, no parents, workspace sizing
+    assert L.specv_tree_workspace_bytes(4, 65, 100, 1) == 0
+    assert L.specv_tree_workspace_bytes(4, 64, 100, 1) > 0
+    assert L.spec_verify_tree_greedy(FAKE, 1, FAKE, FAKE, FAKE, 4, 65, 100, FAKE, FAKE, FAKE, FAKE,
+                                     1 << 24, None, None) == 2
+    assert L.spec_verify_tree_greedy(FAKE, 1, None, FAKE, FAKE, 4, 8, 100, FAKE, FAKE, FAKE, FAKE,
+                                     1 << 24, None, None) == 1
+    # insert: null buffers, misaligned history
+    assert L.spec_insert_accepted(None, FAKE, 4, 2, FAKE, FAKE, 16, FAKE, FAKE, FAKE, FAKE, None) == 1
+    assert L.spec_insert_accepted(FAKE, FAKE, 4, 2, FAKE, FAKE + 2, 16, FAKE, FAKE, FAKE, FAKE,
+                                  None) == 1
