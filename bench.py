@@ -71,7 +71,14 @@ WORKLOAD_TEXT = {
     "dsv3_mtp": "DeepSeek-V3 MTP: B=512 K=1 V=129280 bf16, 25% T=0, else T~U(0,1.2]",
     "ragged": "long ragged: B=128 K=8 V=128256 f32, draft_len~U{1..8}, constant overlap 0.5/0.8/0.95",
     "tiny": "tiny: B=4 K=4 V=1024 f32, T=1",
+    "draft_sampler": "draft-side sampler, DeepSeek-class MTP draft step: R=512 rows V=129280 bf16, "
+                     "T~U(0,1.2], 25% T=0",
+    "onehot": "one-hot (top-token) draft verify: B=128 K=4 V=128256 bf16, T=0.7, 25% T=0",
+    "tree_greedy": "greedy token-tree verify: 32 trees x 32 nodes, V=128256 bf16",
+    "post_accept_insert": "post-accept insert: B=512 requests, K=4, history L=4096 int32",
 }
+# workloads of the steps around verification (timed by time_step_workload)
+STEP_WORKLOADS = ("draft_sampler", "onehot", "tree_greedy", "post_accept_insert")
 
 
 def parse_args():
@@ -82,7 +89,8 @@ def parse_args():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="ragged", choices=sorted(WORKLOAD_TEXT),
                     help="headline workload (the JSON line's top level)")
-    ap.add_argument("--also", default="llama3,greedy,dsv3_mtp",
+    ap.add_argument("--also", default="llama3,greedy,dsv3_mtp,draft_sampler,onehot,tree_greedy,"
+                                      "post_accept_insert",
                     help="comma-separated workloads timed in the same run ('' for none)")
     ap.add_argument("--min-region-s", type=float, default=1.0,
                     help="device time per workload over the repeated K-step regions")
@@ -522,6 +530,230 @@ def time_workload(args, torch, sv, name, dev, world, rank):
     return summary, inp, d0, ws, (acc1, out1)
 
 
+def time_graph_steps(args, torch, dev, world, step, n_copies):
+    """W eager warm-ups of step(i), then the K-step region from CUDA graphs
+    (rotating over n_copies inputs), repeated >= 5 times and ~min_region_s
+    of device time; returns (sorted region times in ms, clock summary)."""
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    K_steps = args.steps
+    stream = torch.cuda.current_stream(dev)
+    cycle = n_copies * max(1, 64 // n_copies)
+    full, rem = divmod(K_steps, cycle)
+
+    def capture(nsteps):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(nsteps):
+                step(i)
+        return g
+
+    graphs = []
+    if not args.no_graph:
+        graphs = ([capture(cycle)] * full if full else []) + ([capture(rem)] if rem else [])
+        graphs[0].replay()
+        torch.cuda.synchronize(dev)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+
+    def region():
+        barrier(torch, world)
+        torch.cuda.synchronize(dev)
+        ev0.record(stream)
+        if graphs:
+            for g in graphs:
+                g.replay()
+        else:
+            for i in range(K_steps):
+                step(i)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(torch, world)
+        return max_over_ranks(torch, world, ev0.elapsed_time(ev1), dev)
+
+    first = region()
+    reps = int(min(2000, max(5, math.ceil(args.min_region_s * 1e3 / max(first, 1e-3)))))
+    reps = int(max_over_ranks(torch, world, float(reps), dev))
+    clocks = None
+    if not args.no_clocks:
+        clocks = ClockSampler(gpu_id_for(torch, dev))
+        clocks.wait_first()
+        clocks.start()
+    times = sorted(region() for _ in range(reps))
+    if clocks:
+        clocks.stop()
+    return times, (clocks.summary() if clocks else None)
+
+
+def summarize_times(times, K_steps):
+    ms = statistics.median(times)
+
+    def pct(q):
+        return round(times[min(len(times) - 1, int(q * (len(times) - 1) + 0.5))] / K_steps, 6)
+
+    return ms / K_steps, {"min": pct(0.0), "p10": pct(0.1), "median": round(ms / K_steps, 6),
+                          "p90": pct(0.9), "max": pct(1.0), "regions": len(times),
+                          "steps_per_region": K_steps}
+
+
+def time_step_workload(args, torch, sv, name, dev, world, rank, cpu_leg):
+    """The steps around verification: the draft-side sampler, the one-hot
+    draft rule, greedy token trees, the post-accept insert.  Same timing as
+    the verification workloads; parity against the oracle in the CPU leg."""
+    from speculative_decoding_verify_sample_gb300 import synth
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    seed = rank_seed(args.seed if args.seed is not None else 7, rank)
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(dev)   # noqa: E731
+    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(dev)  # noqa: E731
+
+    def logits(a, dtype):
+        return device_inputs(torch, {"dtype": dtype, "target": a, "draft": None,
+                                     "draft_tokens": None, "draft_len": None, "temperature": None,
+                                     "uniforms": None, "uniforms_resample": None}, dev)["target"]
+
+    parity = None
+    stats = {}
+    if name == "draft_sampler":
+        d = synth.draft_rows(seed, 512, 129280, "bf16")
+        units, unit_name = d["R"], "rows/s"
+        req = d["R"] * d["V"] * 2
+        base = logits(d["logits"], "bf16")
+        n_copies = max(1, math.ceil(3 * l2 / req))
+        copies = [base] + [base.clone() for _ in range(n_copies - 1)]
+        T, U = f32(d["temperature"]), f32(d["uniforms"])
+        ws = sv.Workspace(d["R"], 0, d["V"], "bf16", dev, kind="sample")
+        tok = torch.empty(d["R"], dtype=torch.int32, device=dev)
+
+        def step(i):
+            sv.sample_draft(copies[i % n_copies], T, U, workspace=ws, tokens=tok)
+
+        def outputs():
+            return sv.sample_draft(copies[0], T, U, workspace=ws).cpu().numpy()
+
+        if cpu_leg:
+            import oracle
+            got = outputs()
+            want, flags = oracle.sample_draft(d["logits"], "bf16", d["temperature"], d["uniforms"],
+                                              nthreads=os.cpu_count() or 1)
+            mism = got != want
+            allowed = (flags & oracle.NEAR_TIE_MASK) != 0
+            parity = {"compared": d["R"], "mismatched": int(mism.sum()),
+                      "unexcused": int((mism & (~allowed | (d["temperature"] == 0))).sum())}
+    elif name == "onehot":
+        inp = synth.onehot_case(seed, 128, 4, 128256, "bf16", temperature=0.7, greedy_frac=0.25)
+        units, unit_name = inp["B"] * (inp["K"] + 1), "rows/s"
+        req = required_bytes(inp)
+        d0 = device_inputs(torch, inp, dev)
+        n_copies = max(1, math.ceil(3 * l2 / req))
+        copies = [d0["target"]] + [d0["target"].clone() for _ in range(n_copies - 1)]
+        ws = sv.Workspace(inp["B"], inp["K"], inp["V"], "bf16", dev)
+        acc = torch.empty(inp["B"], dtype=torch.int32, device=dev)
+        out = torch.empty((inp["B"], inp["K"] + 1), dtype=torch.int32, device=dev)
+
+        def step(i):
+            sv.spec_verify_sample_onehot(copies[i % n_copies], d0["draft_tokens"], d0["draft_len"],
+                                         d0["temperature"], d0["uniforms"],
+                                         d0["uniforms_resample"], workspace=ws, accepted_len=acc,
+                                         out_tokens=out)
+
+        step(0)
+        torch.cuda.synchronize(dev)
+        stats = {"acceptance": acceptance_stats(inp, acc.cpu().numpy())}
+        if cpu_leg:
+            import oracle
+            a_o, o_o, fl = oracle.verify_onehot(inp, nthreads=os.cpu_count() or 1)
+            a_g, o_g = acc.cpu().numpy(), out.cpu().numpy()
+            mism = (a_g != a_o) | np.any(o_g != o_o, axis=1)
+            allowed = (fl & oracle.NEAR_TIE_MASK) != 0
+            parity = {"compared": inp["B"], "mismatched": int(mism.sum()),
+                      "unexcused": int((mism & (~allowed | (inp["temperature"] == 0))).sum())}
+    elif name == "tree_greedy":
+        c = synth.tree_case(seed, 32, 32, 128256, "bf16")
+        units, unit_name = c["B"] * c["N"], "rows/s"
+        req = int(c["n_nodes"].sum()) * c["V"] * 2
+        base = logits(c["target"], "bf16")
+        n_copies = max(1, math.ceil(3 * l2 / req))
+        copies = [base] + [base.clone() for _ in range(n_copies - 1)]
+        par, tokn, nn = i32(c["parents"]), i32(c["tokens"]), i32(c["n_nodes"])
+        ws = sv.Workspace(c["B"], c["N"], c["V"], "bf16", dev, kind="tree")
+        acc = torch.empty(c["B"], dtype=torch.int32, device=dev)
+        out = torch.empty((c["B"], c["N"]), dtype=torch.int32, device=dev)
+        path = torch.empty((c["B"], c["N"]), dtype=torch.int32, device=dev)
+
+        def step(i):
+            sv.verify_tree_greedy(copies[i % n_copies], par, tokn, nn, workspace=ws,
+                                  accepted_len=acc, out_tokens=out, path_nodes=path)
+
+        step(0)
+        torch.cuda.synchronize(dev)
+        stats = {"acceptance": {"mean_accepted_len": round(float(acc.float().mean()), 4)}}
+        if cpu_leg:
+            import oracle
+            a_o, o_o, p_o = oracle.tree_greedy(c["target"], "bf16", c["parents"], c["tokens"],
+                                               c["n_nodes"], nthreads=os.cpu_count() or 1)
+            mism = ((acc.cpu().numpy() != a_o) | np.any(out.cpu().numpy() != o_o, axis=1)
+                    | np.any(path.cpu().numpy() != p_o, axis=1))
+            parity = {"compared": c["B"], "mismatched": int(mism.sum()), "unexcused": int(mism.sum())}
+    else:   # post_accept_insert
+        rng = np.random.default_rng(seed)
+        B, K, L = 512, 4, 4096
+        acc_h = rng.integers(0, K + 1, size=B).astype(np.int32)
+        out_h = rng.integers(0, 128256, size=(B, K + 1)).astype(np.int32)
+        seq0 = rng.integers(0, 64, size=B).astype(np.int32)
+        units, unit_name = B, "requests/s"
+        req = B * 4 + B * (K + 1) * 4 + B * 8 + B * 4 * 3 + int((acc_h + 1).sum()) * 8 + (B + 1) * 4
+        n_copies = 1
+        acc_d, out_d = i32(acc_h), i32(out_h)
+        seq_d = i32(seq0)
+        hist = torch.zeros((B, L), dtype=torch.int32, device=dev)
+        nxt = torch.empty(B, dtype=torch.int32, device=dev)
+        cu = torch.empty(B + 1, dtype=torch.int32, device=dev)
+        packed = torch.empty(B * (K + 1), dtype=torch.int32, device=dev)
+        st = torch.empty(B, dtype=torch.int32, device=dev)
+
+        def step(i):
+            # the lengths rewind every 64 steps (inside a captured graph: a
+            # device copy), so the histories never fill
+            if i % 64 == 0:
+                seq_d.fill_(0)
+            sv.insert_accepted(acc_d, out_d, seq_d, hist, next_tokens=nxt, cu_emitted=cu,
+                               packed=packed, status=st)
+
+        if cpu_leg:
+            import oracle
+            seq_d.fill_(0)
+            hist.zero_()
+            sv.insert_accepted(acc_d, out_d, seq_d, hist, next_tokens=nxt, cu_emitted=cu,
+                               packed=packed, status=st)
+            torch.cuda.synchronize(dev)
+            s_o, h_o, n_o, c_o, p_o, st_o = oracle.insert_accepted(
+                acc_h, out_h, np.zeros(B, np.int32), np.zeros((B, L), np.int32))
+            ok = (np.array_equal(hist.cpu().numpy(), h_o) and np.array_equal(nxt.cpu().numpy(), n_o)
+                  and np.array_equal(cu.cpu().numpy(), c_o)
+                  and np.array_equal(packed.cpu().numpy()[:c_o[-1]], p_o[:c_o[-1]]))
+            parity = {"compared": B, "mismatched": 0 if ok else B, "unexcused": 0 if ok else B}
+    times, clocks = time_graph_steps(args, torch, dev, world, step, n_copies)
+    ms_per_step, spread = summarize_times(times, args.steps)
+    peak, peak_src = measured_hbm_peak()
+    achieved = req / (ms_per_step / 1e3) / 1e9
+    out = {"workload": WORKLOAD_TEXT[name], "value": round(units / (ms_per_step / 1e3) * world, 1),
+           "unit": unit_name, "ms_per_step": round(ms_per_step, 6), "ms_per_step_spread": spread,
+           "required_bytes_per_step": req,
+           "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                        "frac": round(achieved / peak, 4),
+                        "peak_source": f"{peak_src} HBM copy bandwidth",
+                        "algorithmic_bytes_per_launch": req}}
+    if name == "post_accept_insert":
+        out["roofline"]["note"] = "one CTA, latency-bound: bytes moved are a few kB"
+    out.update(stats)
+    if clocks:
+        out["clocks"] = clocks
+    if parity is not None:
+        out["parity"] = parity
+    return out
+
+
 def run_ours(args, torch, world, rank, local):
     import speculative_decoding_verify_sample_gb300 as sv
 
@@ -558,6 +790,10 @@ def run_ours(args, torch, world, rank, local):
     torch.cuda.empty_cache()
     extra = {}
     for name in args.also:
+        if name in STEP_WORKLOADS:
+            extra[name] = time_step_workload(args, torch, sv, name, dev, world, rank, cpu_leg)
+            torch.cuda.empty_cache()
+            continue
         summ, inp_w, d_w, ws_w, outs_w = time_workload(args, torch, sv, name, dev, world, rank)
         if cpu_leg:
             summ["parity"] = oracle_parity(inp_w, *outs_w)
