@@ -761,6 +761,19 @@ def run_ours(args, torch, world, rank, local):
     torch.cuda.set_device(dev)
     sv.build()
     cpu_leg = rank == 0 and world == 1 and not args.no_cpu_baseline
+    if args.workload in STEP_WORKLOADS:   # one of the steps around verification, alone
+        summ = time_step_workload(args, torch, sv, args.workload, dev, world, rank, cpu_leg)
+        line = {"metric": METRIC, "value": summ["value"], "unit": summ["unit"], "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": summ["ms_per_step"],
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+                "data": "synthetic (seeded; logits generated, no model weights)",
+                "config": {"workload": summ["workload"],
+                           "required_bytes_per_step": summ["required_bytes_per_step"]},
+                "roofline": summ["roofline"], "ms_per_step_spread": summ["ms_per_step_spread"]}
+        for k in ("clocks", "parity", "acceptance"):
+            if k in summ:
+                line[k] = summ[k]
+        return line
     head, inp, d0, ws, outs = time_workload(args, torch, sv, args.workload, dev, world, rank)
     line = {
         "metric": METRIC, "value": head["value"], "unit": "rows/s", "n_gpus": world,
