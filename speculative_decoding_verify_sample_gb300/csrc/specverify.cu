@@ -78,8 +78,10 @@ static_assert(kMaxDrawChunks * 4 <= kSlotBytes, "the residual masses of one row 
 static_assert(kMaxChunks < 512, "a stats chunk index fits 9 bits");
 static_assert(kPlanMax <= 1024 && 2 * SPECV_MAX_DRAFT + 1 < 64, "a request fits 10 bits, a row 6");
 
-// workspace header words (int32 index), one 128-byte line each
-constexpr int kHStatus = 0, kHResid = 96, kHExit4 = 128, kHBonus = 160;
+// workspace header words (int32 index), one 128-byte line each: the device
+// status, and the lengths of the residual and bonus lists (the stats kernel
+// empties both lists at the start of every launch sequence)
+constexpr int kHStatus = 0, kHResid = 96, kHBonus = 160;
 constexpr int kHeaderBytes = 1024;
 static_assert((kHBonus + 1) * 4 <= kHeaderBytes, "header words fit the header");
 
@@ -1773,77 +1775,115 @@ __device__ void decide_request(const Params& P, DecideSmem& D, int b, const Deci
   write_outputs(P, b, n, -1, x_lane, lane);
 }
 
+// Whole warp: vectors jv of chunk kp that the cp.async staging skipped
+// (bit jv / 32 of `whole` clear: partly outside the chunk or the tensor's
+// aligned range) read element by element into the stage, -inf outside the
+// chunk.  Rare (a row's edges), so kept out of line.
+template <int DT>
+__device__ __noinline__ void stage_edges(const Params& P, uint4* stage, const Chunk& kp,
+                                         unsigned whole, int lane) {
+  constexpr int CH = Elt<DT>::kPerVec;
+  for (int s = 0; s < kChunkSweeps; ++s) {
+    if ((whole >> s) & 1u) continue;
+    float v[CH];
+    global_vec<DT>(kp, P.t_lo, P.t_hi, s * 32 + lane, v);
+    unsigned char* dst = reinterpret_cast<unsigned char*>(stage + s * 32 + lane);
+#pragma unroll
+    for (int q = 0; q < CH; ++q) {
+      if (DT == SPECV_BF16)
+        reinterpret_cast<unsigned short*>(dst)[q] = static_cast<unsigned short>(__float_as_uint(v[q]) >> 16);
+      else
+        reinterpret_cast<float*>(dst)[q] = v[q];
+    }
+  }
+}
+
 // Whole warp: the bonus token of listed draw r (every draft accepted):
 // the decision's chunk of target row n copied into `stage` (16-byte
-// aligned, kChunkBytes), then its sweeps walked in order until the running
-// mass of p passes the target left at the chunk.  Rounding that leaves the
-// target past the chunk's sweeps falls on the last positive one.  Writes
-// out_tokens[b, n], or -1 throughout (status bit) when nothing is drawn.
+// aligned, kChunkBytes; the token the draw leaves out, if any, set to
+// -inf there), its sweeps' masses of p summed in order, four sweeps at a
+// time, until the running total passes the target left at the chunk, then
+// the token inside that sweep.  Rounding that leaves the target past the
+// chunk's sweeps falls on the last positive one.  Writes out_tokens[b, n], or -1
+// throughout (status bit) when nothing is drawn.
 template <int DT>
 __device__ void bonus_draw(const Params& P, uint4* stage, const Req& r, int lane) {
-  constexpr int CH = Elt<DT>::kPerVec;
+  using E = Elt<DT>;
+  constexpr int CH = E::kPerVec;
   const int K = P.K, V = P.V;
   const int b = r.b, n = r.j, chunk = r.chunk;
   const float rem = r.aux;
   const float4 prm = r.prm;
   const int excl = __float_as_int(prm.y);   // a token the draw leaves out (-1: none)
   const Chunk kp = chunk_of<DT>(target_row<DT>(P, b, n), V, chunk, kChunkBytes);
+  const int e_base = -kp.off0 / E::kBytes;   // the element at stage byte 0
   // every 16-byte vector of the chunk copied at once into the staging area
-  // with cp.async; the few partly outside the chunk (row edges) are read
-  // element by element
+  // with cp.async; the few partly outside the chunk (row edges) element by
+  // element
   unsigned whole = 0u;
 #pragma unroll
   for (int s = 0; s < kChunkSweeps; ++s) {
     const int jv = s * 32 + lane;
-    const int e0 = -kp.off0 / Elt<DT>::kBytes + jv * CH;
+    const int e0 = e_base + jv * CH;
     const uintptr_t a = kp.g0 + static_cast<uintptr_t>(jv) * 16;
     const bool in = e0 >= kp.e_lo && e0 + CH <= kp.e_hi && a >= P.t_lo && a + 16 <= P.t_hi;
     if (in) cp_async16(stage + jv, reinterpret_cast<const void*>(a));
     whole |= static_cast<unsigned>(in) << s;
   }
+  if (__any_sync(0xffffffffu, whole != (1u << kChunkSweeps) - 1u)) stage_edges<DT>(P, stage, kp, whole, lane);
   cp_async_wait_all();
   __syncwarp();
-  // sweeps in order (one compact loop: it runs once per request, cold)
+  if (lane == 0 && excl >= kp.e_lo && excl < kp.e_hi) {
+    unsigned char* x = reinterpret_cast<unsigned char*>(stage) + (excl - e_base) * E::kBytes;
+    if (DT == SPECV_BF16) *reinterpret_cast<unsigned short*>(x) = 0xFF80u;
+    else *reinterpret_cast<float*>(x) = -INFINITY;
+  }
+  __syncwarp();
+  // sweeps in order, four at a time (their sums formed together), until
+  // the running mass passes the target; then the token inside the sweep
+  static_assert(kChunkSweeps % 4 == 0, "a chunk is whole groups of four sweeps");
   float acc = 0.0f, rem2 = 0.0f;
   int found = -1, last = -1;
-  float w[CH];
 #pragma unroll 1
-  for (int s = 0; s < kChunkSweeps; ++s) {
-    float v[CH];
-    if ((whole >> s) & 1u) Elt<DT>::unpack(stage[s * 32 + lane], v);
-    else global_vec<DT>(kp, P.t_lo, P.t_hi, s * 32 + lane, v);
-    float a = 0.0f;
-    const int e0 = -kp.off0 / Elt<DT>::kBytes + (s * 32 + lane) * CH;
+  for (int g = 0; g < kChunkSweeps && found < 0; g += 4) {
+    float t4[4];
 #pragma unroll
-    for (int q = 0; q < CH; ++q) {
-      w[q] = e0 + q == excl ? 0.0f : weight(v[q], 0.0f, false, prm);
-      a = __fadd_rn(a, w[q]);
+    for (int k = 0; k < 4; ++k) {
+      float v[CH];
+      E::unpack(stage[(g + k) * 32 + lane], v);
+      float a = 0.0f;
+#pragma unroll
+      for (int q = 0; q < CH; ++q) a = __fadd_rn(a, weight(v[q], 0.0f, false, prm));
+      t4[k] = a;
     }
-    const float ssum = warp_sum(a);
-    if (ssum > 0.0f) {
-      if (__fadd_rn(acc, ssum) > rem) {
-        found = s;
-        rem2 = __fsub_rn(rem, acc);
-        break;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) t4[k] = warp_sum(t4[k]);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (found >= 0) continue;
+      if (t4[k] > 0.0f) {
+        if (__fadd_rn(acc, t4[k]) > rem) {
+          found = g + k;
+          rem2 = __fsub_rn(rem, acc);
+          continue;
+        }
+        last = g + k;
       }
-      last = s;
+      acc = __fadd_rn(acc, t4[k]);
     }
-    acc = __fadd_rn(acc, ssum);
   }
   if (found < 0 && last >= 0) {   // the last positive sweep, its last positive element
     found = last;
     rem2 = INFINITY;
-    float v[CH];
-    if ((whole >> last) & 1u) Elt<DT>::unpack(stage[last * 32 + lane], v);
-    else global_vec<DT>(kp, P.t_lo, P.t_hi, last * 32 + lane, v);
-#pragma unroll
-    for (int q = 0; q < CH; ++q) {
-      const int e = -kp.off0 / Elt<DT>::kBytes + (last * 32 + lane) * CH + q;
-      w[q] = e == excl ? 0.0f : weight(v[q], 0.0f, false, prm);
-    }
   }
-  const int tok = found >= 0 ? pick_in_sweep<CH>(w, rem2, -kp.off0 / Elt<DT>::kBytes + (found * 32 + lane) * CH, lane)
-                             : -1;
+  int tok = -1;
+  if (found >= 0) {
+    float v[CH], w[CH];
+    E::unpack(stage[found * 32 + lane], v);
+#pragma unroll
+    for (int q = 0; q < CH; ++q) w[q] = weight(v[q], 0.0f, false, prm);
+    tok = pick_in_sweep<CH>(w, rem2, e_base + (found * 32 + lane) * CH, lane);
+  }
   if (P.row_stats && lane == 0)
     P.row_stats[(static_cast<size_t>(b) * (K + 1) + n) * 8 + 7] = static_cast<float>(tok);
   if (tok < 0 || tok >= V) {
@@ -2043,6 +2083,10 @@ __global__ void __launch_bounds__(kThreads, 1) stats_kernel(const Params P) {
   // calls follow each other) may still run: write nothing before it ends.
   wait_previous();
   allow_dependents();
+  if (blockIdx.x == 0 && tid == 0) {   // the lists the decisions fill start empty
+    P.header[kHResid] = 0;
+    P.header[kHBonus] = 0;
+  }
 
   Agent ag;
   ag.A = &S.ag[warp];
@@ -2091,10 +2135,12 @@ __device__ void consume_residual(const Params& P, Agent& ag, int s, const Item& 
   if (lane == 0) pr[kDrawSweeps] = t;
 }
 
-// One lane: residual item i (entry i / NCd, piece i mod NCd).
+// One lane: residual item i (entry i / NCd, piece i mod NCd).  An entry
+// past the list's B slots is read as the last slot (a decode made before
+// the list's length is known; such an item is never used).
 __device__ __forceinline__ Item residual_item(const Params& P, int i) {
   Item it;
-  const int e = i / P.NCd;
+  const int e = min(i / P.NCd, P.B - 1);
   it.kind = kItemR;
   it.c = i - e * P.NCd;
   it.n = e;
@@ -2104,15 +2150,6 @@ __device__ __forceinline__ Item residual_item(const Params& P, int i) {
   it.prm = r.prm;
   it.sT = 0.0f;
   it.x = -1;
-  return it;
-}
-
-__device__ __forceinline__ Item residual_pick_init() {
-  Item it;
-  it.kind = kItemR;
-  it.b = it.row = it.c = it.n = it.x = 0;
-  it.sT = 0.0f;
-  it.prm = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
   return it;
 }
 
@@ -2150,28 +2187,32 @@ __global__ void __launch_bounds__(kThreads, 1) residual_kernel(const Params P) {
   ag.ph = 0;
   ag.lane = lane;
   allow_dependents();
+  // The grid's warps in CTA-interleaved order (consecutive positions on
+  // different SMs): the bonus draws take positions 0, 1, ..., the residual
+  // pieces positions G - 1, G - 2, ..., so both spread over every SM.  A
+  // warp's first piece is decoded (its list entry loaded, by lane 0)
+  // together with the lists' lengths; an entry past the residual list's end
+  // is stale and never used.
+  const int G = static_cast<int>(gridDim.x) * kAgents;
+  const int pos = warp * static_cast<int>(gridDim.x) + static_cast<int>(blockIdx.x);
+  const int first = G - 1 - pos;   // the warp's pieces: first, first + G, ...
+  Item mine{};
+  if (lane == 0) mine = residual_item(P, first);
+  int base = 0, decoded = 1;       // lanes holding decoded items
   const int count = __ldcg(P.header + kHResid);
   const int nb = __ldcg(P.header + kHBonus);
   const int total = count * P.NCd;
-  const int G = static_cast<int>(gridDim.x) * kAgents;
-  const int gw = static_cast<int>(blockIdx.x) * kAgents + warp;
-  // the bonus draws first, a warp each (slot 0 of its ring as staging); the
-  // residual items go to the other warps (to every warp when the bonus
-  // draws take them all)
-  for (int k = gw; k < nb; k += G)
+  for (int k = pos; k < nb; k += G)   // a warp each, slot 0 of its ring as staging
     bonus_draw<DT>(P, reinterpret_cast<uint4*>(ag.slot(0)), load_req(P.req + (P.B - 1 - k)), lane);
-  if (gw < nb) fence_proxy_async_smem();   // staging writes before bulk copies into the slot
-  const int Gr = nb < G ? G - nb : G;
-  const int first = nb < G ? gw - nb : gw;
-  const int mine_n = first >= 0 && first < total ? (total - first + Gr - 1) / Gr : 0;
-  Item mine = residual_pick_init();
-  int base = -64;
+  if (pos < nb) fence_proxy_async_smem();   // staging writes before bulk copies into the slot
+  const int mine_n = first < total ? (total - first + G - 1) / G : 0;
   int issued = 0, consumed = 0;
   for (;;) {
     while (issued - consumed < kSlots && issued < mine_n) {
-      if (issued >= base + 32) {   // decode the next 32 of this warp's items, one per lane
+      if (issued >= base + decoded) {   // decode the next 32 of this warp's items, one per lane
         base = issued;
-        const int i = first + (base + lane) * Gr;
+        decoded = 32;
+        const int i = first + (base + lane) * G;
         if (i < total) mine = residual_item(P, i);
       }
       const Item it = residual_pick(mine, issued - base);
@@ -2220,16 +2261,6 @@ __global__ void __launch_bounds__(kDecideWarps * 32) search_kernel(const Params 
     residual_search<DT>(P, ag, e, r);
   }
   cp_async_wait_all();
-  __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    const int prev = atomicAdd(P.header + kHExit4, 1);
-    if (prev == static_cast<int>(gridDim.x) - 1) {
-      P.header[kHExit4] = 0;
-      P.header[kHResid] = 0;   // the lists are used up: empty for the next call
-      P.header[kHBonus] = 0;
-    }
-  }
 }
 
 // ---------------------------------------------------------------- post-accept insert
