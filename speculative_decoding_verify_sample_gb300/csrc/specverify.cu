@@ -298,17 +298,41 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Non-tensor TMA bulk copy global -> this CTA's shared memory.  Both
-// addresses 16-byte aligned, size a multiple of 16.
+// L2 cache policies: lines of the logits are streamed once (or read once
+// more soon after) and leave L2 first, so the small state the later kernels
+// read (chunk records, the lists, the per-request inputs) stays resident.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// Non-tensor TMA bulk copy global -> this CTA's shared memory, with L2
+// policy `pol`.  Both addresses 16-byte aligned, size a multiple of 16.
 __device__ __forceinline__ void bulk_copy_g2s(void* dst, uintptr_t src, uint32_t bytes,
-                                              uint64_t* bar) {
+                                              uint64_t* bar, uint64_t pol) {
   const unsigned long long gsrc =
       static_cast<unsigned long long>(__cvta_generic_to_global(reinterpret_cast<const void*>(src)));
   asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(smem_addr(dst)),
-      "l"(gsrc), "r"(bytes), "r"(smem_addr(bar))
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
       : "memory");
+}
+
+// An 8-byte store that L2 keeps in preference to streamed lines.
+__device__ __forceinline__ void st_keep(uint2* p, uint2 v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v2.u32 [%0], {%1, %2}, %3;" ::"l"(p), "r"(v.x), "r"(v.y),
+               "l"(pol)
+               : "memory");
+}
+__device__ __forceinline__ void st_keep(float* p, float v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(pol) : "memory");
 }
 
 // 2^x on the MUFU unit (PTX ex2.approx.ftz.f32); -inf -> +0.
@@ -1219,8 +1243,9 @@ __device__ void issue(const Params& P, Agent& ag, int s, const Item& it) {
   }
   fence_proxy_async_smem();
   mbar_arrive_expect_tx(bar, n0 + n1);
-  if (n0) bulk_copy_g2s(dst0, src0, n0, bar);
-  if (n1) bulk_copy_g2s(dst1, src1, n1, bar);
+  const uint64_t pol = l2_evict_first();
+  if (n0) bulk_copy_g2s(dst0, src0, n0, bar, pol);
+  if (n1) bulk_copy_g2s(dst1, src1, n1, bar, pol);
 }
 
 // Whole warp: copies chunk c (size CB) of target row rp, and for a residual
@@ -1239,8 +1264,9 @@ __device__ bool fetch(const Params& P, Agent& ag, int s, uintptr_t rp, uintptr_t
     const uint32_t n1 = residual ? bulk_span<DT>(kq, P.d_lo, P.d_hi, &s1) : 0u;
     fence_proxy_async_smem();
     mbar_arrive_expect_tx(bar, n0 + n1);
-    if (n0) bulk_copy_g2s(slot + (s0 - kp.g0), s0, n0, bar);
-    if (n1) bulk_copy_g2s(slot + kDraftOff + (s1 - kq.g0), s1, n1, bar);
+    const uint64_t pol = l2_evict_first();
+    if (n0) bulk_copy_g2s(slot + (s0 - kp.g0), s0, n0, bar, pol);
+    if (n1) bulk_copy_g2s(slot + kDraftOff + (s1 - kq.g0), s1, n1, bar, pol);
   }
   const bool ok = wait_slot(P, ag, s);
   fix_edges<DT>(kp, P.t_lo, P.t_hi, slot, ag.lane);
@@ -2003,11 +2029,12 @@ __device__ void consume_stats(const Params& P, Agent& ag, int s, const Item& it)
   else
     r = chunk_argmax<DT>(slot, k, lane);
   if (lane == 0) {
-    P.part[(static_cast<size_t>(it.b) * P.R + it.row) * P.NC + it.c] =
-        make_uint2(__float_as_uint(r.x), __float_as_uint(r.y));
+    const uint64_t keep = l2_evict_last();
+    st_keep(P.part + (static_cast<size_t>(it.b) * P.R + it.row) * P.NC + it.c,
+            make_uint2(__float_as_uint(r.x), __float_as_uint(r.y)), keep);
     if (it.x >= k.e_lo && it.x < k.e_hi)
-      P.zx[static_cast<size_t>(it.b) * P.R + it.row] =
-          Elt<DT>::load(slot + k.off0 + it.x * Elt<DT>::kBytes);
+      st_keep(P.zx + static_cast<size_t>(it.b) * P.R + it.row,
+              Elt<DT>::load(slot + k.off0 + it.x * Elt<DT>::kBytes), keep);
   }
 }
 
