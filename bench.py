@@ -842,7 +842,10 @@ def e2e_rate(args, torch, sv, inp, d0, dev, ws, rows_per_step, world):
         step()
     el = time.perf_counter() - t0
     el = max_over_ranks(torch, world, el, dev)
-    h2d = sum(v.numel() * v.element_size() for v in h.values() if v is not None)
+    # the library copies the logit rows the kernels read (required_bytes) and
+    # every small input array whole
+    h2d = required_bytes(inp) + sum(v.numel() * v.element_size() for k, v in h.items()
+                                    if v is not None and k not in ("target", "draft"))
     d2h = acc.numel() * 4 + out.numel() * 4
     return {"value": round(job_rate(rows_per_step, n, world, el), 1), "unit": "rows/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": n,

@@ -192,12 +192,19 @@ specv_status specv_read_device_status(void* workspace, size_t workspace_bytes, i
 size_t specv_host_staging_bytes(int B, int K, int V, specv_dtype dtype, int with_draft);
 
 /*
- * The sampler on HOST buffers: copies each input host->device with one
- * cudaMemcpyAsync into `staging` (device, specv_host_staging_bytes bytes,
- * 256-byte aligned), runs spec_verify_sample, copies accepted_len and
- * out_tokens back, and synchronises `stream` before returning.  Host buffers
- * should be page-locked for asynchronous copies.  Same shapes and readings
- * as spec_verify_sample; draft_len and draft_logits may be NULL as there.
+ * The sampler on HOST buffers: copies the inputs host->device into
+ * `staging` (device, specv_host_staging_bytes bytes, 256-byte aligned),
+ * runs spec_verify_sample, copies accepted_len and out_tokens back, and
+ * synchronises `stream` before returning.  Of the logits only the rows the
+ * kernels read cross the host link: a usable request's target rows
+ * t <= draft_len[b] and, when temperature[b] > 0, its draft rows
+ * t < draft_len[b] (adjacent rows of consecutive requests in one
+ * cudaMemcpyAsync); the other rows of `staging` keep whatever they held and
+ * are never read.  draft_len and temperature are read on the host to decide
+ * this, so they must be host-readable.  Every small input is copied whole.
+ * Host buffers should be page-locked for asynchronous copies.  Same shapes
+ * and readings as spec_verify_sample; draft_len and draft_logits may be NULL
+ * as there.
  */
 specv_status spec_verify_sample_host(const void* target_logits, const void* draft_logits,
                                      specv_dtype dtype, const int32_t* draft_tokens,

@@ -2761,8 +2761,44 @@ specv_status spec_verify_sample_host(const void* target_logits, const void* draf
   float* d_ur = reinterpret_cast<float*>(take(static_cast<size_t>(B) * 4));
   int32_t* d_acc = reinterpret_cast<int32_t*>(take(static_cast<size_t>(B) * 4));
   int32_t* d_out = reinterpret_cast<int32_t*>(take(static_cast<size_t>(B) * (K + 1) * 4));
-  bool ok = h2d(d_t, target_logits, tb);
-  if (draft_logits) ok = ok && h2d(d_d, draft_logits, db);
+  // Only the rows the kernels read cross the host link (its bandwidth bounds
+  // this entry point): a usable request's target rows t <= n_b and, when it
+  // samples, its draft rows t < n_b -- the rule the device applies to the
+  // same draft_len and temperature.  Adjacent ranges go as one copy.
+  bool ok = true;
+  {
+    const size_t row = static_cast<size_t>(V) * eb;
+    size_t t_lo = 0, t_hi = 0, d_lo = 0, d_hi = 0;   // pending ranges (bytes)
+    auto flush = [&](void* dst, const void* src, size_t lo, size_t hi) {
+      if (hi > lo)
+        ok = ok && h2d(static_cast<unsigned char*>(dst) + lo, static_cast<const unsigned char*>(src) + lo,
+                       hi - lo);
+    };
+    for (int b = 0; b < B && ok; ++b) {
+      const int n = draft_len ? draft_len[b] : K;
+      const float T = temperature[b];
+      if (n < 1 || n > K || !(T >= 0.0f) || std::isinf(T)) continue;   // flagged on the device
+      const bool sampled = T > 0.0f;
+      if (sampled && !draft_logits) continue;
+      const size_t t0 = static_cast<size_t>(b) * (K + 1) * row, t1 = t0 + static_cast<size_t>(n + 1) * row;
+      if (t0 != t_hi) {
+        flush(d_t, target_logits, t_lo, t_hi);
+        t_lo = t0;
+      }
+      t_hi = t1;
+      if (sampled) {
+        const size_t q0 = static_cast<size_t>(b) * K * row, q1 = q0 + static_cast<size_t>(n) * row;
+        if (q0 != d_hi) {
+          flush(d_d, draft_logits, d_lo, d_hi);
+          d_lo = q0;
+        }
+        d_hi = q1;
+      }
+    }
+    flush(d_t, target_logits, t_lo, t_hi);
+    if (draft_logits) flush(d_d, draft_logits, d_lo, d_hi);
+  }
+  (void)db;
   ok = ok && h2d(d_tok, draft_tokens, static_cast<size_t>(B) * K * 4);
   if (draft_len) ok = ok && h2d(d_len, draft_len, static_cast<size_t>(B) * 4);
   ok = ok && h2d(d_T, temperature, static_cast<size_t>(B) * 4);

@@ -172,6 +172,33 @@ def test_host_entry_point_matches_device():
     assert np.array_equal(acc_h.numpy(), acc_d) and np.array_equal(out_h.numpy(), out_d)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_host_entry_point_copies_only_read_rows(dtype):
+    """The host entry point copies only the rows the kernels read (target
+    rows t <= n_b, draft rows t < n_b of sampled requests).  The staging
+    buffer starts as all-ones bytes (NaN logits in either dtype), so a read
+    of any row it skipped would change the result; flagged requests (a bad
+    draft length, a negative temperature) have no rows copied at all."""
+    import torch
+    import speculative_decoding_verify_sample_gb300 as sv
+    B, K, V = 24, 6, 7000
+    inp = synth.random_case(61, B, K, V, dtype, temperature=0.9, draft_len="random",
+                            greedy_frac=0.3)
+    inp["draft_len"][3] = K + 2          # flagged: draft length outside 1..K
+    inp["temperature"][5] = -1.0         # flagged: negative temperature
+    acc_d, out_d = run_gpu(inp)
+    assert acc_d[3] == -1 and acc_d[5] == -1
+    h = {k: v.cpu().pin_memory() if v is not None else None for k, v in to_device(inp, "cpu").items()}
+    staging = sv.HostStaging(B, K, V, dtype, with_draft=True, device="cuda")
+    staging.tensor.fill_(255)
+    ws = sv.Workspace(B, K, V, dtype, "cuda")
+    acc_h, out_h = sv.spec_verify_sample_host(h["target"], h["draft"], h["draft_tokens"],
+                                              h["draft_len"], h["temperature"], h["uniforms"],
+                                              h["uniforms_resample"], staging=staging, workspace=ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(acc_h.numpy(), acc_d) and np.array_equal(out_h.numpy(), out_d)
+
+
 # ---------------------------------------------------------------- full sizes
 
 
