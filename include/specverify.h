@@ -198,9 +198,11 @@ size_t specv_host_staging_bytes(int B, int K, int V, specv_dtype dtype, int with
  * synchronises `stream` before returning.  Of the logits only the rows the
  * kernels read cross the host link: a usable request's target rows
  * t <= draft_len[b] and, when temperature[b] > 0, its draft rows
- * t < draft_len[b] (adjacent rows of consecutive requests in one
- * cudaMemcpyAsync); the other rows of `staging` keep whatever they held and
- * are never read.  draft_len and temperature are read on the host to decide
+ * t < draft_len[b].  Page-locked logits whose rows are a multiple of 16
+ * bytes (16-byte-aligned bases) are gathered by one kernel that reads the
+ * host memory through its device-visible address; other logits go as one
+ * cudaMemcpyAsync per range of adjacent rows.  The other rows of `staging`
+ * keep whatever they held and are never read.  draft_len and temperature are read on the host to decide
  * this, so they must be host-readable.  Every small input is copied whole.
  * Host buffers should be page-locked for asynchronous copies.  Same shapes
  * and readings as spec_verify_sample; draft_len and draft_logits may be NULL

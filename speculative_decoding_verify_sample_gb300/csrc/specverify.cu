@@ -2352,6 +2352,56 @@ __global__ void __launch_bounds__(kInsertThreads) insert_kernel(
   }
 }
 
+// ---------------------------------------------------------------- host gather
+
+constexpr int kGatherThreads = 512;
+
+// Copies the logit rows the kernels read from page-locked host memory
+// (device-visible at ht / hd) into the staging copies dt / dd, with 16-byte
+// loads over the host link: target rows t <= n_b and, for a sampled request
+// with draft logits, draft rows t < n_b.  Rows are row16 16-byte words (the
+// host entry point takes this path only when V * elt is a multiple of 16 and
+// every base is 16-byte aligned).  A request that the decision flags (a draft
+// length outside 1..K, a bad temperature) gets no rows.  CTA c takes row
+// slots c, c + grid, ... of the B * (2K + 1) slots, eight words per thread in
+// flight.
+__global__ void __launch_bounds__(kGatherThreads) gather_rows_kernel(
+    const uint4* __restrict__ ht, const uint4* __restrict__ hd, uint4* __restrict__ dt,
+    uint4* __restrict__ dd, const int32_t* __restrict__ draft_len,
+    const float* __restrict__ temperature, int B, int K, size_t row16) {
+  const int S = 2 * K + 1;
+  for (int r = static_cast<int>(blockIdx.x); r < B * S; r += static_cast<int>(gridDim.x)) {
+    const int b = r / S, slot = r - b * S;
+    const int n = draft_len ? draft_len[b] : K;
+    const float T = temperature[b];
+    if (n < 1 || n > K || !(T >= 0.0f) || isinf(T)) continue;
+    const uint4* src;
+    uint4* dst;
+    if (slot <= K) {
+      if (slot > n) continue;
+      const size_t off = (static_cast<size_t>(b) * (K + 1) + slot) * row16;
+      src = ht + off;
+      dst = dt + off;
+    } else {
+      const int t = slot - K - 1;
+      if (!(T > 0.0f) || hd == nullptr || t >= n) continue;
+      const size_t off = (static_cast<size_t>(b) * K + t) * row16;
+      src = hd + off;
+      dst = dd + off;
+    }
+    constexpr int kUnroll = 8;
+    size_t i = threadIdx.x;
+    for (; i + (kUnroll - 1) * kGatherThreads < row16; i += kUnroll * kGatherThreads) {
+      uint4 v[kUnroll];
+#pragma unroll
+      for (int k = 0; k < kUnroll; ++k) v[k] = __ldcs(src + i + k * kGatherThreads);
+#pragma unroll
+      for (int k = 0; k < kUnroll; ++k) dst[i + k * kGatherThreads] = v[k];
+    }
+    for (; i < row16; i += kGatherThreads) dst[i] = __ldcs(src + i);
+  }
+}
+
 // ---------------------------------------------------------------- host side
 
 
@@ -2465,6 +2515,19 @@ cudaError_t launch_sequence(const Params& P, int grid, bool decide_only, cudaStr
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// The device-visible address of page-locked host memory at p (registered
+// or allocated through CUDA), or null for pageable memory and anything
+// else: only such an address is ever read by a kernel.
+const void* mapped_host(const void* p) {
+  cudaPointerAttributes a = {};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    (void)cudaGetLastError();   // pageable memory may report an error on older runtimes
+    return nullptr;
+  }
+  if (a.type != cudaMemoryTypeHost || a.devicePointer == nullptr) return nullptr;
+  return a.devicePointer;
+}
 
 uintptr_t up16(uintptr_t x) { return (x + 15) & ~static_cast<uintptr_t>(15); }
 uintptr_t down16(uintptr_t x) { return x & ~static_cast<uintptr_t>(15); }
@@ -2764,10 +2827,17 @@ specv_status spec_verify_sample_host(const void* target_logits, const void* draf
   // Only the rows the kernels read cross the host link (its bandwidth bounds
   // this entry point): a usable request's target rows t <= n_b and, when it
   // samples, its draft rows t < n_b -- the rule the device applies to the
-  // same draft_len and temperature.  Adjacent ranges go as one copy.
+  // same draft_len and temperature.  Page-locked logits with 16-byte rows
+  // are gathered by one kernel reading host memory; otherwise each range of
+  // adjacent rows goes as one copy.
   bool ok = true;
-  {
-    const size_t row = static_cast<size_t>(V) * eb;
+  const size_t row = static_cast<size_t>(V) * eb;
+  const void* ht = mapped_host(target_logits);
+  const void* hd = draft_logits ? mapped_host(draft_logits) : nullptr;
+  const bool gather = ht && (!draft_logits || hd) && row % 16 == 0 &&
+                      aligned(ht, 16) && (!hd || aligned(hd, 16)) && aligned(d_t, 16) &&
+                      (!d_d || aligned(d_d, 16));
+  if (!gather) {
     size_t t_lo = 0, t_hi = 0, d_lo = 0, d_hi = 0;   // pending ranges (bytes)
     auto flush = [&](void* dst, const void* src, size_t lo, size_t hi) {
       if (hi > lo)
@@ -2798,13 +2868,22 @@ specv_status spec_verify_sample_host(const void* target_logits, const void* draf
     flush(d_t, target_logits, t_lo, t_hi);
     if (draft_logits) flush(d_d, draft_logits, d_lo, d_hi);
   }
-  (void)db;
   ok = ok && h2d(d_tok, draft_tokens, static_cast<size_t>(B) * K * 4);
   if (draft_len) ok = ok && h2d(d_len, draft_len, static_cast<size_t>(B) * 4);
   ok = ok && h2d(d_T, temperature, static_cast<size_t>(B) * 4);
   ok = ok && h2d(d_u, uniforms, static_cast<size_t>(B) * (K + 1) * 4);
   ok = ok && h2d(d_ur, uniforms_resample, static_cast<size_t>(B) * 4);
   if (!ok) return SPECV_ERR_CUDA;
+  if (gather) {
+    int ctas = 0;
+    if (resident_ctas_for(dtype, &ctas) != cudaSuccess || ctas < 1) return SPECV_ERR_CUDA;
+    const long long slots = static_cast<long long>(B) * (2 * K + 1);
+    const int grid = static_cast<int>(std::min<long long>(slots, 4LL * ctas));
+    gather_rows_kernel<<<grid, kGatherThreads, 0, s>>>(
+        static_cast<const uint4*>(ht), static_cast<const uint4*>(hd), static_cast<uint4*>(d_t),
+        static_cast<uint4*>(d_d), draft_len ? d_len : nullptr, d_T, B, K, row / 16);
+    if (cudaGetLastError() != cudaSuccess) return SPECV_ERR_CUDA;
+  }
   specv_status st = launch(d_t, d_d, dtype, d_tok, draft_len ? d_len : nullptr, d_T, d_u, d_ur, B,
                            K, V, d_acc, d_out, workspace, workspace_bytes, nullptr, s);
   if (st != SPECV_OK) return st;

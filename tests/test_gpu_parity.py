@@ -172,13 +172,15 @@ def test_host_entry_point_matches_device():
     assert np.array_equal(acc_h.numpy(), acc_d) and np.array_equal(out_h.numpy(), out_d)
 
 
+@pytest.mark.parametrize("pinned", [True, False])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_host_entry_point_copies_only_read_rows(dtype):
-    """The host entry point copies only the rows the kernels read (target
-    rows t <= n_b, draft rows t < n_b of sampled requests).  The staging
-    buffer starts as all-ones bytes (NaN logits in either dtype), so a read
-    of any row it skipped would change the result; flagged requests (a bad
-    draft length, a negative temperature) have no rows copied at all."""
+def test_host_entry_point_copies_only_read_rows(dtype, pinned):
+    """The host entry point moves only the rows the kernels read (target
+    rows t <= n_b, draft rows t < n_b of sampled requests): gathered by a
+    kernel from page-locked logits, copied range by range from pageable
+    ones.  The staging buffer starts as all-ones bytes (NaN logits in either
+    dtype), so a read of any row it skipped would change the result; flagged
+    requests (a bad draft length, a negative temperature) move no rows."""
     import torch
     import speculative_decoding_verify_sample_gb300 as sv
     B, K, V = 24, 6, 7000
@@ -188,7 +190,8 @@ def test_host_entry_point_copies_only_read_rows(dtype):
     inp["temperature"][5] = -1.0         # flagged: negative temperature
     acc_d, out_d = run_gpu(inp)
     assert acc_d[3] == -1 and acc_d[5] == -1
-    h = {k: v.cpu().pin_memory() if v is not None else None for k, v in to_device(inp, "cpu").items()}
+    h = {k: (v.cpu().pin_memory() if pinned else v.cpu().contiguous()) if v is not None else None
+         for k, v in to_device(inp, "cpu").items()}
     staging = sv.HostStaging(B, K, V, dtype, with_draft=True, device="cuda")
     staging.tensor.fill_(255)
     ws = sv.Workspace(B, K, V, dtype, "cuda")
