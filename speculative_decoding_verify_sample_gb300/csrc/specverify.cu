@@ -140,10 +140,16 @@ struct Params {
 };
 
 // The call's plan, built by every CTA of the stats kernel: the rows each
-// request needs (prefix sums) and its length.
+// request needs (prefix sums) and its length.  The stream takes the rows in
+// two passes: first every row but the position-0 pairs (target row 0 and
+// draft row 0 of a request with draft rows), then those pairs.  Position 0
+// is where a rejection is likeliest, and the pairs read last are the ones
+// still in L2 when the residual pass reads a rejected pair again.
 struct Plan {
-  int rb[kPlanMax + 1];       // rows before request b
+  int rb[kPlanMax + 1];       // first-pass rows before request b
+  int rb2[kPlanMax + 1];      // second-pass rows (0 or 2 per request) before request b
   uint8_t info[kPlanMax];     // draft length | 0x40 | 0x80 if the request samples (0: unusable)
+  int total1;                 // tickets of the first pass
   int total;                  // tickets: chunks of every needed row
 };
 
@@ -624,6 +630,13 @@ __device__ __forceinline__ void write_outputs(const Params& P, int b, int j, int
 
 // ---------------------------------------------------------------- plan
 
+// A usable request's rows in the two passes, packed (second << 16) | first:
+// a request with draft rows reads its position-0 pair in the second pass.
+__device__ __forceinline__ int plan_rows(const Params& P, int n, float T) {
+  const int all = request_rows(P, n, T);
+  return two_rows(P, T > 0.0f) ? ((2 << 16) | (all - 2)) : all;
+}
+
 // Whole CTA: builds the call's plan: the rows each request needs, as
 // prefix sums.  A request whose length or temperature is unusable needs no
 // rows (the decision kernel answers it).
@@ -632,11 +645,13 @@ __device__ void build_plan(const Params& P, Plan& pl, int* red) {
   const int B = P.B;
   const int per = (B + kThreads - 1) / kThreads;
   const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
+  // rows of the two passes packed as (second << 16) | first: a request has
+  // at most 2 K + 1 <= 33 rows, so the first-pass sum stays below 2^16
   int rows = 0;
   for (int b = b0; b < b1; ++b) {
     const int n = request_len(P, b);
     const float T = request_T(P, b);
-    if (!request_bad(P, n, T)) rows += request_rows(P, n, T);
+    if (!request_bad(P, n, T)) rows += plan_rows(P, n, T);
   }
   const int ir = warp_incl_scan_int(rows, lane);
   if (lane == 31) red[w] = ir;
@@ -651,13 +666,16 @@ __device__ void build_plan(const Params& P, Plan& pl, int* red) {
     const int n = request_len(P, b);
     const float T = request_T(P, b);
     const bool bad = request_bad(P, n, T) != 0;
-    pl.rb[b] = r;
+    pl.rb[b] = r & 0xFFFF;
+    pl.rb2[b] = r >> 16;
     pl.info[b] = static_cast<uint8_t>(bad ? 0 : (n | 0x40 | (T > 0.0f ? 0x80 : 0)));
-    if (!bad) r += request_rows(P, n, T);
+    if (!bad) r += plan_rows(P, n, T);
   }
   if (tid == 0) {
-    pl.rb[B] = tr;
-    pl.total = tr * P.NC;
+    pl.rb[B] = tr & 0xFFFF;
+    pl.rb2[B] = tr >> 16;
+    pl.total1 = (tr & 0xFFFF) * P.NC;
+    pl.total = ((tr & 0xFFFF) + (tr >> 16)) * P.NC;
   }
   __syncthreads();
 }
@@ -705,12 +723,16 @@ __device__ __forceinline__ Item unpack_item(uint4 e) {
 // One lane: the item of ticket t < pl.total, packed: tickets run request
 // by request, row slot by row slot, chunk by chunk.
 __device__ uint4 decode_ticket(const Params& P, const Plan& pl, int t) {
-  const int r = div_nc(P, t);
-  const int b = count_le(pl.rb, P.B, r) - 1;
-  const int slot = r - pl.rb[b];
-  const int c = t - r * P.NC;
+  const bool second = t >= pl.total1;
+  const int t2 = second ? t - pl.total1 : t;
+  const int r = div_nc(P, t2);
+  const int b = count_le(second ? pl.rb2 : pl.rb, P.B, r) - 1;
+  const int c = t2 - r * P.NC;
   const int info = pl.info[b];
   const bool sampled = (info & 0x80) != 0;
+  // the request's row slot (slots 0 and 1 are the position-0 pair of a
+  // request with draft rows, read in the second pass)
+  const int slot = second ? r - pl.rb2[b] : r - pl.rb[b] + (two_rows(P, sampled) ? 2 : 0);
   const int n = info & 0x3F;
   const float sT = sampled ? temp_scale(request_T(P, b)) : 0.0f;
   const bool both = two_rows(P, sampled);
