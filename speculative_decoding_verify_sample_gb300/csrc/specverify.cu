@@ -1483,6 +1483,24 @@ __device__ __forceinline__ DecideIn decide_inputs(const Params& P, int b) {
   return in;
 }
 
+// Warp 0, debug calls only: a sampled request's per-row statistics (lane t
+// holds row t's): M_p, S_p, ln p(x_t), M_q, S_q, ln q(x_t).
+__device__ __noinline__ void write_row_stats(float* rs, int n, bool both, float Mp, float Sp,
+                                             float lp, float Mq, float Sq, float lq, int lane) {
+  if (lane <= n) {
+    rs[lane * 8 + 0] = Mp;
+    rs[lane * 8 + 1] = Sp;
+  }
+  if (lane < n) {
+    rs[lane * 8 + 2] = lp * kLn2;
+    if (both) {
+      rs[lane * 8 + 3] = Mq;
+      rs[lane * 8 + 4] = Sq;
+      rs[lane * 8 + 5] = lq * kLn2;
+    }
+  }
+}
+
 // Warp 0: a one-hot draft rejected at j.  The replacement comes from
 // (p_j - 1{x_j})+, which is p_j with x_j removed: row j's chunk masses of p
 // (from its records, staged or in global memory), less x_j's own weight in
@@ -1490,7 +1508,7 @@ __device__ __forceinline__ DecideIn decide_inputs(const Params& P, int b) {
 // chunk and x_j excluded from the walk.  If nothing but x_j weighs (p_j(x_j)
 // = 1 in fp32, only through rounding), the draw is from p_j itself.
 template <int DT>
-__device__ void onehot_rejection(const Params& P, DecideSmem& D, int b, int j, float Mp, float Sp,
+__device__ __noinline__ void onehot_rejection(const Params& P, DecideSmem& D, int b, int j, float Mp, float Sp,
                                  float sT, float ur, bool staged, int x_lane, int lane) {
   const int NC = P.NC;
   const uint2* rec = staged ? D.rec + j * NC
@@ -1543,7 +1561,7 @@ __device__ void onehot_rejection(const Params& P, DecideSmem& D, int b, int j, f
 // then the argmax at its last node, path_nodes = 0 then the path's nodes.
 // A malformed tree (a parent not below its node, a token outside [0, V))
 // gets -1 throughout and a status bit.
-__device__ void tree_decide(const Params& P, DecideSmem& D, int b, int n, int lane) {
+__device__ __noinline__ void tree_decide(const Params& P, DecideSmem& D, int b, int n, int lane) {
   const int N = P.K + 1, V = P.V;
   const size_t o = static_cast<size_t>(b) * N;
   int bad = 0;
@@ -1771,20 +1789,7 @@ __device__ void decide_request(const Params& P, DecideSmem& D, int b, const Deci
   }
   const unsigned rej = __ballot_sync(0xffffffffu, lane < n && !accept);
   const int j = rej ? __ffs(rej) - 1 : n;
-  if (rs) {
-    if (lane <= n) {
-      rs[lane * 8 + 0] = Mp_l;
-      rs[lane * 8 + 1] = Sp_l;
-    }
-    if (lane < n) {
-      rs[lane * 8 + 2] = lp * kLn2;
-      if (both) {
-        rs[lane * 8 + 3] = Mq_l;
-        rs[lane * 8 + 4] = Sq_l;
-        rs[lane * 8 + 5] = lq * kLn2;
-      }
-    }
-  }
+  if (rs) write_row_stats(rs, n, both, Mp_l, Sp_l, lp, Mq_l, Sq_l, lq, lane);
   const float Mp = __shfl_sync(0xffffffffu, Mp_l, j);
   const float Sp = __shfl_sync(0xffffffffu, Sp_l, j);
   if (j < n && !both) {
