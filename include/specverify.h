@@ -111,7 +111,8 @@ const char* specv_status_string(specv_status status);
 
 /* Bytes of device workspace one call over B requests of up to K drafts of
  * a V-entry vocabulary needs: a header (status word, the residual and bonus
- * lists' lengths, an exit counter), one 32-byte draw record per request
+ * lists' lengths, which each launch sequence empties at its start), one
+ * 32-byte draw record per request
  * (the residual and bonus lists), one 8-byte record per (row, 6 KB chunk),
  * the drafted tokens' logits, and one 32-byte record per (listed request,
  * 3 KB piece) holding the piece's residual sweep sums and total.  Batches
