@@ -2536,7 +2536,9 @@ cudaError_t launch_sequence(const Params& P, int grid, bool decide_only, cudaStr
   e = launch_dependent(decide_kernel<DT>, P.B, kDecideWarps * 32, 0, stream, P);
   if (e != cudaSuccess || decide_only) return e;   // greedy trees list no draws
   e = launch_dependent(residual_kernel<DT>, grid, kThreads, kRingBytes, stream, P);
-  if (e != cudaSuccess) return e;
+  // only the verification rule with draft logits lists residual draws (the
+  // sampler and the one-hot rule list walks alone)
+  if (e != cudaSuccess || P.mode != kModeVerify) return e;
   return launch_dependent(search_kernel<DT>, (P.B + kDecideWarps - 1) / kDecideWarps,
                           kDecideWarps * 32, kDecideWarps * kSlotBytes, stream, P);
 }
