@@ -1,5 +1,5 @@
 // libspecverify: the speculative-decoding verification sampler for GB300
-// (sm_103a), as four kernels on the caller's stream.
+// (sm_103a), as a short chain of kernels on the caller's stream.
 //
 // The rule ("Decodificación Especulativa y EAGLE", Phase 10 - Lesson 25,
 // sections "El Concepto", "La Regla de Exactitud", "Caso codicioso"): for
@@ -8,32 +8,41 @@
 // draft is accepted draw a bonus token from p at the next position; at
 // temperature 0 compare argmax(p) with the draft instead.
 //
-// Design: four kernels on the caller's stream, each launched as a
+// Design: up to four kernels on the caller's stream, each launched as a
 // programmatic dependent so its launch and prologue overlap the previous
 // kernel's tail; each waits for the previous kernel before it writes.
 //
 //  1. stats_kernel streams every row a request needs (target rows t <= n,
 //     draft rows t < n when sampled) once from HBM with TMA bulk copies,
-//     in 6 KB chunks.  Each warp is an agent with a private ring of
-//     kSlots shared-memory slots (32 warps with one slot each: the other
-//     warps' copies and reductions hide each one's wait); warp g of the
-//     grid's G takes chunks g, g + G,
-//     g + 2 G, ... (decoded 32 at a time, one per lane).  A chunk is
-//     reduced to a record: its maximum and sum of
+//     in 6 KB chunks: first every row but the position-0 pairs, then those
+//     pairs, so that the pairs a rejection most often re-reads are the ones
+//     left in L2.  Each warp is an agent with a private ring of kSlots
+//     shared-memory slots (32 warps with one slot each: the other warps'
+//     copies and reductions hide each one's wait); warp g of the grid's G
+//     takes chunks g, g + G, g + 2 G, ... (decoded 32 at a time, one per
+//     lane).  A chunk is reduced to a record: its maximum and sum of
 //     exp((z - max)/T), or at T = 0 its maximum and lowest argmax.  The
-//     chunk holding a drafted token also records that token's logit.
+//     chunk holding a drafted token also records that token's logit.  The
+//     copies stream with an L2 evict-first policy, the records are stored
+//     evict-last.
 //  2. decide_kernel, one CTA per request, combines the records, runs the
 //     left-to-right accept test (or the greedy comparison) and writes the
 //     outputs.  A request whose drafts are all accepted gets its bonus
 //     draw's chunk here (from row n's records) and joins a bonus list; a
-//     rejected sampled request joins the residual list.
+//     rejected sampled request joins the residual list.  The sampler and
+//     the one-hot rule walk their chunk here instead, and stop after this
+//     kernel; greedy trees too.
 //  3. residual_kernel reads the rejected rows again (target and draft, in
 //     3 KB pieces) and sums (p - q)+ per piece and per 512-byte sweep.
 //     Warps of its own take the bonus draws meanwhile: the listed chunk
-//     read once more, walked sweep by sweep to the token.
+//     read once more, its sweeps summed four at a time to the token.
 //  4. search_kernel, one warp per listed request, draws its token: the
 //     piece from the piece sums, the sweep from that piece's sweep sums,
 //     the token from the sweep of both rows read again.
+//
+// Beside them: insert_kernel (the post-accept insert, one CTA) and
+// gather_rows_kernel (the host entry point's copy of the needed rows of
+// page-locked logits over the host link).
 //
 // The only waits are a warp's waits on its own bulk copies; each is
 // bounded in time and sets a status bit when it gives up.  No warp waits on
