@@ -29,9 +29,9 @@
 //     left-to-right accept test (or the greedy comparison) and writes the
 //     outputs.  A request whose drafts are all accepted gets its bonus
 //     draw's chunk here (from row n's records) and joins a bonus list; a
-//     rejected sampled request joins the residual list.  The sampler and
-//     the one-hot rule walk their chunk here instead, and stop after this
-//     kernel; greedy trees too.
+//     rejected sampled request joins the residual list.  Greedy trees stop
+//     after this kernel; the sampler and the one-hot rule after the next
+//     (they list walks only).
 //  3. residual_kernel reads the rejected rows again (target and draft, in
 //     3 KB pieces) and sums (p - q)+ per piece and per 512-byte sweep.
 //     Warps of its own take the bonus draws meanwhile: the listed chunk
@@ -1492,25 +1492,6 @@ __device__ __forceinline__ DecideIn decide_inputs(const Params& P, int b) {
   return in;
 }
 
-template <int DT>
-__device__ void bonus_draw(const Params& P, uint4* stage, const Req& r, int lane);
-
-// Warp 0, sampler and one-hot rule: the walk of chunk `chunk` of target row
-// `row` made at once (the decision's staged records, now used, as its
-// staging), instead of listed for the residual kernel.
-template <int DT>
-__device__ void walk_now(const Params& P, DecideSmem& D, int b, int row, float rem, int chunk,
-                         float Mp, int excl, float sT, int lane) {
-  Req r;
-  r.b = b;
-  r.j = row;
-  r.aux = rem;
-  r.chunk = chunk;
-  r.prm = make_float4(Mp, __int_as_float(excl), sT, 0.0f);
-  __syncwarp();
-  bonus_draw<DT>(P, reinterpret_cast<uint4*>(D.rec), r, lane);
-}
-
 // Warp 0, debug calls only: a sampled request's per-row statistics (lane t
 // holds row t's): M_p, S_p, ln p(x_t), M_q, S_q, ln q(x_t).
 __device__ __noinline__ void write_row_stats(float* rs, int n, bool both, float Mp, float Sp,
@@ -1575,8 +1556,10 @@ __device__ __noinline__ void onehot_rejection(const Params& P, DecideSmem& D, in
     write_outputs(P, b, -1, -1, x_lane, lane);
     return;
   }
-  write_outputs(P, b, j, -1, x_lane, lane);   // the walk writes the token
-  walk_now<DT>(P, D, b, j, rem, chunk, Mp, excl, sT, lane);
+  if (lane == 0)
+    store_req(P.req + (P.B - 1 - atomicAdd(P.header + kHBonus, 1)), b, j, rem, chunk,
+              make_float4(Mp, __int_as_float(excl), sT, 0.0f));
+  write_outputs(P, b, j, -1, x_lane, lane);   // the bonus walk writes the token
 }
 
 // Warp 0, tree mode: greedy verification of request b's token tree.  D.arg
@@ -1845,11 +1828,6 @@ __device__ void decide_request(const Params& P, DecideSmem& D, int b, const Deci
   if (chunk < 0) {
     if (lane == 0) atomicOr(P.header + kHStatus, SPECV_DEV_BAD_ROW);
     write_outputs(P, b, -1, -1, x_lane, lane);
-    return;
-  }
-  if (P.mode != kModeVerify) {   // the sampler, the one-hot rule: walk at once
-    write_outputs(P, b, n, -1, x_lane, lane);
-    walk_now<DT>(P, D, b, n, rem, chunk, Mp, -1, sT, lane);
     return;
   }
   if (lane == 0) {
@@ -2565,11 +2543,11 @@ cudaError_t launch_sequence(const Params& P, int grid, bool decide_only, cudaStr
   cudaError_t e = launch_dependent(stats_kernel<DT>, grid, kThreads, kRingBytes, stream, P);
   if (e != cudaSuccess) return e;
   e = launch_dependent(decide_kernel<DT>, P.B, kDecideWarps * 32, 0, stream, P);
-  // greedy trees list no draws; the sampler and the one-hot rule make their
-  // walks in the decision kernel
-  if (e != cudaSuccess || decide_only || P.mode != kModeVerify) return e;
+  if (e != cudaSuccess || decide_only) return e;   // greedy trees list no draws
   e = launch_dependent(residual_kernel<DT>, grid, kThreads, kRingBytes, stream, P);
-  if (e != cudaSuccess) return e;
+  // only the verification rule with draft logits lists residual draws (the
+  // sampler and the one-hot rule list walks alone)
+  if (e != cudaSuccess || P.mode != kModeVerify) return e;
   return launch_dependent(search_kernel<DT>, (P.B + kDecideWarps - 1) / kDecideWarps,
                           kDecideWarps * 32, kDecideWarps * kSlotBytes, stream, P);
 }
