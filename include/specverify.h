@@ -252,9 +252,9 @@ size_t specv_sample_workspace_bytes(int R, int V, specv_dtype dtype);
  *   row_stats    NULL, or [R, 8] float32: slot 0 the row maximum, 1 its
  *                normaliser sum exp((z - max)/T), 6 the drawn mass
  *                (sum of p, ~1), 7 the token; at T = 0 slots 0 and 7.
- * Enqueues three kernels per 1024 rows: those of spec_verify_sample for
- * requests with no drafts (whose bonus draw is the sample), without the
- * residual search.
+ * Enqueues two kernels per 1024 rows: the row statistics, then the
+ * decisions of spec_verify_sample for requests with no drafts, whose bonus
+ * draw (the sample) the decision kernel makes itself.
  */
 specv_status spec_sample_draft(const void* logits, specv_dtype dtype, const float* temperature,
                                const float* uniforms, int R, int V, int32_t* tokens,

@@ -29,9 +29,9 @@
 //     left-to-right accept test (or the greedy comparison) and writes the
 //     outputs.  A request whose drafts are all accepted gets its bonus
 //     draw's chunk here (from row n's records) and joins a bonus list; a
-//     rejected sampled request joins the residual list.  Greedy trees stop
-//     after this kernel; the sampler and the one-hot rule after the next
-//     (they list walks only).
+//     rejected sampled request joins the residual list.  The sampler and
+//     the one-hot rule make their walks here instead and stop after this
+//     kernel; greedy trees too.
 //  3. residual_kernel reads the rejected rows again (target and draft, in
 //     3 KB pieces) and sums (p - q)+ per piece and per 512-byte sweep.
 //     Warps of its own take the bonus draws meanwhile: the listed chunk
@@ -1492,6 +1492,26 @@ __device__ __forceinline__ DecideIn decide_inputs(const Params& P, int b) {
   return in;
 }
 
+template <int DT, int kSite>
+__device__ void bonus_draw(const Params& P, uint4* stage, const Req& r, int lane);
+
+// Warp 0, sampler and one-hot rule: the walk of chunk `chunk` of target row
+// `row` made at once (the decision's staged records, used by then, as its
+// staging) instead of listed for the residual kernel.  Only the walking
+// instance of the decision kernel has it.
+template <int DT>
+__device__ void walk_now(const Params& P, DecideSmem& D, int b, int row, float rem, int chunk,
+                         float Mp, int excl, float sT, int lane) {
+  Req r;
+  r.b = b;
+  r.j = row;
+  r.aux = rem;
+  r.chunk = chunk;
+  r.prm = make_float4(Mp, __int_as_float(excl), sT, 0.0f);
+  __syncwarp();
+  bonus_draw<DT, 1>(P, reinterpret_cast<uint4*>(D.rec), r, lane);
+}
+
 // Warp 0, debug calls only: a sampled request's per-row statistics (lane t
 // holds row t's): M_p, S_p, ln p(x_t), M_q, S_q, ln q(x_t).
 __device__ __noinline__ void write_row_stats(float* rs, int n, bool both, float Mp, float Sp,
@@ -1516,7 +1536,7 @@ __device__ __noinline__ void write_row_stats(float* rs, int n, bool both, float 
 // its chunk, pick the chunk; the request joins the bonus list with that
 // chunk and x_j excluded from the walk.  If nothing but x_j weighs (p_j(x_j)
 // = 1 in fp32, only through rounding), the draw is from p_j itself.
-template <int DT>
+template <int DT, bool kWalk>
 __device__ __noinline__ void onehot_rejection(const Params& P, DecideSmem& D, int b, int j, float Mp, float Sp,
                                  float sT, float ur, bool staged, int x_lane, int lane) {
   const int NC = P.NC;
@@ -1554,6 +1574,11 @@ __device__ __noinline__ void onehot_rejection(const Params& P, DecideSmem& D, in
   if (chunk < 0) {
     if (lane == 0) atomicOr(P.header + kHStatus, SPECV_DEV_BAD_ROW);
     write_outputs(P, b, -1, -1, x_lane, lane);
+    return;
+  }
+  if (kWalk) {
+    write_outputs(P, b, j, -1, x_lane, lane);
+    walk_now<DT>(P, D, b, j, rem, chunk, Mp, excl, sT, lane);
     return;
   }
   if (lane == 0)
@@ -1621,7 +1646,7 @@ __device__ __noinline__ void tree_decide(const Params& P, DecideSmem& D, int b, 
   }
 }
 
-template <int DT>
+template <int DT, bool kWalk>
 __device__ void decide_request(const Params& P, DecideSmem& D, int b, const DecideIn& in) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K = P.K, V = P.V, R = P.R, NC = P.NC;
@@ -1802,7 +1827,7 @@ __device__ void decide_request(const Params& P, DecideSmem& D, int b, const Deci
   const float Mp = __shfl_sync(0xffffffffu, Mp_l, j);
   const float Sp = __shfl_sync(0xffffffffu, Sp_l, j);
   if (j < n && !both) {
-    onehot_rejection<DT>(P, D, b, j, Mp, Sp, sT, ur, all_at_once, x_lane, lane);
+    onehot_rejection<DT, kWalk>(P, D, b, j, Mp, Sp, sT, ur, all_at_once, x_lane, lane);
     return;
   }
   if (j < n) {
@@ -1830,6 +1855,11 @@ __device__ void decide_request(const Params& P, DecideSmem& D, int b, const Deci
     write_outputs(P, b, -1, -1, x_lane, lane);
     return;
   }
+  if (kWalk) {
+    write_outputs(P, b, n, -1, x_lane, lane);
+    walk_now<DT>(P, D, b, n, rem, chunk, Mp, -1, sT, lane);
+    return;
+  }
   if (lane == 0) {
     store_req(P.req + (P.B - 1 - atomicAdd(P.header + kHBonus, 1)), b, n, rem, chunk,
               make_float4(Mp, __int_as_float(-1), sT, 0.0f));   // the bonus list grows down
@@ -1840,8 +1870,10 @@ __device__ void decide_request(const Params& P, DecideSmem& D, int b, const Deci
 // Whole warp: vectors jv of chunk kp that the cp.async staging skipped
 // (bit jv / 32 of `whole` clear: partly outside the chunk or the tensor's
 // aligned range) read element by element into the stage, -inf outside the
-// chunk.  Rare (a row's edges), so kept out of line.
-template <int DT>
+// chunk.  Rare (a row's edges), so kept out of line; one instance per
+// calling kernel (kSite, as bonus_draw's), so that a second caller leaves
+// the residual kernel's register allocation as it was.
+template <int DT, int kSite>
 __device__ __noinline__ void stage_edges(const Params& P, uint4* stage, const Chunk& kp,
                                          unsigned whole, int lane) {
   constexpr int CH = Elt<DT>::kPerVec;
@@ -1868,7 +1900,10 @@ __device__ __noinline__ void stage_edges(const Params& P, uint4* stage, const Ch
 // the token inside that sweep.  Rounding that leaves the target past the
 // chunk's sweeps falls on the last positive one.  Writes out_tokens[b, n], or -1
 // throughout (status bit) when nothing is drawn.
-template <int DT>
+// kSite: which kernel calls it (0 the residual kernel, 1 the decision
+// kernel's own walks), so that each kernel has its own instance and the
+// second caller leaves the residual kernel's compilation as it was.
+template <int DT, int kSite = 0>
 __device__ void bonus_draw(const Params& P, uint4* stage, const Req& r, int lane) {
   using E = Elt<DT>;
   constexpr int CH = E::kPerVec;
@@ -1892,7 +1927,7 @@ __device__ void bonus_draw(const Params& P, uint4* stage, const Req& r, int lane
     if (in) cp_async16(stage + jv, reinterpret_cast<const void*>(a));
     whole |= static_cast<unsigned>(in) << s;
   }
-  if (__any_sync(0xffffffffu, whole != (1u << kChunkSweeps) - 1u)) stage_edges<DT>(P, stage, kp, whole, lane);
+  if (__any_sync(0xffffffffu, whole != (1u << kChunkSweeps) - 1u)) stage_edges<DT, kSite>(P, stage, kp, whole, lane);
   cp_async_wait_all();
   __syncwarp();
   if (lane == 0 && excl >= kp.e_lo && excl < kp.e_hi) {
@@ -2163,7 +2198,9 @@ __global__ void __launch_bounds__(kThreads, 1) stats_kernel(const Params P) {
 
 // ---------------------------------------------------------------- decide kernel
 
-template <int DT>
+// kWalk: the sampler and the one-hot rule, whose draws are walks the
+// decision makes itself; otherwise walks and residual draws are listed.
+template <int DT, bool kWalk>
 __global__ void __launch_bounds__(kDecideWarps * 32, 4) decide_kernel(const Params P) {
   __shared__ DecideSmem D;
   // the first request's own inputs are fetched while the stats kernel runs
@@ -2173,7 +2210,7 @@ __global__ void __launch_bounds__(kDecideWarps * 32, 4) decide_kernel(const Para
   allow_dependents();
   for (; b < P.B; b += gridDim.x) {
     if (b != static_cast<int>(blockIdx.x)) in = decide_inputs(P, b);
-    decide_request<DT>(P, D, b, in);
+    decide_request<DT, kWalk>(P, D, b, in);
     __syncthreads();
   }
 }
@@ -2542,8 +2579,10 @@ template <int DT>
 cudaError_t launch_sequence(const Params& P, int grid, bool decide_only, cudaStream_t stream) {
   cudaError_t e = launch_dependent(stats_kernel<DT>, grid, kThreads, kRingBytes, stream, P);
   if (e != cudaSuccess) return e;
-  e = launch_dependent(decide_kernel<DT>, P.B, kDecideWarps * 32, 0, stream, P);
-  if (e != cudaSuccess || decide_only) return e;   // greedy trees list no draws
+  const bool walk = P.mode == kModeSample || P.mode == kModeOnehot;
+  e = walk ? launch_dependent(decide_kernel<DT, true>, P.B, kDecideWarps * 32, 0, stream, P)
+           : launch_dependent(decide_kernel<DT, false>, P.B, kDecideWarps * 32, 0, stream, P);
+  if (e != cudaSuccess || decide_only || walk) return e;   // greedy trees list no draws
   e = launch_dependent(residual_kernel<DT>, grid, kThreads, kRingBytes, stream, P);
   // only the verification rule with draft logits lists residual draws (the
   // sampler and the one-hot rule list walks alone)
