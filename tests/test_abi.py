@@ -27,6 +27,25 @@ def declared_functions():
     return sorted(set(re.findall(r"\b(spec\w+)\s*\(", text)))
 
 
+def declared_arity():
+    """Parameter count of every function the header declares."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    out = {}
+    for name, params in re.findall(r"\b(spec\w+)\s*\(([^;{]*?)\)\s*;", text):
+        params = params.strip()
+        out[name] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_signatures_match_the_header():
+    """The ctypes table passes exactly the arguments each C function takes."""
+    arity = declared_arity()
+    assert arity, "no declarations parsed"
+    for name, n in arity.items():
+        assert name in _native.SIGNATURES, name
+        assert len(_native.SIGNATURES[name][1]) == n, (name, n, len(_native.SIGNATURES[name][1]))
+
+
 def test_header_declares_expected_entry_points():
     names = declared_functions()
     for must in ("spec_verify_sample", "spec_verify_sample_debug", "spec_verify_sample_host",
