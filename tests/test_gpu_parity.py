@@ -172,9 +172,10 @@ def test_host_entry_point_matches_device():
     assert np.array_equal(acc_h.numpy(), acc_d) and np.array_equal(out_h.numpy(), out_d)
 
 
+@pytest.mark.parametrize("V", [7000, 7001])   # 7001: rows not 16-byte multiples (copies)
 @pytest.mark.parametrize("pinned", [True, False])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_host_entry_point_copies_only_read_rows(dtype, pinned):
+def test_host_entry_point_copies_only_read_rows(dtype, pinned, V):
     """The host entry point moves only the rows the kernels read (target
     rows t <= n_b, draft rows t < n_b of sampled requests): gathered by a
     kernel from page-locked logits, copied range by range from pageable
@@ -183,7 +184,7 @@ def test_host_entry_point_copies_only_read_rows(dtype, pinned):
     requests (a bad draft length, a negative temperature) move no rows."""
     import torch
     import speculative_decoding_verify_sample_gb300 as sv
-    B, K, V = 24, 6, 7000
+    B, K = 24, 6
     inp = synth.random_case(61, B, K, V, dtype, temperature=0.9, draft_len="random",
                             greedy_frac=0.3)
     inp["draft_len"][3] = K + 2          # flagged: draft length outside 1..K
