@@ -273,11 +273,13 @@ def random_case(seed: int, B: int, K: int, V: int, dtype: str = "f32", *, scale:
 
 def rows_needed(inp: dict):
     """(target rows, draft rows) the rule must stream for these inputs:
-    target rows t <= n_b for every request, draft rows t < n_b for T_b > 0."""
+    target rows t <= n_b for every request, draft rows t < n_b for T_b > 0
+    when draft logits are given (the one-hot rule has none)."""
     B, K = inp["B"], inp["K"]
     n = np.full(B, K) if inp.get("draft_len") is None else np.asarray(inp["draft_len"])
     T = np.asarray(inp["temperature"])
-    return int(np.sum(n + 1)), int(np.sum(np.where(T > 0, n, 0)))
+    rows_d = int(np.sum(np.where(T > 0, n, 0))) if inp.get("draft") is not None else 0
+    return int(np.sum(n + 1)), rows_d
 
 
 def draft_rows(seed: int, R: int, V: int, dtype: str = "bf16", *, scale: float = 3.0,
