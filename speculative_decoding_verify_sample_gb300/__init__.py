@@ -52,6 +52,8 @@ def _code(dtype):
 
 
 def workspace_bytes(B: int, K: int, V: int, dtype) -> int:
+    """Device workspace bytes spec_verify_sample needs for these sizes (0:
+    out of range)."""
     return int(lib().specv_workspace_bytes(B, K, V, _code(dtype)))
 
 
@@ -67,6 +69,7 @@ def launch_plan(B: int, K: int, V: int, dtype, with_draft: bool = True) -> dict:
 
 
 def max_vocab(dtype) -> int:
+    """The largest vocabulary the library takes for this dtype (2 MB rows)."""
     torch = _torch()
     code = SPECV_BF16 if dtype in (torch.bfloat16, "bf16") else SPECV_F32
     return int(lib().specv_max_vocab(code))
@@ -212,8 +215,10 @@ class HostStaging:
 def spec_verify_sample_host(target_logits, draft_logits, draft_tokens, draft_len, temperature,
                             uniforms, uniforms_resample, *, staging, workspace, accepted_len=None,
                             out_tokens=None, stream=None):
-    """The sampler on host (CPU, ideally pinned) tensors: the library copies
-    inputs to the device, runs, copies the outputs back and synchronises."""
+    """The sampler on host (CPU, ideally pinned) tensors: the library moves
+    the logit rows the rule reads to the device (gathered by a kernel from
+    pinned tensors, copied range by range from pageable ones) with the small
+    inputs, runs, copies the outputs back and synchronises."""
     torch = _torch()
     if target_logits.device.type != "cpu":
         raise ValueError("spec_verify_sample_host takes host tensors")
